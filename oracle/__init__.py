@@ -1,0 +1,183 @@
+"""fp64 CPU oracle of one block-diffusion denoising round.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()`` and by
+the CPU-baseline leg of ``bench.py``.  The CUDA library never imports, links or calls it,
+and it shares no code with the CUDA library.
+
+``bdlm_oracle.cpp`` holds the definitions (plain loops in fp64); this module compiles it
+with g++ and wraps it with ctypes.  ``brute.py`` holds independent NumPy formulations used
+only to pin the oracle.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bdlm_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (g++, OpenMP, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-fPIC", "-shared", "-fno-fast-math",
+               "-ffp-contract=off", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_block_attention.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P,
+                                                   ctypes.c_double, P, I, P]
+            lib.oracle_block_attention.restype = I
+            lib.oracle_attention_probs.argtypes = [I, I, I, I, I, I, P, P, P, P,
+                                                   ctypes.c_double, I, I, I, P]
+            lib.oracle_attention_probs.restype = I
+            lib.oracle_lm_head.argtypes = [I, I, I, P, P, P, I, P, I, P]
+            lib.oracle_lm_head.restype = I
+            lib.oracle_confidence_commit.argtypes = [I, I, I, P, P, ctypes.c_double,
+                                                     ctypes.c_double, P, I, P, P, P, P, P]
+            lib.oracle_confidence_commit.restype = I
+            lib.oracle_apply_commit.argtypes = [I, P, P]
+            lib.oracle_apply_commit.restype = None
+            lib.oracle_num_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def block_attention(q, k_pages, v_pages, page_table, prefix_lens, L, Hq, Hkv, D, P,
+                    sm_scale=None, seqs=None) -> np.ndarray:
+    """fp64 attention output [B, L, Hq, D]; rows of sequences not in ``seqs`` stay NaN."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_pages = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    v_pages = np.ascontiguousarray(v_pages, dtype=np.uint16)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    prefix_lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    B = prefix_lens.shape[0]
+    max_pages = page_table.shape[1]
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    out = np.full((B, L, Hq, D), np.nan, dtype=np.float64)
+    sl = None if seqs is None else np.ascontiguousarray(seqs, dtype=np.int32)
+    rc = lib.oracle_block_attention(B, L, Hq, Hkv, D, P, max_pages, _ptr(q), _ptr(k_pages),
+                                    _ptr(v_pages), _ptr(page_table), _ptr(prefix_lens),
+                                    float(sm_scale), _ptr(sl), 0 if sl is None else len(sl),
+                                    _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_block_attention: bad arguments")
+    return out
+
+
+def attention_probs(q, k_pages, page_table, prefix_lens, L, Hq, Hkv, D, P, b, i, h,
+                    sm_scale=None) -> np.ndarray:
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_pages = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    prefix_lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    out = np.zeros(int(prefix_lens[b]) + L, dtype=np.float64)
+    lib.oracle_attention_probs(L, Hq, Hkv, D, P, page_table.shape[1], _ptr(q), _ptr(k_pages),
+                               _ptr(page_table), _ptr(prefix_lens), float(sm_scale), b, i, h,
+                               _ptr(out))
+    return out
+
+
+def lm_head(hidden, w, rows, cols=None) -> np.ndarray:
+    """fp64 logits [len(rows), len(cols) or V] of the listed hidden rows."""
+    lib = _load()
+    hidden = np.ascontiguousarray(hidden, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    n_rows, H = hidden.shape
+    V = w.shape[0]
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int32)
+    nc = V if c is None else len(c)
+    out = np.empty((len(rows), nc), dtype=np.float64)
+    rc = lib.oracle_lm_head(n_rows, H, V, _ptr(hidden), _ptr(w), _ptr(rows), len(rows), _ptr(c),
+                            0 if c is None else len(c), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_lm_head: bad arguments")
+    return out
+
+
+class CommitResult:
+    def __init__(self, tok, conf, conf32, commit, near):
+        self.tok, self.conf, self.conf32, self.commit, self.near = tok, conf, conf32, commit, near
+
+
+def confidence_commit(logits, mask, threshold, temperature, blocks=None) -> CommitResult:
+    """Per-position argmax token and confidence, and the per-block commit decision."""
+    lib = _load()
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    B, L = mask.shape
+    logits = np.ascontiguousarray(logits, dtype=np.uint16).reshape(B * L, -1)
+    V = logits.shape[1]
+    tok = np.full((B, L), -1, dtype=np.int32)
+    conf = np.full((B, L), -np.inf, dtype=np.float64)
+    conf32 = np.full((B, L), -np.inf, dtype=np.float32)
+    commit = np.zeros((B, L), dtype=np.uint8)
+    near = np.zeros((B, L), dtype=np.uint8)
+    bl = None if blocks is None else np.ascontiguousarray(blocks, dtype=np.int32)
+    rc = lib.oracle_confidence_commit(B, L, V, _ptr(logits), _ptr(mask), float(threshold),
+                                      float(temperature), _ptr(bl), 0 if bl is None else len(bl),
+                                      _ptr(tok), _ptr(conf), _ptr(conf32), _ptr(commit), _ptr(near))
+    if rc != 0:
+        raise ValueError("oracle_confidence_commit: bad arguments")
+    return CommitResult(tok, conf, conf32, commit, near)
+
+
+def apply_commit(mask, commit) -> np.ndarray:
+    lib = _load()
+    m = np.ascontiguousarray(mask, dtype=np.uint8).copy()
+    c = np.ascontiguousarray(commit, dtype=np.uint8)
+    lib.oracle_apply_commit(m.size, _ptr(m), _ptr(c))
+    return m
+
+
+def round_logits_to_bf16(x64: np.ndarray) -> np.ndarray:
+    """Store fp64 logits as bf16 bits: one round-to-nearest-even (via exact float32 for
+    values whose float32 rounding does not straddle a bf16 tie; ties are resolved on the
+    fp64 value)."""
+    x64 = np.asarray(x64, dtype=np.float64)
+    # Exact RNE from fp64 to bf16: pick the two bf16 neighbours and compare distances.
+    f = x64.astype(np.float32)  # nearest float32 (RNE)
+    u = f.view(np.uint32).astype(np.uint64)
+    lo = (u & 0xFFFF0000).astype(np.uint32)
+    lo_f = lo.view(np.float32).astype(np.float64)
+    hi = (lo.astype(np.uint64) + 0x10000).astype(np.uint32)
+    hi_f = hi.view(np.float32).astype(np.float64)
+    # for negative numbers "lo" (truncated magnitude) is the larger value; distances work
+    # on magnitudes either way
+    d_lo = np.abs(x64 - lo_f)
+    d_hi = np.abs(x64 - hi_f)
+    lo_even = ((lo >> 16) & 1) == 0
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ~lo_even)
+    out = np.where(pick_hi, hi, lo) >> 16
+    return out.astype(np.uint16)

@@ -1,0 +1,261 @@
+"""Pins of the fp64 oracle against things other than itself (no GPU needed).
+
+* the hand-worked commit example (tests/golden), re-evaluated from its closed forms;
+* scipy's softmax and numpy's argmax on random bf16 logits;
+* a dense block-causal attention over a whole multi-block sequence (a different
+  formulation: one masked matrix product per head, no pages);
+* special cases: equal keys give the mean of V, one dominant key gives its V row, MHA,
+  permuted pages, softmax rows summing to one;
+* the LM head against a BLAS matrix product.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import brute
+from workloads import (f32_to_bf16_bits, bf16_bits_to_f32, make_attention, make_logits,
+                       make_mask_fixed_fraction)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "commit_worked_example.txt")
+
+
+def _closed(expr: str) -> float:
+    return float(eval(expr, {"__builtins__": {}}, {"E": math.exp}))
+
+
+def _parse_golden():
+    rows, cases = {}, []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = [p.strip() for p in line.split("|")]
+        if parts[0].startswith("row"):
+            r = int(parts[0].split()[1])
+            rows[r] = dict(logits=[float(x) for x in parts[1].split(",")], tok=int(parts[2]),
+                           conf1=float(parts[3]), conf05=float(parts[4]),
+                           closed1=parts[5], closed05=parts[6])
+        elif parts[0].startswith("case"):
+            cases.append(dict(name=parts[0].split()[1], mask=[int(c) for c in parts[1]],
+                              replace=parts[2], tau=float(parts[3]), T=float(parts[4]),
+                              commit=[int(c) for c in parts[5]]))
+    return rows, cases
+
+
+def test_golden_closed_forms_match_printed_decimals():
+    rows, _ = _parse_golden()
+    assert len(rows) == 4
+    for r in rows.values():
+        assert abs(_closed(r["closed1"]) - r["conf1"]) < 5e-7
+        assert abs(_closed(r["closed05"]) - r["conf05"]) < 5e-7
+
+
+@pytest.mark.parametrize("case", ["A", "B", "C", "D", "E"])
+def test_commit_worked_example(case):
+    rows, cases = _parse_golden()
+    c = [x for x in cases if x["name"] == case][0]
+    logits = np.array([rows[r]["logits"] for r in range(4)], dtype=np.float32)
+    closed = {r: (rows[r]["closed1"] if c["T"] == 1 else rows[r]["closed05"]) for r in range(4)}
+    toks = {r: rows[r]["tok"] for r in range(4)}
+    if c["replace"] != "-":
+        rr, vals = c["replace"].split("=")
+        logits[int(rr)] = [float(x) for x in vals.split(",")]
+        closed[int(rr)] = "1/4"
+        toks[int(rr)] = 0
+    bits = f32_to_bf16_bits(logits)
+    assert np.array_equal(bf16_bits_to_f32(bits), logits)  # exact in bf16
+    mask = np.array([c["mask"]], dtype=np.uint8)
+    res = oracle.confidence_commit(bits, mask, c["tau"], c["T"])
+    for i in range(4):
+        if mask[0, i]:
+            assert res.tok[0, i] == toks[i]
+            assert abs(res.conf[0, i] - _closed(closed[i])) <= 1e-12
+        else:
+            assert res.tok[0, i] == -1 and res.conf[0, i] == -np.inf
+    assert list(res.commit[0]) == c["commit"]
+    if case == "D":
+        assert res.near[0, 0] & 1  # conf exactly at the threshold is flagged
+    if case == "E":
+        assert res.near[0, 0] & 2 and res.near[0, 2] & 2  # confidence tie flagged
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5, 1.7])
+def test_commit_against_scipy_softmax(T):
+    rng = np.random.default_rng(7)
+    B, L, V = 6, 8, 997
+    bits = make_logits(rng, B * L, V, peak_height=(0.0, 12.0))
+    mask = make_mask_fixed_fraction(rng, B, L, 0.6)
+    res = oracle.confidence_commit(bits, mask, 0.3, T)
+    x = bf16_bits_to_f32(bits).astype(np.float64)
+    tok_ref, conf_ref = brute.confidence_scipy(x, T)
+    m = mask.reshape(-1) == 1
+    assert np.array_equal(res.tok.reshape(-1)[m], tok_ref[m])
+    np.testing.assert_allclose(res.conf.reshape(-1)[m], conf_ref[m], rtol=1e-12)
+    assert np.all(res.tok.reshape(-1)[~m] == -1)
+
+
+def test_commit_invariants_and_special_values():
+    rng = np.random.default_rng(11)
+    B, L, V = 40, 8, 513
+    bits = make_logits(rng, B * L, V, peak_height=(0.0, 30.0))
+    frac = rng.uniform(0.0, 1.0, size=B)
+    frac[:3] = 0.0  # SAVING blocks
+    mask = make_mask_fixed_fraction(rng, B, L, frac)
+    res = oracle.confidence_commit(bits, mask, 0.6, 1.0)
+    for b in range(B):
+        masked = mask[b] == 1
+        assert np.all(res.commit[b][~masked] == 0)          # commit within the mask
+        if masked.any():
+            assert res.commit[b].sum() >= 1                  # at least one per block
+            assert np.all((res.conf[b][masked] >= 1.0 / V - 1e-15) & (res.conf[b][masked] <= 1.0))
+        else:
+            assert res.commit[b].sum() == 0                  # SAVING block: nothing
+    # all-equal logits: conf is exactly 1/V, token 0
+    flat = np.full((1, 1 * 4, 300), f32_to_bf16_bits(np.float32(1.5)), dtype=np.uint16)
+    r = oracle.confidence_commit(flat.reshape(4, 300), np.ones((1, 4), np.uint8), 0.9, 1.0)
+    assert np.all(r.tok == 0) and np.allclose(r.conf, 1.0 / 300, rtol=0, atol=1e-15)
+    # one dominant logit: confidence tends to one
+    big = np.zeros((1, 50), dtype=np.float32)
+    big[0, 17] = 120.0
+    r = oracle.confidence_commit(f32_to_bf16_bits(big), np.ones((1, 1), np.uint8), 0.9, 1.0)
+    assert r.tok[0, 0] == 17 and r.conf[0, 0] == 1.0 and r.commit[0, 0] == 1
+    # ties in the logits go to the lowest vocabulary index
+    tie = np.zeros((1, 64), dtype=np.float32)
+    tie[0, [5, 9, 40]] = 3.0
+    r = oracle.confidence_commit(f32_to_bf16_bits(tie), np.ones((1, 1), np.uint8), 0.9, 1.0)
+    assert r.tok[0, 0] == 5
+
+
+def test_apply_commit():
+    mask = np.array([[1, 1, 0, 1]], np.uint8)
+    com = np.array([[0, 1, 0, 1]], np.uint8)
+    assert list(oracle.apply_commit(mask, com)[0]) == [1, 0, 0, 0]
+
+
+def _scatter_sequence(rng, n_tok, Hkv, D, P, pool_pages, k_seq, v_seq):
+    """Place one sequence's tokens into a shuffled pool; unused slots hold NaN."""
+    n_pages = (n_tok + P - 1) // P
+    ids = rng.permutation(pool_pages)[:n_pages].astype(np.int32)
+    kp = np.full((pool_pages, P, Hkv, D), 0x7FC0, np.uint16)
+    vp = np.full((pool_pages, P, Hkv, D), 0x7FC0, np.uint16)
+    for t in range(n_tok):
+        kp[ids[t // P], t % P] = k_seq[t]
+        vp[ids[t // P], t % P] = v_seq[t]
+    return kp, vp, ids
+
+
+@pytest.mark.parametrize("Hq,Hkv,L,P", [(4, 2, 3, 4), (6, 6, 4, 16), (8, 2, 5, 3)])
+def test_attention_matches_dense_block_causal(Hq, Hkv, L, P):
+    rng = np.random.default_rng(Hq * 100 + L)
+    D, n_blocks = 16, 5
+    n = L * n_blocks
+    q_seq = f32_to_bf16_bits(rng.standard_normal((n, Hq, D), dtype=np.float32))
+    k_seq = f32_to_bf16_bits(rng.standard_normal((n, Hkv, D), dtype=np.float32))
+    v_seq = f32_to_bf16_bits(rng.standard_normal((n, Hkv, D), dtype=np.float32))
+    dense = brute.dense_block_causal_attention(bf16_bits_to_f32(q_seq), bf16_bits_to_f32(k_seq),
+                                               bf16_bits_to_f32(v_seq), L, Hq, Hkv)
+    kp, vp, ids = _scatter_sequence(rng, n, Hkv, D, P, 3 * ((n + P - 1) // P), k_seq, v_seq)
+    for blk in range(n_blocks):
+        prefix = blk * L
+        kv = prefix + L
+        table = np.full((1, (n + P - 1) // P), -1, np.int32)
+        table[0, :(kv + P - 1) // P] = ids[:(kv + P - 1) // P]
+        # the cache holds only tokens < kv; later slots of the last page are poisoned
+        kpb, vpb = kp.copy(), vp.copy()
+        for t in range(kv, ((kv + P - 1) // P) * P):
+            kpb[ids[t // P], t % P] = 0x7FC0
+            vpb[ids[t // P], t % P] = 0x7FC0
+        q = q_seq[prefix:prefix + L][None]
+        out = oracle.block_attention(q, kpb, vpb, table, np.array([prefix], np.int32), L, Hq, Hkv,
+                                     D, P)
+        np.testing.assert_allclose(out[0], dense[prefix:prefix + L], rtol=1e-12, atol=1e-13)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(3)
+    Hq, Hkv, D, P, L = 8, 4, 32, 16, 4
+    # equal keys: output is the mean of V over the kv tokens
+    inp = make_attention(rng, 2, L, Hq, Hkv, D, prefix_range=(20, 37), P=P, poison=True)
+    k_eq = inp.k_ref.copy()
+    k_eq[:] = f32_to_bf16_bits(np.float32(0.25))
+    kvl = inp.kv_lens
+    out = oracle.block_attention(inp.q, k_eq, inp.v_ref, inp.page_table_ref, inp.prefix_lens, L,
+                                 Hq, Hkv, D, P)
+    for b in range(2):
+        vs = np.stack([bf16_bits_to_f32(inp.v_ref[inp.page_table_ref[b, t // P], t % P])
+                       for t in range(kvl[b])]).astype(np.float64)
+        mean = vs.mean(axis=0)  # [Hkv, D]
+        for h in range(Hq):
+            np.testing.assert_allclose(out[b, :, h, :], np.broadcast_to(mean[h // 2], (L, D)),
+                                       rtol=1e-12, atol=1e-14)
+    # one dominant key: output equals that token's V row
+    inp = make_attention(rng, 1, L, Hq, Hkv, D, prefix_range=(40, 40), P=P)
+    q = np.zeros((1, L, Hq, D), np.float32)
+    q[..., 0] = 64.0
+    k = np.zeros(inp.k_ref.shape, np.float32)
+    j = 23
+    k[inp.page_table_ref[0, j // P], j % P, :, 0] = 64.0
+    out = oracle.block_attention(f32_to_bf16_bits(q), f32_to_bf16_bits(k), inp.v_ref,
+                                 inp.page_table_ref, inp.prefix_lens, L, Hq, Hkv, D, P)
+    vj = bf16_bits_to_f32(inp.v_ref[inp.page_table_ref[0, j // P], j % P]).astype(np.float64)
+    for h in range(Hq):
+        np.testing.assert_allclose(out[0, :, h, :], np.broadcast_to(vj[h // 2], (L, D)), atol=1e-12)
+    # permuting the pool (pages and table together) changes nothing
+    inp = make_attention(rng, 3, L, Hq, Hkv, D, prefix_range=(5, 50), P=P)
+    base = oracle.block_attention(inp.q, inp.k_ref, inp.v_ref, inp.page_table_ref, inp.prefix_lens,
+                                  L, Hq, Hkv, D, P)
+    perm = rng.permutation(inp.k_ref.shape[0])
+    inv = np.argsort(perm)
+    table = np.where(inp.page_table_ref >= 0, inv[np.maximum(inp.page_table_ref, 0)], -1)
+    out = oracle.block_attention(inp.q, inp.k_ref[perm], inp.v_ref[perm], table.astype(np.int32),
+                                 inp.prefix_lens, L, Hq, Hkv, D, P)
+    assert np.array_equal(out, base)
+    # softmax rows sum to one
+    for (b, i, h) in [(0, 0, 0), (1, 3, 7), (2, 2, 5)]:
+        p = oracle.attention_probs(inp.q, inp.k_ref, inp.page_table_ref, inp.prefix_lens, L, Hq,
+                                   Hkv, D, P, b, i, h)
+        assert abs(p.sum() - 1.0) < 1e-12 and np.all(p >= 0)
+
+
+def test_attention_gqa_grouping_is_contiguous():
+    """Query head h reads KV head h // (Hq/Hkv): with distinct constant V per KV head and
+    equal keys, the output of head h is exactly that constant."""
+    rng = np.random.default_rng(5)
+    Hq, Hkv, D, P, L = 8, 2, 16, 16, 4
+    inp = make_attention(rng, 1, L, Hq, Hkv, D, prefix_range=(9, 9), P=P, poison=False)
+    v = np.zeros(inp.v_ref.shape, np.float32)
+    v[:, :, 0, :] = 1.0
+    v[:, :, 1, :] = -2.0
+    out = oracle.block_attention(inp.q, inp.k_ref, f32_to_bf16_bits(v), inp.page_table_ref,
+                                 inp.prefix_lens, L, Hq, Hkv, D, P)
+    assert np.allclose(out[0, :, :4, :], 1.0) and np.allclose(out[0, :, 4:, :], -2.0)
+
+
+def test_lm_head_against_blas():
+    rng = np.random.default_rng(9)
+    n_rows, H, V = 12, 96, 211
+    hidden = f32_to_bf16_bits(rng.standard_normal((n_rows, H), dtype=np.float32))
+    w = f32_to_bf16_bits(rng.standard_normal((V, H), dtype=np.float32) * np.float32(0.02))
+    rows = np.array([0, 3, 4, 11], np.int32)
+    out = oracle.lm_head(hidden, w, rows)
+    ref = brute.lm_head_matmul(hidden, w, rows)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+    cols = np.array([0, 7, 210, 100], np.int32)
+    sub = oracle.lm_head(hidden, w, rows, cols)
+    np.testing.assert_allclose(sub, ref[:, cols], rtol=1e-12, atol=1e-13)
+
+
+def test_round_logits_to_bf16():
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal(100000).astype(np.float32)
+    # values exact in float32 round exactly as the generator's float32 rounding does
+    assert np.array_equal(oracle.round_logits_to_bf16(x.astype(np.float64)), f32_to_bf16_bits(x))
+    # an fp64 value just above a bf16 midpoint rounds up even when float32 would tie
+    one = 1.0
+    mid = one + 2.0 ** -8          # halfway between 1 and the next bf16 (1 + 2^-7)
+    assert oracle.round_logits_to_bf16(np.array([mid]))[0] == 0x3F80          # tie -> even
+    assert oracle.round_logits_to_bf16(np.array([mid + 2.0 ** -40]))[0] == 0x3F81
+    assert oracle.round_logits_to_bf16(np.array([-(mid + 2.0 ** -40)]))[0] == 0xBF81
