@@ -1,0 +1,289 @@
+// C-ABI of the bdlm library: argument validation, the per-device workspace, TMA tensor
+// maps and kernel launches.  See include/bdlm.h for the contract of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/bdlm.h"
+#include "kernels.h"
+
+namespace {
+
+using bdlm::AttnPlan;
+using bdlm::CommitPlan;
+using bdlm::LmHeadPlan;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  int num_sms = 0;
+  int* err = nullptr;            // device error word
+  int* attn_cnt = nullptr;       // split-KV arrival counters (zero between calls)
+  size_t attn_cnt_cap = 0;
+  int* commit_cnt = nullptr;     // commit row + block counters (zero between calls)
+  size_t commit_cnt_cap = 0;
+  void* data = nullptr;          // partial results / gathered rows
+  size_t data_cap = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device(DeviceState** st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BDLM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return BDLM_ERR_UNSUPPORTED;
+  DeviceState& s = g_dev[dev];
+  if (!s.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BDLM_ERR_CUDA;
+    s.supported = (major == 10 && minor == 3);
+    s.num_sms = sms;
+    s.checked = true;
+    if (s.supported) {
+      if (cudaMalloc(&s.err, 256) != cudaSuccess) return BDLM_ERR_NOMEM;
+      if (cudaMemset(s.err, 0, 256) != cudaSuccess) return BDLM_ERR_CUDA;
+    }
+  }
+  if (!s.supported) return BDLM_ERR_UNSUPPORTED;
+  *st = &s;
+  return BDLM_OK;
+}
+
+// Grows a zero-initialised buffer; growing waits for the device to be idle first.
+int ensure(void** ptr, size_t* cap, size_t need, bool zero) {
+  if (need <= *cap) return BDLM_OK;
+  size_t n = need + need / 4 + 4096;
+  if (*ptr) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return BDLM_ERR_CUDA;
+    cudaFree(*ptr);
+    *ptr = nullptr;
+    *cap = 0;
+  }
+  if (cudaMalloc(ptr, n) != cudaSuccess) {
+    *ptr = nullptr;
+    return BDLM_ERR_NOMEM;
+  }
+  if (zero && cudaMemset(*ptr, 0, n) != cudaSuccess) return BDLM_ERR_CUDA;
+  *cap = n;
+  return BDLM_OK;
+}
+
+int get_encoder() {
+  if (g_encode) return BDLM_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return BDLM_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return BDLM_OK;
+}
+
+// bf16 tensor map, 128-byte swizzle; dims/strides innermost first, strides in bytes.
+int encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
+           const cuuint64_t* strides, const cuuint32_t* box) {
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+                        dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BDLM_OK : BDLM_ERR_INVALID;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* bdlm_status_string(int status) {
+  switch (status) {
+    case BDLM_OK: return "ok";
+    case BDLM_ERR_INVALID: return "invalid argument";
+    case BDLM_ERR_CUDA: return "CUDA error";
+    case BDLM_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case BDLM_ERR_NOMEM: return "workspace allocation failed";
+    default: return "unknown status";
+  }
+}
+
+int bdlm_device_error(int* bits_out) {
+  if (!bits_out) return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return BDLM_ERR_CUDA;
+  if (cudaMemcpy(&v, st->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BDLM_ERR_CUDA;
+  if (cudaMemset(st->err, 0, sizeof(int)) != cudaSuccess) return BDLM_ERR_CUDA;
+  *bits_out = v;
+  return BDLM_OK;
+}
+
+int bdlm_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return BDLM_ERR_CUDA;
+  cudaFree(st->attn_cnt);
+  cudaFree(st->commit_cnt);
+  cudaFree(st->data);
+  st->attn_cnt = nullptr;
+  st->commit_cnt = nullptr;
+  st->data = nullptr;
+  st->attn_cnt_cap = st->commit_cnt_cap = st->data_cap = 0;
+  return BDLM_OK;
+}
+
+int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, int L, int V,
+                           float threshold, float temperature, int32_t* tok_out,
+                           float* conf_out, uint8_t* commit_out, bdlm_stream stream) {
+  if (B < 0 || L < 1 || L > 64 || V < 1) return BDLM_ERR_INVALID;
+  if (!(temperature > 0.f) || !isfinite(temperature)) return BDLM_ERR_INVALID;
+  if (!(threshold >= 0.f && threshold <= 1.f)) return BDLM_ERR_INVALID;
+  if (B == 0) return BDLM_OK;
+  if (!logits || !mask || !tok_out || !conf_out || !commit_out) return BDLM_ERR_INVALID;
+  if (static_cast<long long>(B) * L > 0x7FFFFFFFll) return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  const CommitPlan plan = bdlm::plan_commit(B, L, V);
+  rc = ensure(reinterpret_cast<void**>(&st->commit_cnt), &st->commit_cnt_cap,
+              plan.row_cnt_bytes + plan.blk_cnt_bytes, true);
+  if (rc) return rc;
+  rc = ensure(&st->data, &st->data_cap, plan.part_bytes, false);
+  if (rc) return rc;
+  int* row_cnt = st->commit_cnt;
+  int* blk_cnt = st->commit_cnt + static_cast<size_t>(B) * L;
+  cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
+                                      conf_out, commit_out, plan,
+                                      static_cast<bdlm::CommitPartial*>(st->data), row_cnt,
+                                      blk_cnt, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
+int bdlm_apply_commit(uint8_t* mask, const uint8_t* commit, int n, bdlm_stream stream) {
+  if (n < 0) return BDLM_ERR_INVALID;
+  if (n == 0) return BDLM_OK;
+  if (!mask || !commit) return BDLM_ERR_INVALID;
+  cudaError_t e = bdlm::launch_apply_commit(mask, commit, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
+int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
+                         const bdlm_bf16* k_pages, const bdlm_bf16* v_pages,
+                         const int32_t* page_table, const int32_t* prefix_lens, int L,
+                         bdlm_bf16* out, bdlm_stream stream) {
+  if (!desc) return BDLM_ERR_INVALID;
+  const bdlm_attn_desc d = *desc;
+  if (d.B < 0 || L != d.L || d.L < 1 || d.L > 64 || d.Hq < 1 || d.Hkv < 1 ||
+      d.Hq % d.Hkv != 0 || d.Hq / d.Hkv > 16 || d.D != 128 || d.page_size != 16 ||
+      d.max_pages_per_seq < 1 || d.num_pages < 1 || !isfinite(d.sm_scale))
+    return BDLM_ERR_INVALID;
+  if (d.B == 0) return BDLM_OK;
+  if (!q || !k_pages || !v_pages || !page_table || !prefix_lens || !out) return BDLM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return BDLM_ERR_INVALID;
+  if (static_cast<long long>(d.B) * d.L * d.Hq > 0x7FFFFFFFll ||
+      static_cast<long long>(d.B) * d.max_pages_per_seq > 0x7FFFFFFFll ||
+      static_cast<long long>(d.max_pages_per_seq) * d.page_size > 0x7FFFFFFFll)
+    return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  if ((rc = get_encoder())) return rc;
+  const AttnPlan plan = bdlm::plan_attention(d.B, d.L, d.Hq, d.Hkv, d.max_pages_per_seq,
+                                             d.page_size);
+  if (plan.n_mma == 0) return BDLM_ERR_UNSUPPORTED;
+  rc = ensure(reinterpret_cast<void**>(&st->attn_cnt), &st->attn_cnt_cap, plan.cnt_bytes, true);
+  if (rc) return rc;
+  rc = ensure(&st->data, &st->data_cap, plan.part_bytes, false);
+  if (rc) return rc;
+  // q viewed as [B*L rows][Hq heads][D]; box = 64 dims x G heads x lsub rows
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(d.Hq), static_cast<cuuint64_t>(d.B) * d.L};
+    cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(d.Hq) * 256};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(plan.G), static_cast<cuuint32_t>(plan.lsub)};
+    if ((rc = encode(&tm_q, q, 3, dims, strides, box))) return rc;
+  }
+  {
+    // pools viewed as [num_pages][page_size][Hkv][D]; box = 64 dims x 1 head x 16 slots
+    cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(d.Hkv), 16,
+                          static_cast<cuuint64_t>(d.num_pages)};
+    cuuint64_t strides[3] = {256, static_cast<cuuint64_t>(d.Hkv) * 256,
+                             static_cast<cuuint64_t>(d.Hkv) * 256 * 16};
+    cuuint32_t box[4] = {64, 1, 16, 1};
+    if ((rc = encode(&tm_k, k_pages, 4, dims, strides, box))) return rc;
+    if ((rc = encode(&tm_v, v_pages, 4, dims, strides, box))) return rc;
+  }
+  const float scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / sqrtf(128.0f);
+  cudaError_t e = bdlm::launch_attention(tm_q, tm_k, tm_v, page_table, prefix_lens, out, d.B,
+                                         d.L, d.Hq, d.Hkv, d.max_pages_per_seq, d.num_pages,
+                                         scale, plan, static_cast<float*>(st->data),
+                                         st->attn_cnt, st->err,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
+int bdlm_lm_head(const bdlm_bf16* hidden, const bdlm_bf16* w, const int32_t* active_idx,
+                 int n_active, int n_rows, int H, int V, bdlm_bf16* logits, bdlm_stream stream) {
+  if (n_active < 0 || n_rows < 0 || H < 8 || V < 8 || H % 8 != 0 || V % 8 != 0 ||
+      n_active > n_rows)
+    return BDLM_ERR_INVALID;
+  if (n_active == 0) return BDLM_OK;
+  if (!hidden || !w || !active_idx || !logits) return BDLM_ERR_INVALID;
+  if (!aligned16(hidden) || !aligned16(w)) return BDLM_ERR_INVALID;
+  if (static_cast<long long>(n_rows) * V > (1ll << 40)) return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  if ((rc = get_encoder())) return rc;
+  const LmHeadPlan plan = bdlm::plan_lm_head(n_active, H, V, st->num_sms);
+  rc = ensure(&st->data, &st->data_cap, plan.gather_bytes, false);
+  if (rc) return rc;
+  uint16_t* gathered = static_cast<uint16_t*>(st->data);
+  CUtensorMap tm_w, tm_h;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(V)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, 128};
+    if ((rc = encode(&tm_w, w, 2, dims, strides, box))) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n_active)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(plan.bn)};
+    if ((rc = encode(&tm_h, gathered, 2, dims, strides, box))) return rc;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = bdlm::launch_gather_rows(hidden, active_idx, n_active, n_rows, H, gathered,
+                                           st->err, s);
+  if (e != cudaSuccess) return BDLM_ERR_CUDA;
+  e = bdlm::launch_lm_head(tm_w, tm_h, active_idx, n_active, n_rows, H, V, logits, plan, st->err,
+                           s);
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/bdlm.h"
+
+namespace bdlm {
+
+// ------------------------------------------------------------------ commit
+struct CommitPartial {
+  float m;
+  float s;
+  int idx;
+  int pad;
+};
+
+struct CommitPlan {
+  int S = 1;        // CTAs per logits row
+  int chunk = 0;    // elements per CTA (multiple of 8)
+  size_t part_bytes = 0, row_cnt_bytes = 0, blk_cnt_bytes = 0;
+};
+
+CommitPlan plan_commit(int B, int L, int V);
+cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
+                          float threshold, float temperature, int32_t* tok_out, float* conf_out,
+                          uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
+                          int* row_cnt, int* blk_cnt, cudaStream_t stream);
+cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
+
+// ------------------------------------------------------------------ attention
+struct AttnPlan {
+  int G = 1;             // query heads per KV head
+  int rows = 0;          // query rows of one (sequence, KV head): G * L
+  int row_groups = 1;    // CTAs splitting those rows (<= 128 rows each)
+  int lsub = 0;          // block positions per row group
+  int n_mma = 16;        // UMMA N: rows per group rounded up to a multiple of 16
+  int split_tokens = 0;  // KV tokens per split (multiple of 128)
+  int max_splits = 1;    // splits of the longest possible sequence
+  int chunk_tiles = 1;   // 128-token tiles per S chunk held in tensor memory
+  int tmem_cols = 0;     // tensor-memory columns allocated per CTA
+  size_t smem_bytes = 0;
+  size_t part_bytes = 0, cnt_bytes = 0;
+};
+
+AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size);
+cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                             const CUtensorMap& tm_v, const int32_t* page_table,
+                             const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
+                             int Hkv, int max_pages, int num_pages, float sm_scale,
+                             const AttnPlan& plan, float* part, int* cnt, int* err,
+                             cudaStream_t stream);
+
+// ------------------------------------------------------------------ LM head
+struct LmHeadPlan {
+  int bn = 256;          // UMMA N (gathered rows per tile)
+  int m_tiles = 0, n_tiles = 0, grid = 0;
+  size_t smem_bytes = 0;
+  size_t gather_bytes = 0;
+};
+
+LmHeadPlan plan_lm_head(int n_active, int H, int V, int num_sms);
+cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* active_idx, int n_active,
+                               int n_rows, int H, uint16_t* gathered, int* err,
+                               cudaStream_t stream);
+cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
+                           const int32_t* active_idx, int n_active, int n_rows, int H, int V,
+                           uint16_t* logits, const LmHeadPlan& plan, int* err,
+                           cudaStream_t stream);
+
+}  // namespace bdlm

@@ -1,0 +1,166 @@
+/*
+ * bdlm — one denoising round of block-diffusion LLM decoding on NVIDIA GB300 (sm_103a).
+ *
+ * A round (JetEngine README, "Block Diffusion Decoding"; JetEngine notes (CLAUDE.md),
+ * "Important Patterns"): every sequence of a batch holds a committed prefix in a paged
+ * KV cache and a block of L positions (L = 1..64), some of which are still masked.  One
+ * round runs block attention, the LM head for the rows still being denoised, and the
+ * confidence commit that unmasks positions; the caller then clears the committed
+ * positions from the mask (bdlm_apply_commit) and runs the next round.
+ *
+ * Conventions shared by every call:
+ *  - Pointers are DEVICE pointers on the current CUDA device, owned by the caller, unless
+ *    a parameter says otherwise.  bf16 data are raw bfloat16 bits (bdlm_bf16).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream).  A call validates its host-side arguments and returns before any launch on
+ *    error.  Faults inside a kernel surface at the caller's next synchronisation.
+ *  - Kernels never trust device-resident indices: a page id outside [0, num_pages), a
+ *    prefix length that does not fit the page table, or an out-of-range row index is
+ *    skipped (zero data / no write) and recorded in a device error word that
+ *    bdlm_device_error() reads and clears.  Every wait inside a kernel is bounded; a
+ *    wait that gives up is recorded the same way.
+ *  - Scratch (split-KV partial results, cross-CTA counters, the gathered LM-head rows)
+ *    lives in a per-device workspace that the library allocates on first need and grows
+ *    when a larger problem arrives (growing synchronises the device).  Calls that share
+ *    a device must not run concurrently on different streams: they share that
+ *    workspace.  bdlm_release() frees it.
+ *  - Return value: BDLM_OK (0) or a negative BDLM_ERR_* code; bdlm_status_string() names it.
+ */
+#ifndef BDLM_H
+#define BDLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t bdlm_bf16;  /* raw bfloat16 bits */
+typedef void* bdlm_stream;   /* cudaStream_t */
+
+enum {
+  BDLM_OK = 0,
+  BDLM_ERR_INVALID = -1,     /* bad shape, null pointer, parameter out of range */
+  BDLM_ERR_CUDA = -2,        /* a CUDA runtime call or launch failed */
+  BDLM_ERR_UNSUPPORTED = -3, /* no sm_103 device, or a shape outside the kernels' limits */
+  BDLM_ERR_NOMEM = -4        /* the workspace could not be allocated */
+};
+
+/* Device error word bits (bdlm_device_error). */
+enum {
+  BDLM_DEVERR_PAGE = 1,      /* page id outside [0, num_pages): that page read as zeros */
+  BDLM_DEVERR_LENGTH = 2,    /* prefix_len < 0 or prefix_len + L > max_pages_per_seq*P */
+  BDLM_DEVERR_TIMEOUT = 4,   /* a bounded wait inside a kernel gave up */
+  BDLM_DEVERR_ROW = 8        /* an active row index outside [0, n_rows) was skipped */
+};
+
+/*
+ * Shapes of block attention.
+ *   B                   sequences in the batch
+ *   L                   block length (1..64)
+ *   Hq, Hkv             query / KV heads; Hq % Hkv == 0, Hq/Hkv <= 16
+ *   D                   head dimension; must be 128
+ *   page_size           tokens per KV page; must be 16
+ *   max_pages_per_seq   columns of page_table
+ *   num_pages           pages in the K and V pools
+ *   sm_scale            softmax scale; <= 0 selects 1/sqrt(D)
+ */
+typedef struct {
+  int B, L, Hq, Hkv, D, page_size, max_pages_per_seq, num_pages;
+  float sm_scale;
+} bdlm_attn_desc;
+
+/*
+ * Block attention of one denoising round over the paged KV cache.
+ * Source: JetEngine notes, "ModelRunner" (paged-KV attention for denoise; the pages'
+ * engines use FlashAttention-3 / flashinfer for it) and "Important Patterns" (a block of
+ * L positions on top of the committed prefix); dlmrt page, "Highlights" (every forward
+ * denoises a whole block).
+ *
+ * For sequence b, block position i and query head h, with kv_len = prefix_lens[b] + L:
+ *     out[b,i,h,:] = softmax_j( sm_scale * q[b,i,h,:] . K_b[j, g(h), :] ) V_b[j, g(h), :]
+ * over j = 0..kv_len-1: the whole prefix plus the whole block (bidirectional inside the
+ * block), g(h) = h / (Hq/Hkv) (grouped-query attention).  Token j of sequence b is slot
+ * j % page_size of page page_table[b][j / page_size]; the block's own K/V must already
+ * sit at positions prefix_len .. prefix_len+L-1.
+ *
+ * Layouts (row-major, contiguous):
+ *   q            [B, L, Hq, D]                         bf16
+ *   k_pages      [num_pages, page_size, Hkv, D]        bf16 (16-byte aligned)
+ *   v_pages      [num_pages, page_size, Hkv, D]        bf16 (16-byte aligned)
+ *   page_table   [B, max_pages_per_seq]                int32 (unused entries are ignored)
+ *   prefix_lens  [B]                                   int32
+ *   out          [B, L, Hq, D]                         bf16 (fp32 accumulation, one rounding)
+ * `L` must equal desc->L (it is the block length of this round).
+ * Slots past kv_len in a sequence's last page are never used, whatever they hold.
+ */
+int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
+                         const bdlm_bf16* k_pages, const bdlm_bf16* v_pages,
+                         const int32_t* page_table, const int32_t* prefix_lens, int L,
+                         bdlm_bf16* out, bdlm_stream stream);
+
+/*
+ * Selective LM head.
+ * Source: JetEngine notes, "ModelRunner" (selective logits: the LM head runs only for
+ * DENOISING sequences) and "Optimization History" (opt23: LM head only on masked rows).
+ *
+ *     logits[r, v] = sum_k hidden[r, k] * w[v, k]     for r in active_idx, v in [0, V)
+ *
+ * Layouts: hidden [n_rows, H] bf16; w [V, H] bf16 (one vocabulary row per output);
+ * active_idx [n_active] int32 (distinct row ids in [0, n_rows)); logits [n_rows, V] bf16.
+ * Only the active rows of `logits` are written (fp32 accumulation, one round-to-nearest-
+ * even to bf16); other rows keep whatever they held.  H % 8 == 0, V % 8 == 0
+ * (16-byte row alignment).  n_active == 0 is a no-op.
+ */
+int bdlm_lm_head(const bdlm_bf16* hidden, const bdlm_bf16* w, const int32_t* active_idx,
+                 int n_active, int n_rows, int H, int V, bdlm_bf16* logits, bdlm_stream stream);
+
+/*
+ * Confidence and commit of one denoising step (threshold / low_confidence_dynamic rule).
+ * Source: JetEngine notes, "Remasking Strategies" (low_confidence_dynamic: unmask above a
+ * threshold); dInfer blog, "Algorithmic Innovations" (threshold decoding); SDAR page,
+ * "Reported Performance" (dynamic decoding); JetEngine README, example `SamplingParams`
+ * (temperature, dynamic_threshold).
+ *
+ * For each masked position (mask[b,i] != 0), from logits row b*L+i, in one pass:
+ *     tok_out[b,i]  = argmax_v logits[v]              (lowest index on ties)
+ *     conf_out[b,i] = 1 / sum_v exp((logits[v] - max) / temperature)   (max probability)
+ * Then per block b: commit_out[b,i] = 1 for every masked i with conf >= threshold; if no
+ * masked position reaches the threshold and the block has one, the single most confident
+ * masked position is committed (lowest i on ties).  Confidences are compared as float32.
+ * Unmasked positions get tok_out = -1, conf_out = -inf, commit_out = 0; their logits rows
+ * are never read.
+ *
+ * Layouts: logits [B*L, V] bf16 (finite in masked rows); mask, commit_out [B, L] uint8;
+ * tok_out [B, L] int32; conf_out [B, L] float.  1 <= L <= 64; V >= 1.
+ * temperature > 0; 0 <= threshold <= 1.
+ */
+int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, int L, int V,
+                           float threshold, float temperature, int32_t* tok_out,
+                           float* conf_out, uint8_t* commit_out, bdlm_stream stream);
+
+/*
+ * Mask update between denoising steps: mask[i] = 0 wherever commit[i] != 0.
+ * Source: JetEngine notes, "Important Patterns" (each denoising step moves positions from
+ * masked to unmasked).  mask, commit: [n] uint8.  n == 0 is a no-op.
+ */
+int bdlm_apply_commit(uint8_t* mask, const uint8_t* commit, int n, bdlm_stream stream);
+
+/* Human-readable name of a BDLM_* status code (a static string). */
+const char* bdlm_status_string(int status);
+
+/*
+ * Reads and clears the device error word of the current device (BDLM_DEVERR_* bits) into
+ * *bits_out (a HOST pointer).  Synchronises the device.  Returns BDLM_OK or an error.
+ */
+int bdlm_device_error(int* bits_out);
+
+/* Frees the workspace of the current device.  The device must be idle. */
+int bdlm_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BDLM_H */

@@ -1,0 +1,107 @@
+"""Parity of the CUDA confidence/commit kernel with the fp64 oracle, through the C-ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import bf16_tensor, compare_commit, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(lib, logits_bits, mask, threshold, temperature):
+    import torch
+    B, L = mask.shape
+    V = logits_bits.size // (B * L)
+    lg = bf16_tensor(logits_bits.reshape(B * L, V))
+    mk = dev(mask)
+    tok = torch.empty((B, L), dtype=torch.int32, device="cuda")
+    conf = torch.empty((B, L), dtype=torch.float32, device="cuda")
+    com = torch.full((B, L), 7, dtype=torch.uint8, device="cuda")
+    lib.bdlm_confidence_commit(lg, mk, B, L, V, threshold, temperature, tok, conf, com)
+    torch.cuda.synchronize()
+    return host(tok), host(conf), host(com)
+
+
+def check(lib, ci, threshold=None, temperature=None):
+    thr = ci.threshold if threshold is None else threshold
+    T = ci.temperature if temperature is None else temperature
+    ref = oracle.confidence_commit(ci.logits, ci.mask, thr, T)
+    tok, conf, com = run_gpu(lib, ci.logits, ci.mask, thr, T)
+    near = compare_commit(ref, tok, conf, com, ci.mask)
+    assert lib.bdlm_device_error() == 0
+    return ref, near
+
+
+def test_worked_example(lib):
+    x = np.array([[0, 0, 0, 0], [4, 0, 0, 0], [0, 2, 0, 0], [0, 3, 3, 0]], np.float32)
+    bits = W.f32_to_bf16_bits(x)
+    for mask, tau, T, want in [([1, 1, 1, 1], 0.9, 1.0, [0, 1, 0, 0]),
+                               ([1, 0, 1, 1], 0.9, 1.0, [0, 0, 1, 0]),
+                               ([1, 1, 1, 1], 0.9, 0.5, [0, 1, 1, 0]),
+                               ([1, 1, 1, 1], 0.25, 1.0, [1, 1, 1, 1])]:
+        m = np.array([mask], np.uint8)
+        tok, conf, com = run_gpu(lib, W.poison_unmasked_rows(bits, m), m, tau, T)
+        assert list(com[0]) == want
+        assert list(tok[0][m[0] == 1]) == [t for t, k in zip([0, 0, 1, 1], mask) if k]
+
+
+@pytest.mark.parametrize("config", [1, 2, 4])
+@pytest.mark.parametrize("supplementary", [False, True])
+def test_configs_full_size(lib, config, supplementary):
+    c = W.CONFIGS[config]
+    rng = np.random.default_rng(W.seed_for(config, 1 if supplementary else 0))
+    ci = W.commit_inputs(config, rng, c["B"], c["L"], c["V"], supplementary=supplementary)
+    ref, (near_diff, near_blocks) = check(lib, ci)
+    # every block with a masked position commits at least one
+    assert np.all(ref.commit.sum(1)[ci.mask.sum(1) > 0] >= 1)
+    print(f"config {config} supp={supplementary}: near-threshold blocks {near_blocks}, "
+          f"differing {near_diff}, multi-commit blocks {(ref.commit.sum(1) > 1).sum()}")
+
+
+@pytest.mark.parametrize("B,L,V", [(3, 4, 4), (2, 1, 151939), (5, 7, 1001), (2, 64, 3000),
+                                   (1, 3, 1), (9, 5, 8), (4, 16, 151936 + 5)])
+@pytest.mark.parametrize("T", [1.0, 0.5, 1.7])
+def test_odd_shapes(lib, B, L, V, T):
+    rng = np.random.default_rng(B * 1000 + L * 10 + V)
+    frac = rng.uniform(0.0, 1.0, size=B)
+    frac[0] = 1.0
+    if B > 2:
+        frac[1] = 0.0  # a SAVING block: nothing masked
+    mask = W.make_mask_fixed_fraction(rng, B, L, frac)
+    logits = W.make_logits(rng, B * L, V, peak_height=(0.0, 14.0))
+    ci = W.CommitInputs(B, L, V, W.poison_unmasked_rows(logits, mask), mask, 0.4, T)
+    check(lib, ci)
+
+
+def test_ties_go_to_lowest_index_and_position(lib):
+    B, L, V = 2, 6, 5000
+    x = np.zeros((B * L, V), np.float32)
+    x[:, [17, 4000, 4999]] = 5.0           # equal maxima in different CTAs' ranges
+    bits = W.f32_to_bf16_bits(x)
+    mask = np.ones((B, L), np.uint8)
+    tok, conf, com = run_gpu(lib, bits, mask, 0.9, 1.0)
+    assert np.all(tok == 17)
+    assert np.all(com.sum(1) == 1) and np.all(com[:, 0] == 1)  # equal confidences -> lowest i
+
+
+def test_repeated_calls_reuse_counters(lib):
+    """Counters are reset by the kernel: many calls in a row stay correct."""
+    rng = np.random.default_rng(5)
+    mask = W.make_mask_fixed_fraction(rng, 16, 4, 0.5)
+    logits = W.poison_unmasked_rows(W.make_logits(rng, 64, 20000, peak_height=(0, 12)), mask)
+    ref = oracle.confidence_commit(logits, mask, 0.3, 1.0)
+    for _ in range(5):
+        tok, conf, com = run_gpu(lib, logits, mask, 0.3, 1.0)
+        compare_commit(ref, tok, conf, com, mask)
+
+
+def test_apply_commit(lib):
+    import torch
+    rng = np.random.default_rng(8)
+    mask = (rng.uniform(size=(64, 8)) < 0.6).astype(np.uint8)
+    com = (rng.uniform(size=(64, 8)) < 0.3).astype(np.uint8) & mask
+    m = dev(mask)
+    lib.bdlm_apply_commit(m, dev(com), mask.size)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(m), oracle.apply_commit(mask, com))
