@@ -1,0 +1,114 @@
+"""Parity of the CUDA block attention with the fp64 oracle, through the C-ABI.
+
+Tolerance: |gpu - oracle| <= 1e-2 + 1e-2 * |oracle| per element (bf16 output, fp32
+accumulation, P rounded to bf16 before the PV product)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import bf16_tensor, dev
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-2, 1e-2
+
+
+def device_pools(a: W.AttnInputs, fill_nan=True):
+    import torch
+    shape = (a.pool_pages, a.P, a.Hkv, a.D)
+    fill = float("nan") if fill_nan else 0.0
+    kp = torch.full(shape, fill, dtype=torch.bfloat16, device="cuda")
+    vp = torch.full(shape, fill, dtype=torch.bfloat16, device="cuda")
+    ids = torch.from_numpy(a.ref_page_ids.astype(np.int64)).cuda()
+    kp[ids] = bf16_tensor(a.k_ref)
+    vp[ids] = bf16_tensor(a.v_ref)
+    return kp, vp
+
+
+def run_gpu(lib, a: W.AttnInputs, page_table=None, prefix_lens=None, sm_scale=0.0):
+    import torch
+    kp, vp = device_pools(a)
+    out = torch.full((a.B, a.L, a.Hq, a.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pt = a.page_table if page_table is None else page_table
+    pl = a.prefix_lens if prefix_lens is None else prefix_lens
+    desc = lib.attn_desc(a.B, a.L, a.Hq, a.Hkv, a.D, pt.shape[1], a.pool_pages, sm_scale=sm_scale)
+    lib.bdlm_block_attention(desc, bf16_tensor(a.q), kp, vp, dev(pt), dev(pl), a.L, out)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def check(lib, a, seqs=None, sm_scale=None):
+    got = run_gpu(lib, a, sm_scale=0.0 if sm_scale is None else sm_scale)
+    ref = oracle.block_attention(a.q, a.k_ref, a.v_ref, a.page_table_ref, a.prefix_lens, a.L,
+                                 a.Hq, a.Hkv, a.D, a.P, sm_scale=sm_scale, seqs=seqs)
+    sel = np.arange(a.B) if seqs is None else np.asarray(seqs)
+    g, r = got[sel], ref[sel]
+    assert np.all(np.isfinite(g)), "non-finite output"
+    excess = np.abs(g - r) - (ATOL + RTOL * np.abs(r))
+    assert excess.max() <= 0, f"max excess {excess.max()} at {np.unravel_index(excess.argmax(), excess.shape)}"
+    assert lib.bdlm_device_error() == 0
+    return np.abs(g - r).max()
+
+
+@pytest.mark.parametrize("L", [1, 4, 7, 16, 32, 64])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (16, 8), (8, 8), (16, 2)])
+def test_small_shapes(lib, L, Hq, Hkv):
+    rng = np.random.default_rng(L * 1000 + Hq * 10 + Hkv)
+    a = W.make_attention(rng, 3, L, Hq, Hkv, 128, prefix_range=(0, 700))
+    a.prefix_lens[0] = 0                      # the block alone
+    check(lib, a)
+
+
+@pytest.mark.parametrize("L,prefix", [(4, (1000, 3000)), (16, (2000, 5000)), (64, (2040, 4200))])
+def test_multiple_splits_and_chunks(lib, L, prefix):
+    rng = np.random.default_rng(L + prefix[0])
+    a = W.make_attention(rng, 4, L, 32, 8, 128, prefix_range=prefix)
+    check(lib, a)
+
+
+def test_config1(lib):
+    c = W.CONFIGS[1]
+    a = W.make_attention(np.random.default_rng(W.seed_for(1)), 1, 4, 16, 8, 128,
+                         prefix_range=(60, 60), identity_pages=True)
+    assert a.page_table.tolist() == [[0, 1, 2, 3]]
+    check(lib, a)
+
+
+@pytest.mark.parametrize("config,L,sample", [(2, 4, 24), (3, 16, 6), (3, 32, 6), (4, 64, 2)])
+def test_configs_full_size_sampled(lib, config, L, sample):
+    """The full workload on the GPU; the oracle recomputes a sample of sequences (always
+    the shortest and the longest) exactly."""
+    c = W.CONFIGS[config]
+    rng = np.random.default_rng(W.seed_for(config, L))
+    a = W.make_attention(rng, c["B"], L, c["Hq"], c["Hkv"], c["D"], prefix_range=c["prefix"],
+                         pool_pages=c.get("pool_pages"))
+    order = np.argsort(a.prefix_lens)
+    pick = np.unique(np.concatenate([order[:1], order[-1:],
+                                     rng.choice(a.B, size=sample - 2, replace=False)]))
+    err = check(lib, a, seqs=pick)
+    print(f"config {config} L={L}: sampled {len(pick)} sequences, max abs err {err:.3e}")
+
+
+def test_custom_scale_and_permuted_pool(lib):
+    rng = np.random.default_rng(77)
+    a = W.make_attention(rng, 5, 8, 32, 8, 128, prefix_range=(100, 1500), pool_factor=3.0)
+    check(lib, a, sm_scale=0.05)
+
+
+def test_bad_page_ids_and_lengths_are_flagged_not_faulted(lib):
+    import torch
+    rng = np.random.default_rng(3)
+    a = W.make_attention(rng, 4, 4, 32, 8, 128, prefix_range=(50, 300))
+    pt = a.page_table.copy()
+    pt[1, 0] = a.pool_pages + 5          # outside the pool
+    pt[2, 1] = -7
+    run_gpu(lib, a, page_table=pt)
+    assert lib.bdlm_device_error() & lib.BDLM_DEVERR_PAGE
+    pl = a.prefix_lens.copy()
+    pl[3] = pt.shape[1] * 16 + 100       # longer than the page table
+    pl[0] = -5
+    run_gpu(lib, a, prefix_lens=pl)
+    assert lib.bdlm_device_error() & lib.BDLM_DEVERR_LENGTH
+    # the library still works afterwards
+    check(lib, a)
