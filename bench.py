@@ -1,0 +1,515 @@
+#!/usr/bin/env python3
+"""Benchmark of one block-diffusion denoising round on GB300 (sm_103a), through libbdlm.
+
+Workload (the metric's configuration): batch 128, block length 4, SDAR-4B-shaped attention
+(32 query / 8 KV heads, head dim 128, bf16) with prefixes uniform in [512, 4096] in a
+shuffled 140 000-page pool of 16-token pages; logits 128x4x151936 bf16 N(0, 2^2) with one
+planted peak of height U[0, 10] per row; half of every block masked; threshold 0.75, T = 1.
+
+One step = one denoising round of that batch: block attention -> confidence/commit over the
+supplied logits -> mask update, all on the device.  value = block positions (B*L) per second.
+The JSON line also carries the same round with the selective LM head in the path (SDAR-4B
+hidden 2560, W 151936x2560, LM head on the masked rows feeding the commit), per-kernel times,
+the roofline of the dominant kernel, the end-to-end figure through host buffers and the
+fp64 CPU oracle timed on the host cores.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "denoised block-positions/s per round (B=128, SDAR-4B shape); % HBM roofline"
+UNIT = "block-positions/s"
+WORKLOAD = ("config2: B=128 L=4 Hq=32 Hkv=8 D=128 bf16, prefix U[512,4096], page 16, "
+            "shuffled 140000-page pool, logits 128x4x151936 N(0,4)+peak U[0,10], "
+            "mask 1/2 per block, tau=0.75 T=1")
+L2_BYTES = 129 * 1024 * 1024
+
+
+# --------------------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=W.seed_for(2))
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the e2e, full-round and CPU-baseline legs (profiling runs)")
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="pool of exactly the referenced pages x1.25 (smaller device footprint)")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def profile_traffic(name: str, src: str):
+    """DRAM bytes per launch from the committed ncu summary of kernel `name`, or None when
+    the kernel source changed since the capture (the summary records its sha256)."""
+    path = os.path.join(ROOT, "profiles", f"{name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    rec = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("source_sha256", "traffic_bytes_per_launch")):
+            k, v = line.strip().lstrip("-* ").split(":", 1)
+            rec[k.strip()] = v.strip().strip("`")
+    if rec.get("source_sha256") != digest:
+        return None
+    try:
+        return float(rec["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- workload
+def make_workload(seed: int, compact_pool: bool = False):
+    c = W.CONFIGS[2]
+    rng = np.random.default_rng(seed)
+    a = W.make_attention(rng, c["B"], c["L"], c["Hq"], c["Hkv"], c["D"],
+                         prefix_range=c["prefix"],
+                         pool_pages=None if compact_pool else c["pool_pages"], poison=False)
+    ci = W.commit_inputs(2, rng, c["B"], c["L"], c["V"], poison=False)
+    return c, a, ci
+
+
+def algorithmic_bytes(a, ci):
+    """Bytes the round must move (SURVEY-style accounting): every K/V element once per KV
+    head (exact token count), Q in and O out; the masked logits rows once."""
+    kv = int(a.kv_lens.sum()) * a.Hkv * a.D * 2 * 2
+    qo = a.B * a.L * a.Hq * a.D * 2 * 2
+    commit = int(ci.mask.sum()) * ci.V * 2
+    flops = int(4 * a.L * a.Hq * a.D * a.kv_lens.sum())
+    return kv + qo, commit, flops
+
+
+class Round:
+    """Device-resident inputs and the launch sequence of one round."""
+
+    def __init__(self, lib, a, ci, device, with_lm_head=False, lm_seed=None):
+        import torch
+        self.torch = torch
+        self.lib = lib
+        self.a, self.ci = a, ci
+        self.B, self.L, self.V = a.B, a.L, ci.V
+        shape = (a.pool_pages, a.P, a.Hkv, a.D)
+        self.kp = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.vp = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        ids = torch.from_numpy(a.ref_page_ids.astype(np.int64)).to(device)
+        self.kp[ids] = _bf16(a.k_ref, device)
+        self.vp[ids] = _bf16(a.v_ref, device)
+        self.q = _bf16(a.q, device)
+        self.pt = torch.from_numpy(a.page_table).to(device)
+        self.pl = torch.from_numpy(a.prefix_lens).to(device)
+        self.out = torch.empty((a.B, a.L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
+        self.logits = _bf16(ci.logits.reshape(a.B * a.L, ci.V), device)
+        self.mask0 = torch.from_numpy(ci.mask).to(device)
+        self.mask = self.mask0.clone()
+        self.tok = torch.empty((a.B, a.L), dtype=torch.int32, device=device)
+        self.conf = torch.empty((a.B, a.L), dtype=torch.float32, device=device)
+        self.commit = torch.empty((a.B, a.L), dtype=torch.uint8, device=device)
+        self.desc = lib.attn_desc(a.B, a.L, a.Hq, a.Hkv, a.D, a.page_table.shape[1],
+                                  a.pool_pages)
+        self.with_lm_head = with_lm_head
+        if with_lm_head:
+            rng = np.random.default_rng(lm_seed)
+            act = np.nonzero(ci.mask.reshape(-1))[0].astype(np.int32)
+            lm = W.lm_head_inputs(rng, a.B * a.L, 2560, ci.V, act)
+            self.H = lm.H
+            self.hidden = _bf16(lm.hidden, device)
+            self.w = _bf16(lm.w, device)
+            self.act = torch.from_numpy(act).to(device)
+            self.n_act = len(act)
+
+    def launches_per_step(self):
+        return 5 if self.with_lm_head else 3
+
+    def step(self, stream, events=None):
+        """Enqueue one round on `stream`; events (list) get a record after each stage."""
+        lib, s = self.lib, stream.cuda_stream
+        if events is not None:
+            events[0].record(stream)
+        lib.bdlm_block_attention(self.desc, self.q, self.kp, self.vp, self.pt, self.pl, self.L,
+                                 self.out, s)
+        if events is not None:
+            events[1].record(stream)
+        if self.with_lm_head:
+            lib.bdlm_lm_head(self.hidden, self.w, self.act, self.n_act, self.B * self.L, self.H,
+                             self.V, self.logits, s)
+        if events is not None:
+            events[2].record(stream)
+        lib.bdlm_confidence_commit(self.logits, self.mask, self.B, self.L, self.V,
+                                   self.ci.threshold, self.ci.temperature, self.tok, self.conf,
+                                   self.commit, s)
+        if events is not None:
+            events[3].record(stream)
+        lib.bdlm_apply_commit(self.mask, self.commit, self.B * self.L, s)
+        if events is not None:
+            events[4].record(stream)
+
+    def reset_mask(self, stream):
+        with self.torch.cuda.stream(stream):
+            self.mask.copy_(self.mask0)
+
+
+def _bf16(bits, device):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def time_round(rnd: Round, stream, steps: int, warmup: int, flush, barrier):
+    """Per-step CUDA-event times (ms) of the whole round and of each stage; L2 flushed
+    before every step, outside the timed events."""
+    torch = rnd.torch
+    for _ in range(warmup):
+        rnd.reset_mask(stream)
+        flush(stream)
+        rnd.step(stream)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(steps):
+        rnd.reset_mask(stream)
+        flush(stream)
+        rnd.step(stream, evs[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    stage = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(4)]
+                      for k in range(steps)])
+    total = np.array([evs[k][0].elapsed_time(evs[k][4]) for k in range(steps)])
+    return total, stage, wall
+
+
+def e2e_round(lib, a, ci, device, steps, warmup):
+    """Same round through the C-ABI from pinned host buffers: every step copies its inputs
+    host->device (q, the referenced K/V pages as a compact pool, page table, prefix lengths,
+    logits, mask), runs the round and copies tok/conf/commit back."""
+    import torch
+    stream = torch.cuda.Stream(device=device)
+    n_ref = a.k_ref.shape[0]
+    h = {
+        "q": torch.from_numpy(a.q.view(np.int16)).pin_memory(),
+        "k": torch.from_numpy(a.k_ref.view(np.int16)).pin_memory(),
+        "v": torch.from_numpy(a.v_ref.view(np.int16)).pin_memory(),
+        "pt": torch.from_numpy(a.page_table_ref).pin_memory(),
+        "pl": torch.from_numpy(a.prefix_lens).pin_memory(),
+        "lg": torch.from_numpy(ci.logits.view(np.int16)).pin_memory(),
+        "mk": torch.from_numpy(ci.mask).pin_memory(),
+    }
+    d = {k: torch.empty_like(v, device=device) for k, v in h.items()}
+    outs_h = {"tok": torch.empty((a.B, a.L), dtype=torch.int32).pin_memory(),
+              "conf": torch.empty((a.B, a.L), dtype=torch.float32).pin_memory(),
+              "com": torch.empty((a.B, a.L), dtype=torch.uint8).pin_memory()}
+    outs_d = {k: torch.empty_like(v, device=device) for k, v in outs_h.items()}
+    out = torch.empty((a.B, a.L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
+    desc = lib.attn_desc(a.B, a.L, a.Hq, a.Hkv, a.D, a.page_table.shape[1], n_ref)
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+
+    def one():
+        s = stream.cuda_stream
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        bf = torch.bfloat16
+        lib.bdlm_block_attention(desc, d["q"].view(bf), d["k"].view(bf), d["v"].view(bf), d["pt"],
+                                 d["pl"], a.L, out, s)
+        lib.bdlm_confidence_commit(d["lg"].view(bf), d["mk"], a.B, a.L, ci.V, ci.threshold,
+                                   ci.temperature, outs_d["tok"], outs_d["conf"], outs_d["com"], s)
+        lib.bdlm_apply_commit(d["mk"], outs_d["com"], a.B * a.L, s)
+        for k in outs_h:
+            outs_h[k].copy_(outs_d[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_round(a, ci, seqs):
+    import oracle
+    oracle.block_attention(a.q, a.k_ref, a.v_ref, a.page_table_ref, a.prefix_lens, a.L, a.Hq,
+                           a.Hkv, a.D, a.P, seqs=seqs)
+    oracle.confidence_commit(ci.logits, ci.mask, ci.threshold, ci.temperature, blocks=seqs)
+
+
+def cpu_baseline(a, ci, min_seconds=10.0):
+    """The fp64 oracle as it stands on the host cores: whole config-2 rounds (all 128
+    sequences) repeated until at least `min_seconds` of work."""
+    import oracle
+    oracle.build()
+    seqs = np.arange(a.B, dtype=np.int32)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        cpu_oracle_round(a, ci, seqs)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    per_round = el / reps
+    return {"value": a.B * a.L / per_round, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} full config-2 rounds (128 sequences: attention + commit), fp64 C++ "
+                      f"OpenMP, {per_round:.2f} s/round"}
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: rank 0 times it on the host cores; others exit."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    c, a, ci = make_workload(args.seed, compact_pool=True)
+    seqs = np.arange(16, dtype=np.int32)   # bounded sample per step: 16 of 128 sequences
+    for _ in range(max(0, min(args.warmup, 3))):
+        cpu_oracle_round(a, ci, seqs)
+    steps = max(1, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        cpu_oracle_round(a, ci, seqs)
+    el = (time.perf_counter() - t0) / steps
+    value = len(seqs) * a.L / el
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "16 of 128 sequences per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "attention + commit of 16 of the 128 sequences per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import block_diffusion_gb300 as bd
+    from block_diffusion_gb300 import build as bbuild
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if not os.path.exists(bbuild.OUT):
+        bbuild.build()
+    bd.load_library()
+    peaks = load_peaks()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+
+    def flush(stream):
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(rank & 0xFF)
+
+    # each rank denoises its own batch of 128 sequences (data parallel, no collective)
+    c, a, ci = make_workload(args.seed + 7919 * rank, compact_pool=args.compact_pool)
+    rnd = Round(bd, a, ci, device)
+    stream = torch.cuda.Stream(device=device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    total, stage, wall = time_round(rnd, stream, args.steps, max(3, args.warmup), flush, barrier)
+    clocks = sampler.stop()
+    assert bd.bdlm_device_error() == 0, "device error during the timed round"
+
+    ms = float(total.mean())
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    else:
+        ms_max = ms
+    units = a.B * a.L * world
+    value = units / (ms_max / 1e3)
+
+    attn_bytes, commit_bytes, attn_flops = algorithmic_bytes(a, ci)
+    attn_ms = float(stage[:, 0].mean())
+    commit_ms = float(stage[:, 2].mean())
+    src = os.path.join(ROOT, "block_diffusion_gb300", "csrc", "attention.cu")
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+    roofline = {"kernel": "attention", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": profile_traffic("attention_config2", src),
+                "algorithmic_bytes": attn_bytes, "peak_source": peaks["source"],
+                "round_frac": (attn_bytes + commit_bytes) / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    commit_gbs = commit_bytes / (commit_ms / 1e3) / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 128 * world, "block_len": 4,
+                       "l2": "flushed before every step (256 MB fill, outside the timed events)",
+                       "parallelism": f"dp{world} (independent batches, no collective)",
+                       "seed": args.seed},
+            "clocks": clocks,
+            "gpu_launches": rnd.launches_per_step() * args.steps,
+            "stages_ms": {"attention": attn_ms, "commit": commit_ms,
+                          "mask_update": float(stage[:, 3].mean())},
+            "commit_hbm": {"achieved": commit_gbs, "unit": "GB/s",
+                           "frac": commit_gbs / peaks["hbm_gbs"], "algorithmic_bytes": commit_bytes},
+            "roofline": roofline,
+            "attention_tflops": attn_flops / (attn_ms / 1e3) / 1e12,
+            "wall_s": wall}
+
+    if not args.quick and rank == 0:
+        # the same round with the selective LM head in the path (all rows of the hot path)
+        full = Round(bd, a, ci, device, with_lm_head=True, lm_seed=args.seed + 1)
+        ftotal, fstage, _ = time_round(full, stream, max(20, args.steps // 4), 3, flush,
+                                       lambda: None)
+        lm_ms = float(fstage[:, 1].mean())
+        H, n_act = full.H, full.n_act
+        lm_flops = 2.0 * n_act * H * ci.V
+        lm_bytes = ci.V * H * 2 + n_act * H * 2 + n_act * ci.V * 2
+        tf = lm_flops / (lm_ms / 1e3) / 1e12
+        line["full_round"] = {
+            "value": a.B * a.L / (float(ftotal.mean()) / 1e3), "unit": UNIT,
+            "ms_per_step": float(ftotal.mean()),
+            "workload": "config2 + selective LM head on the masked rows (H=2560, V=151936, "
+                        f"{n_act} rows, W N(0,0.02^2))",
+            "stages_ms": {"attention": float(fstage[:, 0].mean()), "lm_head": lm_ms,
+                          "commit": float(fstage[:, 2].mean()),
+                          "mask_update": float(fstage[:, 3].mean())},
+            "lm_head_roofline": {"bound": "tensor" if lm_flops / lm_bytes > 292 else "hbm",
+                                 "achieved_tflops": tf, "peak_tflops": peaks["bf16_tflops"],
+                                 "frac_tensor": tf / peaks["bf16_tflops"],
+                                 "achieved_gbs": lm_bytes / (lm_ms / 1e3) / 1e9,
+                                 "frac_hbm": lm_bytes / (lm_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+            "gpu_launches": full.launches_per_step() * max(20, args.steps // 4)}
+        del full
+        torch.cuda.empty_cache()
+        e2e_ms, h2d, d2h = e2e_round(bd, a, ci, device, max(10, args.steps // 20), 3)
+        line["e2e"] = {"value": a.B * a.L / (e2e_ms / 1e3), "unit": UNIT,
+                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                       "ms_per_step": e2e_ms,
+                       "note": "K/V copied as a compact pool of the referenced pages"}
+        line["cpu_baseline"] = cpu_baseline(a, ci)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -167,18 +167,20 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
   DeviceState* st = nullptr;
   int rc = current_device(&st);
   if (rc) return rc;
-  const CommitPlan plan = bdlm::plan_commit(B, L, V);
+  const CommitPlan plan = bdlm::plan_commit(B, L, V, st->num_sms);
+  if (plan.total_items > 0x7FFFFFFFll) return BDLM_ERR_INVALID;
   rc = ensure(reinterpret_cast<void**>(&st->commit_cnt), &st->commit_cnt_cap,
-              plan.row_cnt_bytes + plan.blk_cnt_bytes, true);
+              plan.work_bytes + plan.row_cnt_bytes + plan.blk_cnt_bytes, true);
   if (rc) return rc;
   rc = ensure(&st->data, &st->data_cap, plan.part_bytes, false);
   if (rc) return rc;
-  int* row_cnt = st->commit_cnt;
-  int* blk_cnt = st->commit_cnt + static_cast<size_t>(B) * L;
+  int* work = st->commit_cnt;
+  int* row_cnt = st->commit_cnt + 2;
+  int* blk_cnt = row_cnt + static_cast<size_t>(B) * L;
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
                                       conf_out, commit_out, plan,
                                       static_cast<bdlm::CommitPartial*>(st->data), row_cnt,
-                                      blk_cnt, static_cast<cudaStream_t>(stream));
+                                      blk_cnt, work, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 
@@ -241,7 +243,7 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
   cudaError_t e = bdlm::launch_attention(tm_q, tm_k, tm_v, page_table, prefix_lens, out, d.B,
                                          d.L, d.Hq, d.Hkv, d.max_pages_per_seq, d.num_pages,
                                          scale, plan, static_cast<float*>(st->data),
-                                         st->attn_cnt, st->err,
+                                         st->attn_cnt, st->err, st->num_sms,
                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }

@@ -6,21 +6,23 @@
 //     out = softmax_j(scale * q . K[j]) V[j]   over every j < prefix_len + L
 // (full prefix, bidirectional inside the block), KV head = h / (Hq/Hkv).
 //
-// Design (one CTA = one (sequence, KV head, KV split, query-row group)):
-//  * GQA packing: the G*L query rows that share a KV head are one UMMA operand, so each K/V
-//    page is read once per KV head.  The product is computed transposed, S^T = K Q^T, with
-//    128 KV tokens on the UMMA M side and the (few) query rows on N, so a 4-token block
-//    still fills a 128-row tensor-core tile.
-//  * TMA streams K and V pages (one 16-slot x 64-dim box per page and half) into a ring of
-//    32 KB stages with 128-byte swizzle; tcgen05.mma reads them straight from shared memory.
-//  * Softmax in two phases over a chunk of tiles held in tensor memory: all S^T tiles of the
-//    chunk are computed first, the exact column maximum is taken once, then P^T = exp(S^T - m)
-//    is written to shared memory (bf16) and O^T += V^T P^T accumulates in tensor memory.
-//    Chunks after the first rescale O^T once per chunk.
-//  * Long sequences are split across CTAs; each split writes (O, m, l) and the last split to
-//    arrive (atomic counter) merges them.  Nothing waits on another CTA.
-//  * Threads: warp 0 issues TMA, warp 1 owns tensor memory and issues the MMAs, warps 2-5
-//    (128 threads, one per tensor-memory lane) do the softmax and the epilogue.
+// Design.
+//  * Work item = (sequence, KV head, KV split, query-row group).  GQA packing: the G*L query
+//    rows that share a KV head form one UMMA operand, so each K/V page is read once per KV
+//    head.  The product is computed transposed, S^T = K Q^T, with 128 KV tokens on the UMMA
+//    M side and the query rows on N, so a 4-token block still fills a 128-row tile.
+//  * Persistent CTAs take items from a global counter.  Warp 0 streams K and V pages with
+//    TMA (one 16-slot x 64-dim box per page and half, 128-byte swizzle) into a ring of 32 KB
+//    stages; warp 1 issues tcgen05.mma from shared memory into tensor memory; warps 2-5 (one
+//    thread per tensor-memory lane) run the softmax and the epilogue.
+//  * An item is cut into chunks of tiles whose S^T fits in tensor memory.  Softmax per chunk
+//    in two phases: all S^T tiles first, the exact column maximum once, then P^T = exp(S^T-m)
+//    (bf16, shared memory) and O^T += V^T P^T in tensor memory; later chunks of the same
+//    item rescale O^T once.  The ring carries K of chunk u+1 ahead of V of chunk u and S^T
+//    is double-buffered, so the softmax of one chunk overlaps the K stream of the next and
+//    the pipeline never drains between items.
+//  * Splits of a long sequence write (O, m, l) partials that a small second kernel merges, so
+//    no CTA ever waits on another one; every wait inside a CTA is bounded.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -32,13 +34,15 @@
 namespace bdlm {
 namespace {
 
-constexpr int kTile = 128;            // KV tokens per tile
-constexpr int kPage = 16;             // tokens per page
-constexpr int kStageBytes = 32768;    // one K or V tile: 2 halves x 8 pages x 16 x 128 B
+constexpr int kTile = 128;          // KV tokens per tile (UMMA M)
+constexpr int kPage = 16;           // tokens per page
+constexpr int kStageBytes = 32768;  // one K or V tile: 2 halves x 8 pages x 16 slots x 128 B
 constexpr int kHalfBytes = 16384;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
 constexpr int kSoftmaxThreads = 128;
+constexpr int kMaxSplitTokens = 2048;
+constexpr int kMaxSplitPages = kMaxSplitTokens / kPage;
+constexpr int kItemRing = 4;
 
 struct AttnParams {
   const int32_t* page_table;
@@ -47,9 +51,18 @@ struct AttnParams {
   float* part;
   int* cnt;
   int* err;
-  int L, Hq, Hkv, G, max_pages, num_pages;
+  int* work;  // [0] next item, [1] CTAs finished
+  int B, L, Hq, Hkv, G, max_pages, num_pages;
   int lsub, row_groups, rows_per_group, split_tokens, max_splits, chunk_tiles;
+  int total_items;
   float scale_log2;  // sm_scale * log2(e)
+};
+
+struct Item {
+  int b, kvh, split, rg;
+  int t_begin, t_end, n_splits;
+  int n_tiles, n_chunks;
+  int end;
 };
 
 __device__ __forceinline__ void record_error(int* err, int bits) { atomicOr(err, bits); }
@@ -60,10 +73,38 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   mbar_wait(bar, parity, &dummy);
 }
 
-template <int N, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// Item index -> work item; items are enumerated split-major so that the short last splits
+// of long sequences come at the end of the schedule.  Returns false for an empty split.
+__device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& it) {
+  it.rg = idx % p.row_groups;
+  idx /= p.row_groups;
+  it.kvh = idx % p.Hkv;
+  idx /= p.Hkv;
+  it.b = idx % p.B;
+  it.split = idx / p.B;
+  const int prefix = p.prefix_lens[it.b];
+  const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
+  long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
+  if (kvl > max_tok) kvl = max_tok;
+  const int kv_len = static_cast<int>(kvl);
+  it.t_begin = it.split * p.split_tokens;
+  if (it.t_begin >= kv_len) return false;
+  it.t_end = min(kv_len, it.t_begin + p.split_tokens);
+  it.n_splits = (kv_len + p.split_tokens - 1) / p.split_tokens;
+  it.n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
+  it.n_chunks = (it.n_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
+  it.end = 0;
+  if (it.split == 0 && it.rg == 0 && it.kvh == 0 &&
+      (prefix < 0 || static_cast<long long>(prefix) + p.L > max_tok))
+    record_error(p.err, BDLM_DEVERR_LENGTH);
+  return true;
+}
+
+template <int N, int STAGES, int CTAS_PER_SM>
+__global__ void __launch_bounds__(kThreads, CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  constexpr uint32_t kTmemCols = 512 / CTAS_PER_SM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -71,56 +112,41 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   uint8_t* sKV = sQ + N * 256;                 // STAGES x 32 KB
   uint8_t* sP = sKV + STAGES * kStageBytes;    // 2 buffers x (2 K-atoms x N rows x 128 B)
 
-  __shared__ uint64_t bar_q, bar_full[STAGES], bar_empty[STAGES], bar_sfull, bar_sfree;
-  __shared__ uint64_t bar_pfull[2], bar_pempty[2], bar_oready, bar_ofull, bar_done;
+  __shared__ uint64_t bar_qfull, bar_qempty, bar_full[STAGES], bar_empty[STAGES];
+  __shared__ uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_pempty[2];
+  __shared__ uint64_t bar_oready, bar_ofull, bar_done;
+  __shared__ uint64_t bar_ifull[kItemRing], bar_iempty[kItemRing];
+  __shared__ Item s_item[kItemRing];
+  __shared__ int s_pid[3][kMaxSplitPages];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ int s_last;
   __shared__ float s_m[N], s_mc[N], s_alpha[N], s_l[N];
   __shared__ float s_red[4][N];
-
-  // ---- work item
-  int item = blockIdx.x;
-  const int rg = item % p.row_groups;
-  item /= p.row_groups;
-  const int split = item % p.max_splits;
-  item /= p.max_splits;
-  const int kvh = item % p.Hkv;
-  const int b = item / p.Hkv;
-  const int prefix = p.prefix_lens[b];
-  const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
-  long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
-  const bool len_bad = prefix < 0 || kvl > max_tok;
-  if (kvl > max_tok) kvl = max_tok;
-  const int kv_len = static_cast<int>(kvl);
-  const int t_begin = split * p.split_tokens;
-  if (len_bad && split == 0 && rg == 0 && threadIdx.x == 0) record_error(p.err, BDLM_DEVERR_LENGTH);
-  if (t_begin >= kv_len) return;
-  const int t_end = min(kv_len, t_begin + p.split_tokens);
-  const int n_splits = (kv_len + p.split_tokens - 1) / p.split_tokens;
-  const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
-  const int n_chunks = (n_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
-  const int rows = p.rows_per_group;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   // ---- setup
   if (threadIdx.x == 0) {
-    mbar_init(&bar_q, 1);
+    mbar_init(&bar_qfull, 1);
+    mbar_init(&bar_qempty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    mbar_init(&bar_sfull, 1);
-    mbar_init(&bar_sfree, kSoftmaxThreads);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_sfull[i], 1);
+      mbar_init(&bar_sfree[i], kSoftmaxThreads);
       mbar_init(&bar_pfull[i], kSoftmaxThreads);
       mbar_init(&bar_pempty[i], 1);
     }
     mbar_init(&bar_oready, kSoftmaxThreads);
     mbar_init(&bar_ofull, 1);
     mbar_init(&bar_done, 1);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&bar_ifull[i], 1);
+      mbar_init(&bar_iempty[i], 2);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -129,78 +155,191 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     tmem_relinquish();
   }
   if (warp >= 2) {
-    // zero the padding rows of the Q operand (rows >= rows_per_group)
+    // zero the padding rows of the Q operand (rows >= rows_per_group); TMA never writes them
+    const int rows = p.rows_per_group;
     const int t = threadIdx.x - 64;
-    const int pad_bytes = (N - rows) * 128;
-    for (int o = t * 16; o < pad_bytes; o += kSoftmaxThreads * 16) {
+    for (int o = t * 16; o < (N - rows) * 128; o += kSoftmaxThreads * 16) {
       *reinterpret_cast<uint4*>(sQ + rows * 128 + o) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(sQ + N * 128 + rows * 128 + o) = make_uint4(0, 0, 0, 0);
     }
-    const int x = ((warp & 3) << 5) | lane;
-    if (x < N) s_m[x] = -CUDART_INF_F;
     fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t tS = tmem;
-  const uint32_t tO = tmem + static_cast<uint32_t>(p.chunk_tiles * N);
+  const uint32_t tO = tmem + static_cast<uint32_t>(2 * p.chunk_tiles * N);
 
   if (warp == 0) {
     // =================================================================== TMA producer
+    int st = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int seq = -1;  // sequence number of the most recently published item
+    // Publishes `it` to the item ring (lane 0).
+    auto publish = [&](const Item& it) {
+      const int rs = seq % kItemRing;
+      if (ok) ok = mbar_wait(&bar_iempty[rs], ((seq / kItemRing) & 1) ^ 1, &abort_flag);
+      s_item[rs] = it;
+      mbar_arrive(&bar_ifull[rs]);
+    };
+    // Takes the next non-empty item from the global counter, publishes it to the item ring
+    // and loads its page ids (whole warp).  When the work is done it publishes the end marker
+    // at once (the MMA warp needs it before it can finish the current item) and returns false.
+    auto grab = [&](Item& it) -> bool {
+      while (true) {
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(p.work, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx >= p.total_items) {
+          ++seq;
+          if (lane == 0) {
+            Item e{};
+            e.end = 1;
+            publish(e);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          return false;
+        }
+        if (decode_item(idx, p, it)) break;
+      }
+      ++seq;
+      int* pid = s_pid[seq % 3];
+      const int32_t* pt =
+          p.page_table + static_cast<size_t>(it.b) * p.max_pages + it.t_begin / kPage;
+      const int np = (it.t_end - it.t_begin + kPage - 1) / kPage;
+      int bad = 0;
+      for (int q = lane; q < np; q += 32) {
+        int id = pt[q];
+        if (id < 0 || id >= p.num_pages) {
+          bad = 1;
+          id = -1;
+        }
+        pid[q] = id;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, BDLM_DEVERR_PAGE);
+      __syncwarp();
+      if (lane == 0) publish(it);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      return true;
+    };
+    // Loads the Q tile of item `it` (sequence number s) into the single Q buffer once the
+    // previous item's S^T MMAs are done with it.  Lane 0.
+    int q_loads = 0;
+    auto load_q = [&](const Item& it, int s) {
+      if (ok) ok = mbar_wait(&bar_qempty, (s & 1) ^ 1, &abort_flag);
+      if (!ok) return;
+      mbar_arrive_expect_tx(&bar_qfull, 2u * 128u * static_cast<uint32_t>(p.G * p.lsub));
+      for (int h = 0; h < 2; ++h)
+        tma_load_3d(sQ + h * N * 128, &tm_q, &bar_qfull, h * 64, it.kvh * p.G,
+                    it.b * p.L + it.rg * p.lsub);
+      ++q_loads;
+    };
+    // Streams the K (pass 0) or V (pass 1) tiles of chunk c of item `it` (page ids in
+    // s_pid[pbuf]).  Whole warp: lane 0 waits for a free stage and posts the byte count, then
+    // lane q issues the two boxes of page q, so a stage's 16 copies go out in one instruction.
+    auto emit = [&](const Item& it, int c, int pbuf, int pass, Item* gi = nullptr,
+                    bool* gh = nullptr, int* gs = nullptr) {
+      const CUtensorMap* tm = pass == 0 ? &tm_k : &tm_v;
+      const int j0 = c * p.chunk_tiles;
+      const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
+      for (int j = j0; j < j1 && ok; ++j) {
+        if (gi != nullptr && j == j0 + STAGES) {
+          // the ring is full of this chunk's tiles: take the next item now, while waiting
+          *gh = grab(*gi);
+          *gs = seq;
+          gi = nullptr;
+          if (!ok) break;
+        }
+        if (lane == 0) ok = mbar_wait(&bar_empty[st], ph ^ 1, &abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int tok0 = it.t_begin + j * kTile;
+        const int npg = min(kTile / kPage, (it.t_end - tok0 + kPage - 1) / kPage);
+        const int id = lane < npg ? s_pid[pbuf][j * (kTile / kPage) + lane] : -1;
+        const uint32_t have = __ballot_sync(0xffffffffu, id >= 0);
+        uint8_t* stage = sKV + st * kStageBytes;
+        if (lane == 0) {
+          if (have)
+            mbar_arrive_expect_tx(&bar_full[st], static_cast<uint32_t>(__popc(have)) * 4096u);
+          else
+            mbar_arrive(&bar_full[st]);
+        }
+        __syncwarp();
+        if (id >= 0) {
+          tma_load_4d(stage + lane * 2048, tm, &bar_full[st], 0, it.kvh, 0, id);
+          tma_load_4d(stage + kHalfBytes + lane * 2048, tm, &bar_full[st], 64, it.kvh, 0, id);
+        }
+        if (++st == STAGES) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+      if (gi != nullptr && ok) {
+        *gh = grab(*gi);
+        *gs = seq;
+      }
+    };
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bar_q, 2u * 128u * static_cast<uint32_t>(p.G * p.lsub));
-      for (int h = 0; h < 2; ++h)
-        tma_load_3d(sQ + h * N * 128, &tm_q, &bar_q, h * 64, kvh * p.G, b * p.L + rg * p.lsub);
-      const int32_t* pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
-      int st = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        const int j0 = c * p.chunk_tiles;
-        const int j1 = min(n_tiles, j0 + p.chunk_tiles);
-        for (int pass = 0; pass < 2 && ok; ++pass) {
-          const CUtensorMap* tm = pass == 0 ? &tm_k : &tm_v;
-          for (int j = j0; j < j1; ++j) {
-            if (!(ok = mbar_wait(&bar_empty[st], ph ^ 1, &abort_flag))) break;
-            const int tok0 = t_begin + j * kTile;
-            const int npg = min(kTile / kPage, (t_end - tok0 + kPage - 1) / kPage);
-            int pid[kTile / kPage];
-            uint32_t bytes = 0;
-            for (int q = 0; q < npg; ++q) {
-              int id = pt[tok0 / kPage + q];
-              if (id < 0 || id >= p.num_pages) {
-                if (pass == 0) record_error(p.err, BDLM_DEVERR_PAGE);
-                id = -1;
-              } else {
-                bytes += 2 * 2048;
-              }
-              pid[q] = id;
-            }
-            uint8_t* stage = sKV + st * kStageBytes;
-            if (bytes)
-              mbar_arrive_expect_tx(&bar_full[st], bytes);
-            else
-              mbar_arrive(&bar_full[st]);
-            for (int q = 0; q < npg; ++q) {
-              if (pid[q] < 0) continue;
-              tma_load_4d(stage + q * 2048, tm, &bar_full[st], 0, kvh, 0, pid[q]);
-              tma_load_4d(stage + kHalfBytes + q * 2048, tm, &bar_full[st], 64, kvh, 0, pid[q]);
-            }
-            if (++st == STAGES) {
-              st = 0;
-              ph ^= 1;
-            }
-          }
-        }
+    }
+    // Ring order: K of chunk u+1, then V of chunk u.  One item of look-ahead (`pend`) is
+    // grabbed and published early, so the MMA warp always knows what follows the current
+    // chunk; the next look-ahead is grabbed once the ring is full of V tiles waiting for the
+    // softmax, so the scheduler's latency stays off the stream (three page-id buffers: cur,
+    // pend, new pend).
+    Item cur, pend, pend2;
+    bool have = grab(cur);
+    int cur_seq = seq, pend_seq = seq;
+    bool have_pend = false;
+    if (have) {
+      if (lane == 0) load_q(cur, cur_seq);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      emit(cur, 0, cur_seq % 3, 0);
+      have_pend = grab(pend);
+      pend_seq = seq;
+    }
+    int c = 0;
+    while (have && ok) {
+      const bool same = c + 1 < cur.n_chunks;
+      const bool has_next = same || have_pend;
+      bool have_pend2 = false;
+      int pend2_seq = 0;
+      if (same) {
+        emit(cur, c + 1, cur_seq % 3, 0);
+      } else if (have_pend) {
+        if (lane == 0) load_q(pend, pend_seq);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        emit(pend, 0, pend_seq % 3, 0);
+      }
+      if (!same && have_pend)
+        emit(cur, c, cur_seq % 3, 1, &pend2, &have_pend2, &pend2_seq);
+      else
+        emit(cur, c, cur_seq % 3, 1);
+      if (!has_next) break;
+      if (same) {
+        ++c;
+      } else {
+        cur = pend;
+        cur_seq = pend_seq;
+        c = 0;
+        pend = pend2;
+        pend_seq = pend2_seq;
+        have_pend = have_pend2;
+      }
+    }
+    if (lane == 0) {
+      // the last CTA to finish taking work resets the counter for the next launch
+      __threadfence();
+      if (atomicAdd(p.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        p.work[0] = 0;
+        p.work[1] = 0;
       }
       if (!ok) {
-        // drain: every stage's most recent load must land before the CTA exits
         for (int s = 0; s < STAGES; ++s) mbar_wait_drain(&bar_full[s], ph ^ (s < st ? 0 : 1));
+        if (q_loads > 0) mbar_wait_drain(&bar_qfull, (q_loads - 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -211,24 +350,27 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t kv_addr = smem_u32(sKV);
       const uint32_t p_addr = smem_u32(sP);
-      bool ok = mbar_wait(&bar_q, 0, &abort_flag);
+      bool ok = true;
       int st = 0;
       uint32_t ph = 0;
-      int pcount = 0;
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        const int j0 = c * p.chunk_tiles;
-        const int j1 = min(n_tiles, j0 + p.chunk_tiles);
-        if (c > 0 && !(ok = mbar_wait(&bar_sfree, (c - 1) & 1, &abort_flag))) break;
+      int pcount = 0, ocount = 0;
+      // S^T of chunk `c` of `it` (global chunk number u) into S buffer u & 1
+      auto do_s = [&](const Item& it, int c, int u, int seq) {
+        if (!(ok = ok && mbar_wait(&bar_sfree[u & 1], ((u >> 1) & 1) ^ 1, &abort_flag))) return;
+        if (c == 0 && !(ok = mbar_wait(&bar_qfull, seq & 1, &abort_flag))) return;
         tc_fence_after();
-        // S^T[tile] = K[tile] . Q^T, K over the 128 head dims in 8 steps of 16
+        const uint32_t tS = tmem + static_cast<uint32_t>((u & 1) * p.chunk_tiles * N);
+        const int j0 = c * p.chunk_tiles;
+        const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
-          if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) break;
+          if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
           tc_fence_after();
           const uint32_t ka = kv_addr + st * kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t ad = smem_desc(ka + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc(q_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                smem_desc(q_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
             umma_bf16(tS + (j - j0) * N, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bar_empty[st]);
@@ -237,17 +379,24 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             ph ^= 1;
           }
         }
-        if (!ok) break;
-        umma_commit(&bar_sfull);
-        // O^T += V^T[tile] . P^T[tile], K over the tile's pages (16 tokens each)
+        umma_commit(&bar_sfull[u & 1]);
+        if (c == it.n_chunks - 1) umma_commit(&bar_qempty);  // Q no longer needed
+      };
+      // O^T += V^T P^T over the tiles of chunk `c`
+      auto do_pv = [&](const Item& it, int c) {
+        const int j0 = c * p.chunk_tiles;
+        const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
           const int pb = pcount & 1;
-          if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) break;
-          if (!(ok = mbar_wait(&bar_pfull[pb], (pcount >> 1) & 1, &abort_flag))) break;
-          if (c > 0 && j == j0 && !(ok = mbar_wait(&bar_oready, (c - 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
+          if (!(ok = mbar_wait(&bar_pfull[pb], (pcount >> 1) & 1, &abort_flag))) return;
+          if (c > 0 && j == j0) {
+            if (!(ok = mbar_wait(&bar_oready, ocount & 1, &abort_flag))) return;
+            ++ocount;
+          }
           tc_fence_after();
-          const int tok0 = t_begin + j * kTile;
-          const int valid = min(kTile, t_end - tok0);
+          const int tok0 = it.t_begin + j * kTile;
+          const int valid = min(kTile, it.t_end - tok0);
           const int npg = (valid + kPage - 1) / kPage;
           const int tail = valid - (npg - 1) * kPage;
           uint8_t* stage = sKV + st * kStageBytes;
@@ -275,8 +424,40 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             ph ^= 1;
           }
         }
-        if (!ok) break;
         umma_commit(&bar_ofull);
+      };
+      int seq = 0;
+      Item cur, nxt;
+      ok = mbar_wait(&bar_ifull[0], 0, &abort_flag);
+      cur = s_item[0];
+      if (ok && !cur.end) {
+        int c = 0, u = 0;
+        do_s(cur, 0, 0, 0);
+        while (ok) {
+          bool has_next;
+          int nc = 0, nseq = seq;
+          if (c + 1 < cur.n_chunks) {
+            has_next = true;
+            nc = c + 1;
+            nxt = cur;
+          } else {
+            nseq = seq + 1;
+            const int rs = nseq % kItemRing;
+            if (!(ok = mbar_wait(&bar_ifull[rs], (nseq / kItemRing) & 1, &abort_flag))) break;
+            nxt = s_item[rs];
+            has_next = !nxt.end;
+          }
+          if (has_next) do_s(nxt, nc, u + 1, nseq);
+          if (!ok) break;
+          do_pv(cur, c);
+          if (!ok) break;
+          if (c == cur.n_chunks - 1) mbar_arrive(&bar_iempty[seq % kItemRing]);
+          if (!has_next) break;
+          cur = nxt;
+          c = nc;
+          seq = nseq;
+          ++u;
+        }
       }
       umma_commit(&bar_done);
     }
@@ -286,181 +467,223 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int x = (q4 << 5) | lane;  // tensor-memory lane: KV token of a tile, or head dim
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const float cs = p.scale_log2;
+    const int rows = p.rows_per_group;
     float l[N];
-#pragma unroll
-    for (int n = 0; n < N; ++n) l[n] = 0.f;
     bool ok = true;
-    int pcount = 0;
-    for (int c = 0; c < n_chunks && ok; ++c) {
-      const int j0 = c * p.chunk_tiles;
-      const int j1 = min(n_tiles, j0 + p.chunk_tiles);
-      if (!(ok = mbar_wait(&bar_sfull, c & 1, &abort_flag))) break;
-      tc_fence_after();
-      // phase A: exact column maxima over the chunk
+    int pcount = 0, u = 0;
+    for (int seq = 0; ok; ++seq) {
+      const int rs = seq % kItemRing;
+      if (!(ok = mbar_wait(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      const Item it = s_item[rs];
+      if (it.end) break;
 #pragma unroll
-      for (int cg = 0; cg < N / 16; ++cg) {
-        float mx[16];
+      for (int n = 0; n < N; ++n) l[n] = 0.f;
+      if (x < N) s_m[x] = -CUDART_INF_F;
+      for (int c = 0; c < it.n_chunks && ok; ++c, ++u) {
+        const int j0 = c * p.chunk_tiles;
+        const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
+        const uint32_t tS = tmem + lane_off + static_cast<uint32_t>((u & 1) * p.chunk_tiles * N);
+        if (!(ok = mbar_wait(&bar_sfull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        tc_fence_after();
+        // phase A: exact column maxima over the chunk
 #pragma unroll
-        for (int k = 0; k < 16; ++k) mx[k] = -CUDART_INF_F;
-        for (int j = j0; j < j1; ++j) {
-          uint32_t r[16];
-          tmem_ld16(tS + lane_off + (j - j0) * N + cg * 16, r);
-          tmem_wait_ld();
-          tmem_regs_ready(r);
-          const bool valid = t_begin + j * kTile + x < t_end;
+        for (int cg = 0; cg < N / 16; ++cg) {
+          float mx[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            if (valid) mx[k] = fmaxf(mx[k], __uint_as_float(r[k]));
+          for (int k = 0; k < 16; ++k) mx[k] = -CUDART_INF_F;
+          for (int j = j0; j < j1; ++j) {
+            uint32_t r[16];
+            tmem_ld16(tS + (j - j0) * N + cg * 16, r);
+            tmem_wait_ld();
+            tmem_regs_ready(r);
+            const bool valid = it.t_begin + j * kTile + x < it.t_end;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              if (valid) mx[k] = fmaxf(mx[k], __uint_as_float(r[k]));
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+              mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], off));
+          }
+          if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) s_red[q4][cg * 16 + k] = mx[k];
+          }
         }
+        named_barrier(1, kSoftmaxThreads);
+        if (x < N) {
+          const float mc = fmaxf(fmaxf(s_red[0][x], s_red[1][x]), fmaxf(s_red[2][x], s_red[3][x]));
+          const float mo = s_m[x];
+          const float mn = fmaxf(mo, mc);
+          s_alpha[x] = (mo == -CUDART_INF_F) ? 0.f : exp2f((mo - mn) * cs);
+          s_m[x] = mn;
+          s_mc[x] = mn * cs;
+        }
+        named_barrier(1, kSoftmaxThreads);
+        if (c > 0) {
+          // rescale the running O^T columns (and l) to the new maxima
+          if (!(ok = mbar_wait(&bar_ofull, (u - 1) & 1, &abort_flag))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+          for (int cg = 0; cg < N / 16; ++cg) {
+            uint32_t r[16];
+            tmem_ld16(tO + lane_off + cg * 16, r);
+            tmem_wait_ld();
+            tmem_regs_ready(r);
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
-            mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], off));
+            for (int k = 0; k < 16; ++k)
+              r[k] = __float_as_uint(__uint_as_float(r[k]) * s_alpha[cg * 16 + k]);
+            tmem_st16(tO + lane_off + cg * 16, r);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar_oready);
+#pragma unroll
+          for (int n = 0; n < N; ++n) l[n] *= s_alpha[n];
+        }
+        // phase B: P^T = exp(S^T - m) to shared memory, tile by tile
+        if constexpr (N <= 32) {
+          // narrow N: maxima in registers, the next tile's S^T read from tensor memory
+          // while this one is exponentiated
+          float mcr[N];
+  #pragma unroll
+          for (int n = 0; n < N; ++n) mcr[n] = s_mc[n];
+          uint32_t r[N];
+  #pragma unroll
+          for (int cg = 0; cg < N / 16; ++cg) {
+            uint32_t (&rg)[16] = *reinterpret_cast<uint32_t(*)[16]>(r + cg * 16);
+            tmem_ld16(tS + cg * 16, rg);
+          }
+          for (int j = j0; j < j1 && ok; ++j) {
+            tmem_wait_ld();
+  #pragma unroll
+            for (int cg = 0; cg < N / 16; ++cg)
+              tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + cg * 16));
+            float pv[N];
+            const bool valid = it.t_begin + j * kTile + x < it.t_end;
+  #pragma unroll
+            for (int n = 0; n < N; ++n)
+              pv[n] = valid ? exp2f(fmaf(__uint_as_float(r[n]), cs, -mcr[n])) : 0.f;
+            if (j + 1 < j1) {
+  #pragma unroll
+              for (int cg = 0; cg < N / 16; ++cg) {
+                uint32_t (&rg)[16] = *reinterpret_cast<uint32_t(*)[16]>(r + cg * 16);
+                tmem_ld16(tS + (j + 1 - j0) * N + cg * 16, rg);
+              }
+            }
+            const int pb = pcount & 1;
+            if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1, &abort_flag))) break;
+            uint8_t* pbuf = sP + pb * (N * 256) + (x >> 6) * (N * 128);
+            const uint32_t xc = (x & 63) >> 3;
+            const uint32_t xb = (x & 7) * 2;
+  #pragma unroll
+            for (int n = 0; n < N; ++n) {
+              l[n] += pv[n];
+              const uint32_t off = n * 128 + ((xc ^ (n & 7)) << 4) + xb;
+              *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = __float2bfloat16_rn(pv[n]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar_pfull[pb]);
+            ++pcount;
+          }
+          if (!ok) tmem_wait_ld();
+        } else {
+          // phase B (wide N): column groups of 16, maxima read from shared memory
+          for (int j = j0; j < j1 && ok; ++j) {
+            const int pb = pcount & 1;
+            if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1, &abort_flag))) break;
+            uint8_t* pbuf = sP + pb * (N * 256) + (x >> 6) * (N * 128);
+            const bool valid = it.t_begin + j * kTile + x < it.t_end;
+            const uint32_t xc = (x & 63) >> 3;
+            const uint32_t xb = (x & 7) * 2;
+  #pragma unroll
+            for (int cg = 0; cg < N / 16; ++cg) {
+              uint32_t r[16];
+              tmem_ld16(tS + (j - j0) * N + cg * 16, r);
+              tmem_wait_ld();
+              tmem_regs_ready(r);
+  #pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const int n = cg * 16 + k;
+                const float pv = valid ? exp2f(fmaf(__uint_as_float(r[k]), cs, -s_mc[n])) : 0.f;
+                l[n] += pv;
+                const uint32_t off = n * 128 + ((xc ^ (n & 7)) << 4) + xb;
+                *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = __float2bfloat16_rn(pv);
+              }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar_pfull[pb]);
+            ++pcount;
+          }
+        }
+        if (!ok) break;
+        if (!ok) break;
+        tc_fence_before();
+        mbar_arrive(&bar_sfree[u & 1]);
+        if (c != it.n_chunks - 1) continue;
+        // ---- epilogue of the item
+        if (!(ok = mbar_wait(&bar_ofull, u & 1, &abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+          float v = l[n];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          l[n] = v;
         }
         if (lane == 0) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) s_red[q4][cg * 16 + k] = mx[k];
+          for (int n = 0; n < N; ++n) s_red[q4][n] = l[n];
         }
-      }
-      named_barrier(1, kSoftmaxThreads);
-      if (x < N) {
-        const float mc = fmaxf(fmaxf(s_red[0][x], s_red[1][x]), fmaxf(s_red[2][x], s_red[3][x]));
-        const float mo = s_m[x];
-        const float mn = fmaxf(mo, mc);
-        s_alpha[x] = (mo == -CUDART_INF_F) ? 0.f : exp2f((mo - mn) * cs);
-        s_m[x] = mn;
-        s_mc[x] = mn * cs;
-      }
-      named_barrier(1, kSoftmaxThreads);
-      if (c > 0) {
-        // rescale the running O^T columns (and l) to the new maxima
-        if (!(ok = mbar_wait(&bar_ofull, (c - 1) & 1, &abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int cg = 0; cg < N / 16; ++cg) {
-          uint32_t r[16];
-          tmem_ld16(tO + lane_off + cg * 16, r);
-          tmem_wait_ld();
-          tmem_regs_ready(r);
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            r[k] = __float_as_uint(__uint_as_float(r[k]) * s_alpha[cg * 16 + k]);
-          tmem_st16(tO + lane_off + cg * 16, r);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar_oready);
-#pragma unroll
-        for (int n = 0; n < N; ++n) l[n] *= s_alpha[n];
-      }
-      // phase B: P^T = exp(S^T - m) to shared memory, tile by tile
-      for (int j = j0; j < j1 && ok; ++j) {
-        const int pb = pcount & 1;
-        if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1, &abort_flag))) break;
-        uint8_t* pbuf = sP + pb * (N * 256) + (x >> 6) * (N * 128);
-        const bool valid = t_begin + j * kTile + x < t_end;
-        const uint32_t xc = (x & 63) >> 3;
-        const uint32_t xb = (x & 7) * 2;
-#pragma unroll
-        for (int cg = 0; cg < N / 16; ++cg) {
-          uint32_t r[16];
-          tmem_ld16(tS + lane_off + (j - j0) * N + cg * 16, r);
-          tmem_wait_ld();
-          tmem_regs_ready(r);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int n = cg * 16 + k;
-            const float pv = valid ? exp2f(fmaf(__uint_as_float(r[k]), cs, -s_mc[n])) : 0.f;
-            l[n] += pv;
-            const uint32_t off = n * 128 + ((xc ^ (n & 7)) << 4) + xb;
-            *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = __float2bfloat16_rn(pv);
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar_pfull[pb]);
-        ++pcount;
-      }
-      if (!ok) break;
-      tc_fence_before();
-      mbar_arrive(&bar_sfree);
-    }
-    // ---- epilogue
-    if (ok) ok = mbar_wait(&bar_ofull, (n_chunks - 1) & 1, &abort_flag);
-    if (ok) {
-      tc_fence_after();
-#pragma unroll
-      for (int n = 0; n < N; ++n) {
-        float v = l[n];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        l[n] = v;
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int n = 0; n < N; ++n) s_red[q4][n] = l[n];
-      }
-      named_barrier(1, kSoftmaxThreads);
-      if (x < N) s_l[x] = (s_red[0][x] + s_red[1][x]) + (s_red[2][x] + s_red[3][x]);
-      named_barrier(1, kSoftmaxThreads);
-      const size_t head_base = static_cast<size_t>(kvh) * p.G;
-      if (n_splits == 1) {
-#pragma unroll
-        for (int cg = 0; cg < N / 16; ++cg) {
-          uint32_t r[16];
-          tmem_ld16(tO + lane_off + cg * 16, r);
-          tmem_wait_ld();
-          tmem_regs_ready(r);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int n = cg * 16 + k;
-            if (n >= rows) continue;
-            const int i = rg * p.lsub + n / p.G;
-            if (i >= p.L) continue;
-            const size_t o = ((static_cast<size_t>(b) * p.L + i) * p.Hq + head_base + n % p.G) * 128 + x;
-            p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[k]) / s_l[n]));
-          }
-        }
-      } else {
-        const size_t unit = static_cast<size_t>(N) * 130;
-        const size_t grp = (static_cast<size_t>(b) * p.Hkv + kvh) * p.row_groups + rg;
-        float* mine = p.part + (grp * p.max_splits + split) * unit;
-#pragma unroll
-        for (int cg = 0; cg < N / 16; ++cg) {
-          uint32_t r[16];
-          tmem_ld16(tO + lane_off + cg * 16, r);
-          tmem_wait_ld();
-          tmem_regs_ready(r);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) mine[(cg * 16 + k) * 128 + x] = __uint_as_float(r[k]);
-        }
-        if (x < N) {
-          mine[N * 128 + x] = s_m[x];
-          mine[N * 128 + N + x] = s_l[x];
-        }
-        __threadfence();
         named_barrier(1, kSoftmaxThreads);
-        if (x == 0) s_last = (atomicAdd(p.cnt + grp, 1) == n_splits - 1);
+        if (x < N) s_l[x] = (s_red[0][x] + s_red[1][x]) + (s_red[2][x] + s_red[3][x]);
         named_barrier(1, kSoftmaxThreads);
-        if (s_last) {
-          __threadfence();
-          const float* all = p.part + grp * p.max_splits * unit;
-          for (int n = 0; n < rows; ++n) {
-            const int i = rg * p.lsub + n / p.G;
-            if (i >= p.L) break;
-            float M = -CUDART_INF_F;
-            for (int s = 0; s < n_splits; ++s) M = fmaxf(M, __ldcg(all + s * unit + N * 128 + n));
-            float num = 0.f, den = 0.f;
-            for (int s = 0; s < n_splits; ++s) {
-              const float w = exp2f((__ldcg(all + s * unit + N * 128 + n) - M) * cs);
-              num += w * __ldcg(all + s * unit + n * 128 + x);
-              den += w * __ldcg(all + s * unit + N * 128 + N + n);
+        const size_t head_base = static_cast<size_t>(it.kvh) * p.G;
+        if (it.n_splits == 1) {
+#pragma unroll
+          for (int cg = 0; cg < N / 16; ++cg) {
+            uint32_t r[16];
+            tmem_ld16(tO + lane_off + cg * 16, r);
+            tmem_wait_ld();
+            tmem_regs_ready(r);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int n = cg * 16 + k;
+              if (n >= rows) continue;
+              const int i = it.rg * p.lsub + n / p.G;
+              if (i >= p.L) continue;
+              const size_t o =
+                  ((static_cast<size_t>(it.b) * p.L + i) * p.Hq + head_base + n % p.G) * 128 + x;
+              p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[k]) / s_l[n]));
             }
-            const size_t o = ((static_cast<size_t>(b) * p.L + i) * p.Hq + head_base + n % p.G) * 128 + x;
-            p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
           }
-          if (x == 0) p.cnt[grp] = 0;
+        } else {
+          // one split of a longer sequence: write (O, m, l); attn_merge_kernel combines them
+          const size_t unit = static_cast<size_t>(N) * 130;
+          const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
+          float* mine = p.part + (grp * p.max_splits + it.split) * unit;
+#pragma unroll
+          for (int cg = 0; cg < N / 16; ++cg) {
+            uint32_t r[16];
+            tmem_ld16(tO + lane_off + cg * 16, r);
+            tmem_wait_ld();
+            tmem_regs_ready(r);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) mine[(cg * 16 + k) * 128 + x] = __uint_as_float(r[k]);
+          }
+          if (x < N) {
+            mine[N * 128 + x] = s_m[x];
+            mine[N * 128 + N + x] = s_l[x];
+          }
         }
+        // O^T and the item descriptor are free for the next item
+        tc_fence_before();
+        named_barrier(1, kSoftmaxThreads);
+        if (x == 0) mbar_arrive(&bar_iempty[rs]);
       }
     }
   }
@@ -477,25 +700,94 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   if (threadIdx.x == 0 && abort_flag) record_error(p.err, BDLM_DEVERR_TIMEOUT);
 }
 
+
+// Merges the splits of every (sequence, KV head, row group) whose KV range was cut into more
+// than one item: out = sum_s w_s O_s with w_s = exp(m_s - M) / sum_s exp(m_s - M) l_s.
+// One CTA (128 threads, one per head dim) per group.
+__global__ void __launch_bounds__(128)
+attn_merge_kernel(const AttnParams p, int N) {
+  extern __shared__ float sm[];  // [max_splits][N] weights, then [max_splits][N] l
+  const int grp = blockIdx.x;
+  const int rg = grp % p.row_groups;
+  const int bk = grp / p.row_groups;
+  const int kvh = bk % p.Hkv;
+  const int b = bk / p.Hkv;
+  const int prefix = p.prefix_lens[b];
+  const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
+  long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
+  if (kvl > max_tok) kvl = max_tok;
+  const int ns = static_cast<int>((kvl + p.split_tokens - 1) / p.split_tokens);
+  if (ns <= 1) return;
+  const int rows = p.rows_per_group;
+  const int x = threadIdx.x;
+  const size_t unit = static_cast<size_t>(N) * 130;
+  const float* all = p.part + static_cast<size_t>(grp) * p.max_splits * unit;
+  float* w = sm;
+  float* ls = sm + p.max_splits * N;
+  for (int t = x; t < ns * rows; t += 128) {
+    const int sidx = t / rows, n = t - sidx * rows;
+    w[sidx * N + n] = all[sidx * unit + N * 128 + n];
+    ls[sidx * N + n] = all[sidx * unit + N * 128 + N + n];
+  }
+  __syncthreads();
+  if (x < rows) {
+    float M = -CUDART_INF_F;
+    for (int sidx = 0; sidx < ns; ++sidx) M = fmaxf(M, w[sidx * N + x]);
+    float den = 0.f;
+    for (int sidx = 0; sidx < ns; ++sidx) {
+      const float e = exp2f((w[sidx * N + x] - M) * p.scale_log2);
+      w[sidx * N + x] = e;
+      den += e * ls[sidx * N + x];
+    }
+    const float inv = 1.0f / den;
+    for (int sidx = 0; sidx < ns; ++sidx) w[sidx * N + x] *= inv;
+  }
+  __syncthreads();
+  const size_t head_base = static_cast<size_t>(kvh) * p.G;
+  for (int n0 = 0; n0 < rows; n0 += 16) {
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    for (int sidx = 0; sidx < ns; ++sidx) {
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        v[k] = n0 + k < rows ? all[sidx * unit + (n0 + k) * 128 + x] : 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (n0 + k < rows) acc[k] += w[sidx * N + n0 + k] * v[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int n = n0 + k;
+      if (n >= rows) break;
+      const int i = rg * p.lsub + n / p.G;
+      if (i >= p.L) break;
+      const size_t o = ((static_cast<size_t>(b) * p.L + i) * p.Hq + head_base + n % p.G) * 128 + x;
+      p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[k]));
+    }
+  }
+}
+
 template <int N, int STAGES>
-size_t smem_bytes() {
+constexpr size_t smem_bytes() {
   return 1024 + static_cast<size_t>(N) * 256 + static_cast<size_t>(STAGES) * kStageBytes +
          static_cast<size_t>(2) * N * 256;
 }
 
-template <int N, int STAGES>
+template <int N, int STAGES, int CPS>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const AttnParams& prm, int grid, cudaStream_t stream) {
-  const size_t smem = smem_bytes<N, STAGES>();
+                     const AttnParams& prm, int num_sms, cudaStream_t stream) {
+  constexpr size_t smem = smem_bytes<N, STAGES>();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  attn_kernel<N, STAGES><<<grid, kThreads, smem, stream>>>(tq, tk, tv, prm);
+  attn_kernel<N, STAGES, CPS><<<num_sms * CPS, kThreads, smem, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();
 }
 
@@ -518,14 +810,18 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
   }
   const int rpg = pl.G * pl.lsub;
   pl.n_mma = rpg <= 16 ? 16 : rpg <= 32 ? 32 : rpg <= 64 ? 64 : 128;
-  pl.chunk_tiles = (static_cast<int>(kTmemCols) - pl.n_mma) / pl.n_mma;
-  pl.split_tokens = pl.n_mma <= 32 ? 1024 : 2048;
+  // tensor memory per CTA holds two S^T chunks and O^T
+  const int ctas_per_sm = pl.n_mma <= 32 ? 2 : 1;
+  pl.tmem_cols = 512 / ctas_per_sm;
+  pl.chunk_tiles = (pl.tmem_cols - pl.n_mma) / (2 * pl.n_mma);
+  const int chunks_per_split = pl.n_mma == 16 ? 1 : pl.n_mma == 32 ? 3 : pl.n_mma == 64 ? 4 : 16;
+  pl.split_tokens = pl.chunk_tiles * kTile * chunks_per_split;
+  if (pl.split_tokens > kMaxSplitTokens) pl.split_tokens = kMaxSplitTokens;
   const long long max_tok = static_cast<long long>(max_pages) * kPage;
   pl.max_splits = static_cast<int>((max_tok + pl.split_tokens - 1) / pl.split_tokens);
-  pl.tmem_cols = kTmemCols;
   const size_t groups = static_cast<size_t>(B) * Hkv * pl.row_groups;
   pl.part_bytes = groups * pl.max_splits * static_cast<size_t>(pl.n_mma) * 130 * sizeof(float);
-  pl.cnt_bytes = groups * sizeof(int);
+  pl.cnt_bytes = groups * sizeof(int) + 2 * sizeof(int);
   return pl;
 }
 
@@ -533,15 +829,17 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const int32_t* page_table,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
-                             const AttnPlan& plan, float* part, int* cnt, int* err,
+                             const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
                              cudaStream_t stream) {
   AttnParams prm;
   prm.page_table = page_table;
   prm.prefix_lens = prefix_lens;
   prm.out = out;
   prm.part = part;
-  prm.cnt = cnt;
+  prm.work = cnt;  // two words of scheduler state, then the split counters
+  prm.cnt = cnt + 2;
   prm.err = err;
+  prm.B = B;
   prm.L = L;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -555,16 +853,31 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   prm.max_splits = plan.max_splits;
   prm.chunk_tiles = plan.chunk_tiles;
   prm.scale_log2 = sm_scale * 1.4426950408889634f;
-  const long long grid_ll = static_cast<long long>(B) * Hkv * plan.max_splits * plan.row_groups;
-  if (grid_ll > 0x7FFFFFFFll) return cudaErrorInvalidValue;
-  const int grid = static_cast<int>(grid_ll);
+  const long long items = static_cast<long long>(B) * Hkv * plan.max_splits * plan.row_groups;
+  if (items > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  prm.total_items = static_cast<int>(items);
+  cudaError_t e;
   switch (plan.n_mma) {
-    case 16: return launch_t<16, 3>(tm_q, tm_k, tm_v, prm, grid, stream);
-    case 32: return launch_t<32, 2>(tm_q, tm_k, tm_v, prm, grid, stream);
-    case 64: return launch_t<64, 4>(tm_q, tm_k, tm_v, prm, grid, stream);
-    case 128: return launch_t<128, 3>(tm_q, tm_k, tm_v, prm, grid, stream);
+    case 16: e = launch_t<16, 3, 2>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
+    case 32: e = launch_t<32, 2, 2>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
+    case 64: e = launch_t<64, 5, 1>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
+    case 128: e = launch_t<128, 3, 1>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess || plan.max_splits <= 1) return e;
+  const size_t merge_smem = static_cast<size_t>(2) * plan.max_splits * plan.n_mma * sizeof(float);
+  if (merge_smem > 48 * 1024) {
+    static size_t attr = 0;
+    if (merge_smem > attr) {
+      e = cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(merge_smem));
+      if (e != cudaSuccess) return e;
+      attr = merge_smem;
+    }
+  }
+  const long long groups = static_cast<long long>(B) * Hkv * plan.row_groups;
+  attn_merge_kernel<<<static_cast<unsigned>(groups), 128, merge_smem, stream>>>(prm, plan.n_mma);
+  return cudaGetLastError();
 }
 
 }  // namespace bdlm

@@ -19,16 +19,18 @@ struct CommitPartial {
 };
 
 struct CommitPlan {
-  int S = 1;        // CTAs per logits row
-  int chunk = 0;    // elements per CTA (multiple of 8)
-  size_t part_bytes = 0, row_cnt_bytes = 0, blk_cnt_bytes = 0;
+  int S = 1;                  // work items per logits row
+  int chunk = 0;              // logits per work item (a multiple of 8)
+  long long total_items = 0;  // B * L * S
+  int grid = 1;               // CTAs (all resident at once)
+  size_t part_bytes = 0, row_cnt_bytes = 0, blk_cnt_bytes = 0, work_bytes = 0;
 };
 
-CommitPlan plan_commit(int B, int L, int V);
+CommitPlan plan_commit(int B, int L, int V, int num_sms);
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* row_cnt, int* blk_cnt, cudaStream_t stream);
+                          int* row_cnt, int* blk_cnt, int* work, cudaStream_t stream);
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention
@@ -51,7 +53,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const int32_t* page_table,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
-                             const AttnPlan& plan, float* part, int* cnt, int* err,
+                             const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
                              cudaStream_t stream);
 
 // ------------------------------------------------------------------ LM head

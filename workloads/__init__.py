@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 from typing import Optional
 
 import numpy as np
@@ -47,16 +48,36 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 
 
 def _normal_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
-    """N(0, std^2) drawn in float32 chunks, rounded once to bf16 bits."""
+    """N(0, std^2) drawn in float32, rounded once to bf16 bits.
+
+    One 63-bit seed is drawn from ``rng``; chunk k of 2^22 values then comes from its own
+    PCG64 stream seeded with (seed, k), so large arrays are drawn by several threads and
+    the result depends only on ``rng``'s state, never on the thread count."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    step = 1 << 24
-    for s in range(0, n, step):
+    seed = int(rng.integers(0, 2**63 - 1))
+    step = 1 << 22
+
+    def chunk(k):
+        s = k * step
         m = min(step, n - s)
-        v = rng.standard_normal(m, dtype=np.float32)
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, k])))
+        v = g.standard_normal(m, dtype=np.float32)
         if std != 1.0:
             v *= np.float32(std)
-        out[s:s + m] = f32_to_bf16_bits(v)
+        u = v.view(np.uint32)
+        u += (u >> 16) & 1
+        u += np.uint32(0x7FFF)
+        out[s:s + m] = (u >> 16).astype(np.uint16)
+
+    nchunks = (n + step - 1) // step
+    if nchunks <= 1:
+        for k in range(nchunks):
+            chunk(k)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(chunk, range(nchunks)))
     return out.reshape(shape)
 
 
