@@ -141,6 +141,26 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
                            float* conf_out, uint8_t* commit_out, bdlm_stream stream);
 
 /*
+ * bdlm_confidence_commit without any device allocation (the pages have no counterpart of
+ * this entry point; it exists for callers that cannot let the library allocate: an engine
+ * that reserved the GPU's memory up front for its own pools, or a latency-critical loop that
+ * cannot afford an allocation's implicit synchronisation).
+ *
+ * Same arguments, layouts and results as bdlm_confidence_commit.  Its scratch lives in a
+ * fixed device array of about 1 MiB inside the library, resident on every GPU that loads
+ * it until the process exits; nothing is allocated or freed per call.
+ *  - Limits: B*L <= 2048 and V <= 262144; larger problems return BDLM_ERR_UNSUPPORTED
+ *    before any launch.
+ *  - The first call on a device looks up the array's address with that device current;
+ *    make that first call before any stream capture.
+ *  - All calls share the array, which keeps the last call's contents: each call clears its
+ *    counters on `stream` first, and calls that overlap on the GPU race.
+ */
+int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uint8_t* mask, int B, int L,
+                                   int V, float threshold, float temperature, int32_t* tok_out,
+                                   float* conf_out, uint8_t* commit_out, bdlm_stream stream);
+
+/*
  * Mask update between denoising steps: mask[i] = 0 wherever commit[i] != 0.
  * Source: JetEngine notes, "Important Patterns" (each denoising step moves positions from
  * masked to unmasked).  mask, commit: [n] uint8.  n == 0 is a no-op.
