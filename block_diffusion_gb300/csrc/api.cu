@@ -174,13 +174,12 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
   if (rc) return rc;
   rc = ensure(&st->data, &st->data_cap, plan.part_bytes, false);
   if (rc) return rc;
-  int* work = st->commit_cnt;
-  int* row_cnt = st->commit_cnt + 2;
+  int* row_cnt = st->commit_cnt;
   int* blk_cnt = row_cnt + static_cast<size_t>(B) * L;
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
                                       conf_out, commit_out, plan,
                                       static_cast<bdlm::CommitPartial*>(st->data), row_cnt,
-                                      blk_cnt, work, static_cast<cudaStream_t>(stream));
+                                      blk_cnt, st->err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 

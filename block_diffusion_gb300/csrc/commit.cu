@@ -6,13 +6,15 @@
 // max softmax probability at temperature T; per block: commit every masked position at or
 // above the threshold, else the single most confident one.
 //
-// Layout of the work: each row of logits is cut into S items of kItem elements; warps take
-// items from a global atomic counter (any order, so the load balances whatever the mask),
-// stream the item with 16-byte loads keeping a running (max, sum of exp, first argmax) per
-// lane, merge the lanes with shuffles and write one partial.  The last warp to finish a row
-// (atomic counter) merges the row's S partials in item order, writes tok/conf, and the last
-// row to finish a block decides the block's commit.  Nothing waits on another warp; every
-// counter is reset by whoever consumed it, the work counter by the last warp to leave.
+// Layout of the work: the masked rows, laid end to end, form one sequence of T = n_masked * V
+// logits that is cut evenly across every warp of a persistent grid (each CTA first counts the
+// mask to learn n_masked and where each masked row sits).  A warp streams its range through a
+// private ring of three 4 KB shared-memory stages filled by bulk copies (one instruction per
+// stage), keeping a running (max, sum of exp, first argmax) per lane, and at the end of each
+// row segment merges its lanes with shuffles into one partial.  The last warp to finish a row
+// (atomic counter) merges the row's partials in a fixed order and writes tok/conf; the last
+// row to finish a block decides the block's commit.  Nothing waits on another warp or CTA;
+// every counter is reset by whoever consumed it.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -23,45 +25,59 @@
 namespace bdlm {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kUnroll = 8;   // 16-byte vectors in flight per lane
-constexpr int kItem = 8192;  // logits per work item (a multiple of 8)
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRing = 3;              // shared-memory stages per warp
+constexpr int kChunkBytes = 4096;     // bytes per stage
+constexpr int kChunk = kChunkBytes / 2;
+constexpr int kUnroll = 4;            // 16-byte vectors per lane per pass
 
 struct Acc {
   float m;    // running max (raw logit)
-  float s;    // sum of exp2((x - m) * c)
+  float s;    // sum of 2^((x - m) * c)
   int idx;    // first index of the max
 };
+
+// 2^x with the SFU's approximate base-2 exponential (relative error about 2^-22).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ Acc merge(Acc a, Acc b, float c) {
   if (b.m == -CUDART_INF_F) return a;
   if (a.m == -CUDART_INF_F) return b;
   Acc o;
   o.m = fmaxf(a.m, b.m);
-  o.s = a.s * exp2f((a.m - o.m) * c) + b.s * exp2f((b.m - o.m) * c);
+  o.s = a.s * ex2((a.m - o.m) * c) + b.s * ex2((b.m - o.m) * c);
   const int ia = (a.m == o.m) ? a.idx : 0x7FFFFFFF;
   const int ib = (b.m == o.m) ? b.idx : 0x7FFFFFFF;
   o.idx = min(ia, ib);
   return o;
 }
 
-// Adds elements x[0..n) (first index `base`) to the accumulator.
-__device__ __forceinline__ void absorb(Acc& a, const float* x, int n, int base, float c) {
+// Adds logits x[0..n) (index of x[0] is `base`) to the accumulator: the max of the group is
+// taken with a min/max tree; only when it beats the running max (rare once a row is under
+// way) is the first position of it located and the sum rescaled.
+template <int n>
+__device__ __forceinline__ void absorb(Acc& a, const float* x, int base, float c) {
   float lm = x[0];
-  int li = 0;
 #pragma unroll
-  for (int k = 1; k < n; ++k) {
-    if (x[k] > lm) { lm = x[k]; li = k; }
-  }
+  for (int k = 1; k < n; ++k) lm = fmaxf(lm, x[k]);
   if (lm > a.m) {
-    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * exp2f((a.m - lm) * c);
+    int li = n - 1;
+#pragma unroll
+    for (int k = n - 2; k >= 0; --k)
+      if (x[k] == lm) li = k;
+    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - lm) * c);
     a.m = lm;
     a.idx = base + li;
   }
   const float mc = a.m * c;
   float t = 0.f;
 #pragma unroll
-  for (int k = 0; k < n; ++k) t += exp2f(fmaf(x[k], c, -mc));
+  for (int k = 0; k < n; ++k) t += ex2(fmaf(x[k], c, -mc));
   a.s += t;
 }
 
@@ -105,108 +121,255 @@ __device__ __forceinline__ Acc warp_merge(Acc a, float c) {
   return a;
 }
 
-__global__ void __launch_bounds__(kThreads)
-commit_kernel(const uint16_t* __restrict__ logits, const uint8_t* __restrict__ mask, int L,
-              int V, int S, int total_items, int total_warps, float threshold, float c,
-              int32_t* __restrict__ tok_out, float* __restrict__ conf_out,
-              uint8_t* __restrict__ commit_out, CommitPartial* __restrict__ part,
-              int* __restrict__ row_cnt, int* __restrict__ blk_cnt, int* __restrict__ work) {
-  const int lane = threadIdx.x & 31;
-  int item = 0;
-  if (lane == 0) item = atomicAdd(work, 1);
-  item = __shfl_sync(0xffffffffu, item, 0);
-  while (item < total_items) {
-    int next = 0;
-    if (lane == 0) next = atomicAdd(work, 1);  // the next grab overlaps this item
-    const int r = item / S;
-    const int s = item - r * S;
-    const int b = r / L;
-    if (!mask[r]) {
-      if (s == 0 && lane == 0) {
-        tok_out[r] = -1;
-        conf_out[r] = -CUDART_INF_F;
-        __threadfence();
-        if (atomicAdd(blk_cnt + b, 1) == L - 1)
-          decide_block(b, L, mask, conf_out, commit_out, blk_cnt, threshold);
-      }
+struct ChunkMeta {
+  int r;         // row id
+  int k;         // masked-row index
+  int g0, g1;    // logits [g0, g1) of the row in this stage
+  int i0, i1;    // the 16-byte aligned interior [i0, i1) that the bulk copy brought in
+  int last;      // last stage of this row segment
+  int pad;
+};
+
+struct CommitArgs {
+  const uint16_t* logits;
+  const uint8_t* mask;
+  int R, L, V;
+  float threshold, c;
+  int32_t* tok_out;
+  float* conf_out;
+  uint8_t* commit_out;
+  CommitPartial* part;
+  int* row_cnt;
+  int* blk_cnt;
+  int* err;  // device error word (may be null)
+};
+
+// First logit (in the masked concatenation) of warp w out of W; a multiple of 8.
+__device__ __forceinline__ long long range_start(long long T, int W, int w) {
+  if (w >= W) return T;
+  return ((T * w) / W) & ~7ll;
+}
+// The warp whose range holds element e (an estimate from the even split, then corrected for
+// the rounding of range starts down to multiples of 8).
+__device__ __forceinline__ int warp_of(long long e, long long T, int W) {
+  int w = static_cast<int>((e * W) / T);
+  if (w >= W) w = W - 1;
+  while (w > 0 && range_start(T, W, w) > e) --w;
+  while (w + 1 < W && range_start(T, W, w + 1) <= e) ++w;
+  return w;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+commit_kernel(const CommitArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring_base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                  ~static_cast<uintptr_t>(127));
+  __shared__ uint64_t s_bar[kWarps][kRing];
+  __shared__ ChunkMeta s_meta[kWarps][kRing];
+  __shared__ int s_pref[kThreads + 1];
+  __shared__ int s_wsum[kWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- count the mask: s_pref[t] = masked rows before thread t's byte range
+  const int per = (a.R + kThreads - 1) / kThreads;
+  const int r_lo = min(a.R, tid * per), r_hi = min(a.R, r_lo + per);
+  int cnt = 0;
+  for (int r = r_lo; r < r_hi; ++r) cnt += a.mask[r] != 0;
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  if (tid < kWarps * kRing) mbar_init(&s_bar[tid / kRing][tid % kRing], 1);
+  fence_mbar_init();
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
+  s_pref[tid] = wbase + incl - cnt;
+  if (tid == kThreads - 1) s_pref[kThreads] = wbase + incl;
+  __syncthreads();
+  const long long n_masked = s_pref[kThreads];
+
+  // ---- unmasked rows: tok = -1, conf = -inf, and they count towards their block
+  for (int r = blockIdx.x * kThreads + tid; r < a.R; r += gridDim.x * kThreads) {
+    if (a.mask[r]) continue;
+    const int b = r / a.L;
+    a.tok_out[r] = -1;
+    a.conf_out[r] = -CUDART_INF_F;
+    __threadfence();
+    if (atomicAdd(a.blk_cnt + b, 1) == a.L - 1)
+      decide_block(b, a.L, a.mask, a.conf_out, a.commit_out, a.blk_cnt, a.threshold);
+  }
+
+  // ---- this warp's range of the masked concatenation
+  const long long T = n_masked * a.V;
+  const long long Wcap = static_cast<long long>(gridDim.x) * kWarps;
+  const int W = static_cast<int>(max(1ll, min(Wcap, T / kChunk)));
+  const int w = blockIdx.x * kWarps + warp;
+  if (w >= W || T == 0) return;
+  const long long e0 = range_start(T, W, w);
+  const long long e1 = range_start(T, W, w + 1);
+  if (e0 >= e1) return;
+
+  // row id of masked index k: binary search over the per-thread counts, then a byte scan
+  auto row_of = [&](long long k) -> int {
+    int lo = 0, hi = kThreads - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pref[mid] <= k) lo = mid; else hi = mid - 1;
+    }
+    int left = static_cast<int>(k - s_pref[lo]);
+    int r = min(a.R, lo * per);
+    for (;; ++r)
+      if (a.mask[r] && left-- == 0) break;
+    return r;
+  };
+
+  uint8_t* ring = ring_base + warp * (kRing * kChunkBytes);
+  uint64_t* bars = s_bar[warp];
+  ChunkMeta* meta = s_meta[warp];
+  // producer cursor (lane 0): masked row k, offset in that row, logits left in the range
+  long long left = e1 - e0;
+  int cur_k = static_cast<int>(e0 / a.V);
+  int cur_off = static_cast<int>(e0 - static_cast<long long>(cur_k) * a.V);
+  int cur_r = -1;
+  int issued = 0;
+  auto issue = [&](int slot) -> bool {  // lane 0; false when the range is exhausted
+    if (left <= 0) return false;
+    if (cur_r < 0) cur_r = row_of(cur_k);
+    const int seg_end = static_cast<int>(min(static_cast<long long>(a.V), cur_off + left));
+    const int q1 = min(seg_end, cur_off + kChunk);
+    ChunkMeta m;
+    m.r = cur_r;
+    m.k = cur_k;
+    m.g0 = cur_off;
+    m.g1 = q1;
+    const uint16_t* row = a.logits + static_cast<size_t>(cur_r) * a.V;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(row + m.g0);
+    const uintptr_t b1 = reinterpret_cast<uintptr_t>(row + m.g1);
+    const uintptr_t al0 = (b0 + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t al1 = b1 & ~static_cast<uintptr_t>(15);
+    if (al1 > al0) {
+      m.i0 = m.g0 + static_cast<int>((al0 - b0) >> 1);
+      m.i1 = m.g0 + static_cast<int>((al1 - b0) >> 1);
     } else {
-      Acc a{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
-      const int e0 = s * kItem;
-      const int e1 = min(V, e0 + kItem);
-      const uint16_t* row = logits + static_cast<size_t>(r) * V;
-      // scalar head up to a 16-byte boundary, vector body, scalar tail
-      const uintptr_t addr0 = reinterpret_cast<uintptr_t>(row + e0);
-      int head = static_cast<int>(((16 - (addr0 & 15)) & 15) >> 1);
-      head = min(head, e1 - e0);
-      const int vb = e0 + head;
-      const int nvec = (e1 - vb) >> 3;
-      const int tail0 = vb + nvec * 8;
-      if (lane < head) {
-        float x = bf16f(row[e0 + lane]);
-        absorb(a, &x, 1, e0 + lane, c);
-      }
-      const uint4* vp = reinterpret_cast<const uint4*>(row + vb);
-      for (int v0 = 0; v0 < nvec; v0 += kUnroll * 32) {
-        uint4 w[kUnroll];
+      m.i0 = m.i1 = m.g1;  // no aligned interior: lanes read the few logits directly
+    }
+    m.last = q1 == seg_end;
+    meta[slot] = m;
+    const uint32_t bytes = static_cast<uint32_t>((m.i1 - m.i0) * 2);
+    if (bytes) {
+      mbar_arrive_expect_tx(&bars[slot], bytes);
+      bulk_load(ring + slot * kChunkBytes, row + m.i0, bytes, &bars[slot]);
+    } else {
+      mbar_arrive(&bars[slot]);
+    }
+    left -= q1 - cur_off;
+    cur_off = q1;
+    if (cur_off == a.V) {
+      ++cur_k;
+      cur_off = 0;
+      cur_r = -1;
+    }
+    return true;
+  };
+  if (lane == 0) {
+    for (int i = 0; i < kRing; ++i)
+      if (issue(i)) ++issued;
+  }
+  issued = __shfl_sync(0xffffffffu, issued, 0);
+
+  int abort_flag = 0;
+  Acc acc{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+  for (int u = 0; u < issued; ++u) {
+    const int slot = u % kRing;
+    if (!mbar_wait(&bars[slot], (u / kRing) & 1, &abort_flag)) {
+      if (lane == 0 && a.err) atomicOr(a.err, BDLM_DEVERR_TIMEOUT);
+      break;
+    }
+    const ChunkMeta m = meta[slot];
+    const uint16_t* row = a.logits + static_cast<size_t>(m.r) * a.V;
+    const uint4* vp = reinterpret_cast<const uint4*>(ring + slot * kChunkBytes);
+    const int nvec = (m.i1 - m.i0) >> 3;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+      uint4 wv[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (v < nvec) w[u] = __ldcs(vp + v);
-        }
+      for (int q = 0; q < kUnroll; ++q) {
+        const int v = v0 + q * 32 + lane;
+        if (v < nvec) wv[q] = vp[v];
+      }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (v < nvec) {
-            float x[8];
-            x[0] = bf16_lo(w[u].x); x[1] = bf16_hi(w[u].x);
-            x[2] = bf16_lo(w[u].y); x[3] = bf16_hi(w[u].y);
-            x[4] = bf16_lo(w[u].z); x[5] = bf16_hi(w[u].z);
-            x[6] = bf16_lo(w[u].w); x[7] = bf16_hi(w[u].w);
-            absorb(a, x, 8, vb + v * 8, c);
-          }
-        }
-      }
-      if (tail0 + lane < e1) {
-        float x = bf16f(row[tail0 + lane]);
-        absorb(a, &x, 1, tail0 + lane, c);
-      }
-      a = warp_merge(a, c);
-      int last = 0;
-      if (lane == 0) {
-        part[static_cast<size_t>(r) * S + s] = CommitPartial{a.m, a.s, a.idx, 0};
-        __threadfence();
-        last = (atomicAdd(row_cnt + r, 1) == S - 1);
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        // merge the row's partials in a fixed order (lanes then tree) -> deterministic
-        __threadfence();
-        const volatile CommitPartial* pr = part + static_cast<size_t>(r) * S;
-        Acc f{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
-        for (int k0 = 0; k0 < S; k0 += 32) {
-          Acc q{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
-          if (k0 + lane < S) q = Acc{pr[k0 + lane].m, pr[k0 + lane].s, pr[k0 + lane].idx};
-          q = warp_merge(q, c);
-          f = merge(f, q, c);
-        }
-        if (lane == 0) {
-          tok_out[r] = f.idx;
-          conf_out[r] = 1.0f / f.s;
-          row_cnt[r] = 0;
-          __threadfence();
-          if (atomicAdd(blk_cnt + b, 1) == L - 1)
-            decide_block(b, L, mask, conf_out, commit_out, blk_cnt, threshold);
+      for (int q = 0; q < kUnroll; ++q) {
+        const int v = v0 + q * 32 + lane;
+        if (v < nvec) {
+          float x[8];
+          x[0] = bf16_lo(wv[q].x); x[1] = bf16_hi(wv[q].x);
+          x[2] = bf16_lo(wv[q].y); x[3] = bf16_hi(wv[q].y);
+          x[4] = bf16_lo(wv[q].z); x[5] = bf16_hi(wv[q].z);
+          x[6] = bf16_lo(wv[q].w); x[7] = bf16_hi(wv[q].w);
+          absorb<8>(acc, x, m.i0 + v * 8, a.c);
         }
       }
     }
-    item = __shfl_sync(0xffffffffu, next, 0);
-  }
-  // the last warp to leave resets the work counter for the next launch
-  if (lane == 0) {
+    // logits outside the aligned interior (at most 7 on each side)
+    if (m.g0 + lane < m.i0) {
+      float x = bf16f(row[m.g0 + lane]);
+      absorb<1>(acc, &x, m.g0 + lane, a.c);
+    }
+    if (m.i1 + lane < m.g1) {
+      float x = bf16f(row[m.i1 + lane]);
+      absorb<1>(acc, &x, m.i1 + lane, a.c);
+    }
+    __syncwarp();
+    if (lane == 0 && issue(slot)) ++issued;  // refill the stage just read
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    if (!m.last) continue;
+    // ---- end of a row segment: one partial per (warp, row); the warp that completes the
+    // row's element count finalizes it
+    Acc t = warp_merge(acc, a.c);
+    acc = Acc{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    const long long kv = static_cast<long long>(m.k) * a.V;
+    const int seg_len = static_cast<int>(min(kv + a.V, e1) - max(kv, e0));
+    int last = 0;
+    if (lane == 0) {
+      a.part[w + m.k] = CommitPartial{t.m, t.s, t.idx, 0};
+      __threadfence();
+      last = (atomicAdd(a.row_cnt + m.r, seg_len) + seg_len == a.V);
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    int first_w = 0, n_w = 0;
+    if (lane == 0) {
+      first_w = warp_of(kv, T, W);
+      n_w = warp_of(min(kv + a.V, T) - 1, T, W) - first_w + 1;
+    }
+    first_w = __shfl_sync(0xffffffffu, first_w, 0);
+    n_w = __shfl_sync(0xffffffffu, n_w, 0);
     __threadfence();
-    if (atomicAdd(work + 1, 1) == total_warps - 1) {
-      work[0] = 0;
-      work[1] = 0;
+    const volatile CommitPartial* pr = a.part + first_w + m.k;
+    Acc f{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    for (int j0 = 0; j0 < n_w; j0 += 32) {
+      Acc q{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+      if (j0 + lane < n_w) q = Acc{pr[j0 + lane].m, pr[j0 + lane].s, pr[j0 + lane].idx};
+      f = merge(f, warp_merge(q, a.c), a.c);
+    }
+    if (lane == 0) {
+      a.tok_out[m.r] = f.idx;
+      a.conf_out[m.r] = 1.0f / f.s;
+      a.row_cnt[m.r] = 0;
+      __threadfence();
+      const int b = m.r / a.L;
+      if (atomicAdd(a.blk_cnt + b, 1) == a.L - 1)
+        decide_block(b, a.L, a.mask, a.conf_out, a.commit_out, a.blk_cnt, a.threshold);
+    }
+  }
+  // drain: nothing may still be landing in this warp's stages when it exits
+  if (lane == 0) {
+    for (int u = max(0, issued - kRing); u < issued; ++u) {
+      int dummy = 0;
+      mbar_wait(&bars[u % kRing], (u / kRing) & 1, &dummy);
     }
   }
 }
@@ -221,37 +384,48 @@ __global__ void apply_commit_kernel(uint8_t* __restrict__ mask, const uint8_t* _
 
 CommitPlan plan_commit(int B, int L, int V, int num_sms) {
   CommitPlan p;
-  const long rows = static_cast<long>(B) * L;
-  p.S = (V + kItem - 1) / kItem;
-  p.chunk = kItem;
-  p.total_items = static_cast<long long>(rows) * p.S;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, commit_kernel, kThreads, 0) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  long long grid = static_cast<long long>(num_sms) * per_sm;
-  const long long warps_needed = (p.total_items + 0) / 1;
-  if (grid * (kThreads / 32) > warps_needed)
-    grid = (warps_needed + kThreads / 32 - 1) / (kThreads / 32);
-  if (grid < 1) grid = 1;
-  p.grid = static_cast<int>(grid);
-  p.part_bytes = static_cast<size_t>(rows) * p.S * sizeof(CommitPartial);
+  const long long rows = static_cast<long long>(B) * L;
+  p.grid = num_sms > 0 ? num_sms : 1;
+  p.S = 1;
+  p.chunk = kChunk;
+  p.total_items = rows;
+  p.smem_bytes = static_cast<size_t>(kWarps) * kRing * kChunkBytes + 128;
+  // one partial per (warp, masked row segment): slots w + k < warps + rows
+  p.part_bytes = static_cast<size_t>(p.grid * kWarps + rows) * sizeof(CommitPartial);
   p.row_cnt_bytes = static_cast<size_t>(rows) * sizeof(int);
   p.blk_cnt_bytes = static_cast<size_t>(B) * sizeof(int);
-  p.work_bytes = 2 * sizeof(int);
+  p.work_bytes = 0;
+  (void)V;
   return p;
 }
 
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* row_cnt, int* blk_cnt, int* work, cudaStream_t stream) {
-  (void)B;
-  const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
-  commit_kernel<<<plan.grid, kThreads, 0, stream>>>(
-      logits, mask, L, V, plan.S, static_cast<int>(plan.total_items), plan.grid * (kThreads / 32),
-      threshold, c, tok_out, conf_out, commit_out, part, row_cnt, blk_cnt, work);
+                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream) {
+  static size_t attr = 0;
+  if (plan.smem_bytes > attr) {
+    cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(plan.smem_bytes));
+    if (e != cudaSuccess) return e;
+    attr = plan.smem_bytes;
+  }
+  CommitArgs args;
+  args.logits = logits;
+  args.mask = mask;
+  args.R = B * L;
+  args.L = L;
+  args.V = V;
+  args.threshold = threshold;
+  args.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  args.tok_out = tok_out;
+  args.conf_out = conf_out;
+  args.commit_out = commit_out;
+  args.part = part;
+  args.row_cnt = row_cnt;
+  args.blk_cnt = blk_cnt;
+  args.err = err;
+  commit_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -11,7 +11,7 @@
 // Limits and behaviour (also stated in include/bdlm.h):
 //  * B * L <= kNoAllocMaxRows (2048) and V <= kNoAllocMaxVocab (262144); larger problems are
 //    rejected with BDLM_ERR_UNSUPPORTED before anything is launched.
-//  * The array (about 1 MiB) stays resident on every GPU that loads the library until the
+//  * The array (about 80 KiB) stays resident on every GPU that loads the library until the
 //    process exits.
 //  * The first call on a device looks the array's device address up (cudaGetSymbolAddress)
 //    with that device current; make that first call before any stream capture.
@@ -31,12 +31,12 @@ namespace {
 
 constexpr int kNoAllocMaxRows = 2048;
 constexpr int kNoAllocMaxVocab = 262144;
-constexpr int kNoAllocMaxItemsPerRow = (kNoAllocMaxVocab + 8191) / 8192;  // logits per item: 8192
-// layout: [work: 2][row counters: max rows][block counters: max rows] ints, then partials
-constexpr size_t kCounterInts = 2 + 2 * static_cast<size_t>(kNoAllocMaxRows);
+constexpr int kNoAllocMaxWarps = 16 * 256;  // the commit kernel runs 16 warps per SM
+// layout: [error word][row counters: max rows][block counters: max rows] ints, then partials
+constexpr size_t kCounterInts = 1 + 2 * static_cast<size_t>(kNoAllocMaxRows);
 constexpr size_t kCounterBytes = ((kCounterInts * sizeof(int)) + 255) / 256 * 256;
 constexpr size_t kPartialBytes =
-    static_cast<size_t>(kNoAllocMaxRows) * kNoAllocMaxItemsPerRow * sizeof(bdlm::CommitPartial);
+    static_cast<size_t>(kNoAllocMaxWarps + kNoAllocMaxRows) * sizeof(bdlm::CommitPartial);
 constexpr size_t kScratchBytes = kCounterBytes + kPartialBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -88,19 +88,17 @@ extern "C" int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uin
   int rc = scratch_address(&base, &sms);
   if (rc) return rc;
   const bdlm::CommitPlan plan = bdlm::plan_commit(B, L, V, sms);
-  if (plan.S > kNoAllocMaxItemsPerRow || plan.part_bytes > kPartialBytes)
-    return BDLM_ERR_UNSUPPORTED;
+  if (plan.part_bytes > kPartialBytes) return BDLM_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* counters = static_cast<int*>(base);
-  int* work = counters;
-  int* row_cnt = counters + 2;
+  int* err = counters;
+  int* row_cnt = counters + 1;
   int* blk_cnt = row_cnt + static_cast<size_t>(B) * L;
-  const size_t clear = (2 + static_cast<size_t>(B) * L + B) * sizeof(int);
+  const size_t clear = (1 + static_cast<size_t>(B) * L + B) * sizeof(int);
   if (cudaMemsetAsync(counters, 0, clear, s) != cudaSuccess) return BDLM_ERR_CUDA;
   auto* part = reinterpret_cast<bdlm::CommitPartial*>(static_cast<unsigned char*>(base) +
                                                       kCounterBytes);
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
-                                      conf_out, commit_out, plan, part, row_cnt, blk_cnt, work,
-                                      s);
+                                      conf_out, commit_out, plan, part, row_cnt, blk_cnt, err, s);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }

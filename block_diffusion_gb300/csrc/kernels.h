@@ -19,10 +19,11 @@ struct CommitPartial {
 };
 
 struct CommitPlan {
-  int S = 1;                  // work items per logits row
-  int chunk = 0;              // logits per work item (a multiple of 8)
-  long long total_items = 0;  // B * L * S
-  int grid = 1;               // CTAs (all resident at once)
+  int S = 1;                  // partial results per row and warp
+  int chunk = 0;              // logits per shared-memory stage
+  long long total_items = 0;  // rows
+  int grid = 1;               // CTAs (one per SM, persistent)
+  size_t smem_bytes = 0;
   size_t part_bytes = 0, row_cnt_bytes = 0, blk_cnt_bytes = 0, work_bytes = 0;
 };
 
@@ -30,7 +31,7 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms);
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* row_cnt, int* blk_cnt, int* work, cudaStream_t stream);
+                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream);
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention

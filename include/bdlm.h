@@ -147,7 +147,7 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
  * cannot afford an allocation's implicit synchronisation).
  *
  * Same arguments, layouts and results as bdlm_confidence_commit.  Its scratch lives in a
- * fixed device array of about 1 MiB inside the library, resident on every GPU that loads
+ * fixed device array of about 80 KiB inside the library, resident on every GPU that loads
  * it until the process exits; nothing is allocated or freed per call.
  *  - Limits: B*L <= 2048 and V <= 262144; larger problems return BDLM_ERR_UNSUPPORTED
  *    before any launch.
