@@ -52,7 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=W.seed_for(2))
     ap.add_argument("--quick", action="store_true",
-                    help="skip the e2e, full-round and CPU-baseline legs (profiling runs)")
+                    help="skip the end-to-end and CPU-baseline legs (profiling runs)")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of one CUDA graph per round")
     ap.add_argument("--compact-pool", action="store_true",
                     help="pool of exactly the referenced pages x1.25 (smaller device footprint)")
     return ap.parse_args(argv)
@@ -274,6 +276,37 @@ def time_round(rnd: Round, stream, steps: int, warmup: int, flush, barrier):
     return total, stage, wall
 
 
+def time_round_graph(rnd: Round, stream, steps: int, warmup: int, flush, barrier):
+    """Per-step times (ms) of the round replayed as one CUDA graph (captured once, after the
+    eager warm-up has sized the library's workspace); L2 flushed before every replay."""
+    torch = rnd.torch
+    for _ in range(warmup):
+        rnd.reset_mask(stream)
+        flush(stream)
+        rnd.step(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        rnd.step(stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for k in range(steps):
+            rnd.reset_mask(stream)
+            flush(stream)
+            evs[k][0].record(stream)
+            graph.replay()
+            evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    return np.array([a.elapsed_time(b) for a, b in evs]), wall
+
+
 def e2e_round(lib, a, ci, device, steps, warmup):
     """Same round through the C-ABI from pinned host buffers: every step copies its inputs
     host->device (q, the referenced K/V pages as a compact pool, page table, prefix lengths,
@@ -418,9 +451,16 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=device)
     sampler = ClockSampler(local)
     sampler.start()
-    total, stage, wall = time_round(rnd, stream, args.steps, max(3, args.warmup), flush, barrier)
+    if args.eager:
+        total, stage, wall = time_round(rnd, stream, args.steps, max(3, args.warmup), flush,
+                                        barrier)
+    else:
+        total, wall = time_round_graph(rnd, stream, args.steps, max(3, args.warmup), flush,
+                                       barrier)
     clocks = sampler.stop()
     assert bd.bdlm_device_error() == 0, "device error during the timed round"
+    eager_total, stage, _ = time_round(rnd, stream, max(20, min(args.steps, 200)), 3, flush,
+                                       barrier)
 
     ms = float(total.mean())
     if world > 1:
@@ -455,19 +495,22 @@ def run_ours(args, rank, world, local):
                        "seed": args.seed},
             "clocks": clocks,
             "gpu_launches": rnd.launches_per_step() * args.steps,
+            "launch": "eager" if args.eager else "cuda_graph",
+            "eager_ms_per_step": float(eager_total.mean()),
             "stages_ms": {"attention": attn_ms, "commit": commit_ms,
-                          "mask_update": float(stage[:, 3].mean())},
+                          "mask_update": float(stage[:, 3].mean()),
+                          "note": "eager launches; each stage includes its launch gap"},
             "commit_hbm": {"achieved": commit_gbs, "unit": "GB/s",
                            "frac": commit_gbs / peaks["hbm_gbs"], "algorithmic_bytes": commit_bytes},
             "roofline": roofline,
             "attention_tflops": attn_flops / (attn_ms / 1e3) / 1e12,
             "wall_s": wall}
 
-    if not args.quick and rank == 0:
+    if rank == 0:
         # the same round with the selective LM head in the path (all rows of the hot path)
         full = Round(bd, a, ci, device, with_lm_head=True, lm_seed=args.seed + 1)
-        ftotal, fstage, _ = time_round(full, stream, max(20, args.steps // 4), 3, flush,
-                                       lambda: None)
+        f_steps = max(3, min(args.steps, max(20, args.steps // 4)))
+        ftotal, fstage, _ = time_round(full, stream, f_steps, 3, flush, lambda: None)
         lm_ms = float(fstage[:, 1].mean())
         H, n_act = full.H, full.n_act
         lm_flops = 2.0 * n_act * H * ci.V
@@ -486,9 +529,10 @@ def run_ours(args, rank, world, local):
                                  "frac_tensor": tf / peaks["bf16_tflops"],
                                  "achieved_gbs": lm_bytes / (lm_ms / 1e3) / 1e9,
                                  "frac_hbm": lm_bytes / (lm_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
-            "gpu_launches": full.launches_per_step() * max(20, args.steps // 4)}
+            "gpu_launches": full.launches_per_step() * f_steps}
         del full
         torch.cuda.empty_cache()
+    if not args.quick and rank == 0:
         e2e_ms, h2d, d2h = e2e_round(bd, a, ci, device, max(10, args.steps // 20), 3)
         line["e2e"] = {"value": a.B * a.L / (e2e_ms / 1e3), "unit": UNIT,
                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

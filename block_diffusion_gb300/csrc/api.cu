@@ -203,7 +203,8 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
     return BDLM_ERR_INVALID;
   if (d.B == 0) return BDLM_OK;
   if (!q || !k_pages || !v_pages || !page_table || !prefix_lens || !out) return BDLM_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return BDLM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return BDLM_ERR_INVALID;
   if (static_cast<long long>(d.B) * d.L * d.Hq > 0x7FFFFFFFll ||
       static_cast<long long>(d.B) * d.max_pages_per_seq > 0x7FFFFFFFll ||
       static_cast<long long>(d.max_pages_per_seq) * d.page_size > 0x7FFFFFFFll)

@@ -167,6 +167,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();  // inputs written by the previous grid on the stream are visible from here
   const uint32_t tmem = tmem_base;
   const uint32_t tO = tmem + static_cast<uint32_t>(2 * p.chunk_tiles * N);
 
@@ -331,6 +332,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
     }
     if (lane == 0) {
+      griddep_launch_dependents();  // this CTA takes no more work
       // the last CTA to finish taking work resets the counter for the next launch
       __threadfence();
       if (atomicAdd(p.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
@@ -703,70 +705,98 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
 // Merges the splits of every (sequence, KV head, row group) whose KV range was cut into more
 // than one item: out = sum_s w_s O_s with w_s = exp(m_s - M) / sum_s exp(m_s - M) l_s.
-// One CTA (128 threads, one per head dim) per group.
-__global__ void __launch_bounds__(128)
+// One warp per (group, query row): lane s fetches split s's (m, l), the weights come from
+// warp shuffles, and each lane then sums a float4 of head dims over the splits with
+// independent loads (two round trips to memory in all).
+__global__ void __launch_bounds__(256)
 attn_merge_kernel(const AttnParams p, int N) {
-  extern __shared__ float sm[];  // [max_splits][N] weights, then [max_splits][N] l
-  const int grp = blockIdx.x;
-  const int rg = grp % p.row_groups;
-  const int bk = grp / p.row_groups;
-  const int kvh = bk % p.Hkv;
-  const int b = bk / p.Hkv;
+  const int lane = threadIdx.x & 31;
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int rows = p.rows_per_group;
+  const long long groups = static_cast<long long>(p.B) * p.Hkv * p.row_groups;
+  if (wid >= groups * rows) return;
+  const int n = static_cast<int>(wid % rows);
+  const long long grp = wid / rows;
+  const int rg = static_cast<int>(grp % p.row_groups);
+  const long long bk = grp / p.row_groups;
+  const int kvh = static_cast<int>(bk % p.Hkv);
+  const int b = static_cast<int>(bk / p.Hkv);
+  const int i = rg * p.lsub + n / p.G;
+  if (i >= p.L) return;
   const int prefix = p.prefix_lens[b];
   const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
   long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
   if (kvl > max_tok) kvl = max_tok;
   const int ns = static_cast<int>((kvl + p.split_tokens - 1) / p.split_tokens);
   if (ns <= 1) return;
-  const int rows = p.rows_per_group;
-  const int x = threadIdx.x;
   const size_t unit = static_cast<size_t>(N) * 130;
   const float* all = p.part + static_cast<size_t>(grp) * p.max_splits * unit;
-  float* w = sm;
-  float* ls = sm + p.max_splits * N;
-  for (int t = x; t < ns * rows; t += 128) {
-    const int sidx = t / rows, n = t - sidx * rows;
-    w[sidx * N + n] = all[sidx * unit + N * 128 + n];
-    ls[sidx * N + n] = all[sidx * unit + N * 128 + N + n];
-  }
-  __syncthreads();
-  if (x < rows) {
+  // the row's maximum and normaliser over all splits: lane s holds split s's (m, l); beyond
+  // 32 splits the lanes walk the list in steps of 32
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (ns <= 32) {
+    float ml = -CUDART_INF_F, ll = 0.f;
+    if (lane < ns) {
+      ml = __ldcg(all + lane * unit + N * 128 + n);
+      ll = __ldcg(all + lane * unit + N * 128 + N + n);
+    }
+    float M = ml;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float e = lane < ns ? exp2f((ml - M) * p.scale_log2) : 0.f;
+    float den = e * ll;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    const float wl = e / den;
+#pragma unroll 4
+    for (int j = 0; j < ns; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wl, j);
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(all + j * unit + n * 128) + lane);
+      acc.x += wj * o.x;
+      acc.y += wj * o.y;
+      acc.z += wj * o.z;
+      acc.w += wj * o.w;
+    }
+  } else {
     float M = -CUDART_INF_F;
-    for (int sidx = 0; sidx < ns; ++sidx) M = fmaxf(M, w[sidx * N + x]);
+    for (int s0 = 0; s0 < ns; s0 += 32)
+      if (s0 + lane < ns) M = fmaxf(M, __ldcg(all + (s0 + lane) * unit + N * 128 + n));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float den = 0.f;
-    for (int sidx = 0; sidx < ns; ++sidx) {
-      const float e = exp2f((w[sidx * N + x] - M) * p.scale_log2);
-      w[sidx * N + x] = e;
-      den += e * ls[sidx * N + x];
-    }
+    for (int s0 = 0; s0 < ns; s0 += 32)
+      if (s0 + lane < ns) {
+        const float* pm = all + (s0 + lane) * unit + N * 128;
+        den += exp2f((__ldcg(pm + n) - M) * p.scale_log2) * __ldcg(pm + N + n);
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
     const float inv = 1.0f / den;
-    for (int sidx = 0; sidx < ns; ++sidx) w[sidx * N + x] *= inv;
-  }
-  __syncthreads();
-  const size_t head_base = static_cast<size_t>(kvh) * p.G;
-  for (int n0 = 0; n0 < rows; n0 += 16) {
-    float acc[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    for (int sidx = 0; sidx < ns; ++sidx) {
-      float v[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        v[k] = n0 + k < rows ? all[sidx * unit + (n0 + k) * 128 + x] : 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (n0 + k < rows) acc[k] += w[sidx * N + n0 + k] * v[k];
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int n = n0 + k;
-      if (n >= rows) break;
-      const int i = rg * p.lsub + n / p.G;
-      if (i >= p.L) break;
-      const size_t o = ((static_cast<size_t>(b) * p.L + i) * p.Hq + head_base + n % p.G) * 128 + x;
-      p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[k]));
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const int cnt = min(32, ns - s0);
+      float wl = 0.f;
+      if (lane < cnt)
+        wl = exp2f((__ldcg(all + (s0 + lane) * unit + N * 128 + n) - M) * p.scale_log2) * inv;
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wl, j);
+        const float4 o =
+            __ldcg(reinterpret_cast<const float4*>(all + (s0 + j) * unit + n * 128) + lane);
+        acc.x += wj * o.x;
+        acc.y += wj * o.y;
+        acc.z += wj * o.z;
+        acc.w += wj * o.w;
+      }
     }
   }
+  const size_t o = ((static_cast<size_t>(b) * p.L + i) * p.Hq + static_cast<size_t>(kvh) * p.G +
+                    n % p.G) * 128 + 4 * lane;
+  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
+  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
+  *reinterpret_cast<uint2*>(p.out + o) = make_uint2(lo, hi);
 }
 
 template <int N, int STAGES>
@@ -787,8 +817,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  attn_kernel<N, STAGES, CPS><<<num_sms * CPS, kThreads, smem, stream>>>(tq, tk, tv, prm);
-  return cudaGetLastError();
+  return launch_pdl(attn_kernel<N, STAGES, CPS>, dim3(num_sms * CPS), dim3(kThreads), smem,
+                    stream, tq, tk, tv, prm);
 }
 
 }  // namespace
@@ -865,18 +895,10 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess || plan.max_splits <= 1) return e;
-  const size_t merge_smem = static_cast<size_t>(2) * plan.max_splits * plan.n_mma * sizeof(float);
-  if (merge_smem > 48 * 1024) {
-    static size_t attr = 0;
-    if (merge_smem > attr) {
-      e = cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(merge_smem));
-      if (e != cudaSuccess) return e;
-      attr = merge_smem;
-    }
-  }
-  const long long groups = static_cast<long long>(B) * Hkv * plan.row_groups;
-  attn_merge_kernel<<<static_cast<unsigned>(groups), 128, merge_smem, stream>>>(prm, plan.n_mma);
+  const long long warps = static_cast<long long>(B) * Hkv * plan.row_groups * plan.G * plan.lsub;
+  e = launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0,
+                 stream, prm, plan.n_mma);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -226,6 +226,8 @@ commit_kernel(const CommitArgs a) {
   __shared__ int s_pref[kThreads + 1];
   __shared__ int s_wsum[kWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();
+  griddep_launch_dependents();
 
   // ---- count the mask: s_pref[t] = masked rows before thread t's byte range
   const int per = (a.R + kThreads - 1) / kThreads;
@@ -429,6 +431,8 @@ commit_kernel(const CommitArgs a) {
 
 __global__ void apply_commit_kernel(uint8_t* __restrict__ mask, const uint8_t* __restrict__ commit,
                                     int n) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n && commit[i]) mask[i] = 0;
 }
@@ -455,7 +459,8 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms) {
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream) {
+                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream,
+                          bool programmatic) {
   static size_t attr = 0;
   if (plan.smem_bytes > attr) {
     cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -478,13 +483,16 @@ cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, in
   args.row_cnt = row_cnt;
   args.blk_cnt = blk_cnt;
   args.err = err;
-  commit_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(args);
-  return cudaGetLastError();
+  if (!programmatic) {
+    commit_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(args);
+    return cudaGetLastError();
+  }
+  return launch_pdl(commit_kernel, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream, args);
 }
 
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream) {
-  apply_commit_kernel<<<(n + 255) / 256, 256, 0, stream>>>(mask, commit, n);
-  return cudaGetLastError();
+  return launch_pdl(apply_commit_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, mask,
+                    commit, n);
 }
 
 }  // namespace bdlm

@@ -99,6 +99,7 @@ extern "C" int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uin
   auto* part = reinterpret_cast<bdlm::CommitPartial*>(static_cast<unsigned char*>(base) +
                                                       kCounterBytes);
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
-                                      conf_out, commit_out, plan, part, row_cnt, blk_cnt, err, s);
+                                      conf_out, commit_out, plan, part, row_cnt, blk_cnt, err, s,
+                                      /*programmatic=*/false);  // ordered after the memset
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }

@@ -10,6 +10,25 @@
 
 namespace bdlm {
 
+// Launches `kernel` with a programmatic dependency on the previous work of `stream`: its
+// CTAs may start while the predecessor drains, and wait (griddepcontrol.wait) before they
+// read anything the predecessor writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------------ commit
 struct CommitPartial {
   float m;
@@ -31,7 +50,8 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms);
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream);
+                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream,
+                          bool programmatic = true);
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention

@@ -44,6 +44,8 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ hidden,
                                    const int32_t* __restrict__ active_idx, int n_active,
                                    int n_rows, int H, uint16_t* __restrict__ gathered,
                                    int* __restrict__ err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = blockIdx.y;
   const int r = active_idx[i];
   const bool bad = r < 0 || r >= n_rows;
@@ -94,6 +96,7 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();
   const uint32_t tmem = tmem_base;
 
   if (warp == 0) {
@@ -118,6 +121,7 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
           }
         }
       }
+      griddep_launch_dependents();  // every tile of this CTA is being loaded
       if (!ok) {
         int dummy = 0;
         for (int s = 0; s < kStages; ++s) mbar_wait(&bar_full[s], ph ^ (s < st ? 0 : 1), &dummy);
@@ -226,8 +230,7 @@ cudaError_t launch_bn(const CUtensorMap& tw, const CUtensorMap& th, const LmPara
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  lm_head_kernel<BN><<<grid, kThreads, smem, stream>>>(tw, th, prm);
-  return cudaGetLastError();
+  return launch_pdl(lm_head_kernel<BN>, dim3(grid), dim3(kThreads), smem, stream, tw, th, prm);
 }
 
 }  // namespace
@@ -250,9 +253,8 @@ cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* active_idx
   const int nv = H / 8;
   const int threads = nv < 256 ? ((nv + 31) / 32) * 32 : 256;
   dim3 grid((nv + threads - 1) / threads, n_active);
-  gather_rows_kernel<<<grid, threads, 0, stream>>>(hidden, active_idx, n_active, n_rows, H,
-                                                   gathered, err);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, grid, dim3(threads), 0, stream, hidden, active_idx,
+                    n_active, n_rows, H, gathered, err);
 }
 
 cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,

@@ -91,7 +91,8 @@ typedef struct {
  *   v_pages      [num_pages, page_size, Hkv, D]        bf16 (16-byte aligned)
  *   page_table   [B, max_pages_per_seq]                int32 (unused entries are ignored)
  *   prefix_lens  [B]                                   int32
- *   out          [B, L, Hq, D]                         bf16 (fp32 accumulation, one rounding)
+ *   out          [B, L, Hq, D]                         bf16 (16-byte aligned; fp32
+ *                                                      accumulation, one rounding)
  * `L` must equal desc->L (it is the block length of this round).
  * Slots past kv_len in a sequence's last page are never used, whatever they hold.
  */
