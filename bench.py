@@ -67,6 +67,29 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank denoises its own batch: a distinct, reproducible seed per rank."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of `x` over all ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = (torch.device("cuda", torch.cuda.current_device())
+           if dist.get_backend() == "nccl" else torch.device("cpu"))
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -89,8 +112,9 @@ def profile_traffic(name: str, src: str):
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     rec = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("source_sha256", "traffic_bytes_per_launch")):
-            k, v = line.strip().lstrip("-* ").split(":", 1)
+        line = line.strip().lstrip("-* ")
+        if ":" in line and line.startswith(("source_sha256", "traffic_bytes_per_launch")):
+            k, v = line.split(":", 1)
             rec[k.strip()] = v.strip().strip("`")
     if rec.get("source_sha256") != digest:
         return None
@@ -446,7 +470,7 @@ def run_ours(args, rank, world, local):
             flush_buf.fill_(rank & 0xFF)
 
     # each rank denoises its own batch of 128 sequences (data parallel, no collective)
-    c, a, ci = make_workload(args.seed + 7919 * rank, compact_pool=args.compact_pool)
+    c, a, ci = make_workload(rank_seed(args.seed, rank), compact_pool=args.compact_pool)
     rnd = Round(bd, a, ci, device)
     stream = torch.cuda.Stream(device=device)
     sampler = ClockSampler(local)
@@ -463,15 +487,8 @@ def run_ours(args, rank, world, local):
                                        barrier)
 
     ms = float(total.mean())
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    else:
-        ms_max = ms
-    units = a.B * a.L * world
-    value = units / (ms_max / 1e3)
+    ms_max = max_over_ranks(ms, world)
+    value = job_value(a.B * a.L, world, ms_max)
 
     attn_bytes, commit_bytes, attn_flops = algorithmic_bytes(a, ci)
     attn_ms = float(stage[:, 0].mean())
@@ -532,13 +549,17 @@ def run_ours(args, rank, world, local):
             "gpu_launches": full.launches_per_step() * f_steps}
         del full
         torch.cuda.empty_cache()
-    if not args.quick and rank == 0:
+    if not args.quick:
+        barrier()
         e2e_ms, h2d, d2h = e2e_round(bd, a, ci, device, max(10, args.steps // 20), 3)
-        line["e2e"] = {"value": a.B * a.L / (e2e_ms / 1e3), "unit": UNIT,
+        e2e_max = max_over_ranks(e2e_ms, world)
+        line["e2e"] = {"value": job_value(a.B * a.L, world, e2e_max), "unit": UNIT,
                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                       "ms_per_step": e2e_ms,
-                       "note": "K/V copied as a compact pool of the referenced pages"}
-        line["cpu_baseline"] = cpu_baseline(a, ci)
+                       "ms_per_step": e2e_max,
+                       "note": "per rank and step; K/V copied as a compact pool of the "
+                               "referenced pages"}
+        if rank == 0:
+            line["cpu_baseline"] = cpu_baseline(a, ci)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
