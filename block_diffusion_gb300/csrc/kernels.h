@@ -79,7 +79,8 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
 
 // ------------------------------------------------------------------ LM head
 struct LmHeadPlan {
-  int bn = 256;          // UMMA N (gathered rows per tile)
+  int bn = 256;          // UMMA N (gathered rows per tile), a multiple of 16
+  int bn_max = 256;      // shared-memory ring layout: 64, 128 or 256 rows per row stage
   int m_tiles = 0, n_tiles = 0, grid = 0;
   size_t smem_bytes = 0;
   size_t gather_bytes = 0;

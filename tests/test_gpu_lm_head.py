@@ -39,7 +39,8 @@ def check(lib, inp, rows_sample=None, cols=None):
 
 @pytest.mark.parametrize("n_rows,n_act,H,V", [(40, 23, 256, 1000), (8, 1, 64, 136),
                                               (300, 300, 512, 2048), (700, 600, 128, 4104),
-                                              (130, 129, 2560, 640), (64, 64, 72, 128 + 8)])
+                                              (130, 129, 2560, 640), (64, 64, 72, 128 + 8),
+                                              (100, 100, 320, 1000), (512, 256, 2560, 1288)])
 def test_small_shapes(lib, n_rows, n_act, H, V):
     rng = np.random.default_rng(n_rows + H + V)
     act = np.sort(rng.choice(n_rows, size=n_act, replace=False)).astype(np.int32)
