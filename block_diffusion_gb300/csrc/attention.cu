@@ -224,6 +224,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       ok = __shfl_sync(0xffffffffu, ok, 0);
       return true;
     };
+    // K/V pages are read exactly once: first to leave L2, so that the split partials (and Q)
+    // stay resident for the merge
+    const uint64_t kv_policy = l2_policy_evict_first();
     // Loads the Q tile of item `it` (sequence number s) into the single Q buffer once the
     // previous item's S^T MMAs are done with it.  Lane 0.
     int q_loads = 0;
@@ -268,8 +271,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         __syncwarp();
         if (id >= 0) {
-          tma_load_4d(stage + lane * 2048, tm, &bar_full[st], 0, it.kvh, 0, id);
-          tma_load_4d(stage + kHalfBytes + lane * 2048, tm, &bar_full[st], 64, it.kvh, 0, id);
+          tma_load_4d_hint(stage + lane * 2048, tm, &bar_full[st], 0, it.kvh, 0, id, kv_policy);
+          tma_load_4d_hint(stage + kHalfBytes + lane * 2048, tm, &bar_full[st], 64, it.kvh, 0, id,
+                           kv_policy);
         }
         if (++st == STAGES) {
           st = 0;
@@ -668,6 +672,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           const size_t unit = static_cast<size_t>(N) * 130;
           const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
           float* mine = p.part + (grp * p.max_splits + it.split) * unit;
+          const uint64_t keep = l2_policy_evict_last();  // read back by the merge soon
 #pragma unroll
           for (int cg = 0; cg < N / 16; ++cg) {
             uint32_t r[16];
@@ -675,11 +680,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tmem_wait_ld();
             tmem_regs_ready(r);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) mine[(cg * 16 + k) * 128 + x] = __uint_as_float(r[k]);
+            for (int k = 0; k < 16; ++k)
+              st_global_hint(mine + (cg * 16 + k) * 128 + x, __uint_as_float(r[k]), keep);
           }
           if (x < N) {
-            mine[N * 128 + x] = s_m[x];
-            mine[N * 128 + N + x] = s_l[x];
+            st_global_hint(mine + N * 128 + x, s_m[x], keep);
+            st_global_hint(mine + N * 128 + N + x, s_l[x], keep);
           }
         }
         // O^T and the item descriptor are free for the next item
@@ -708,39 +714,44 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // One warp per (group, query row): lane s fetches split s's (m, l), the weights come from
 // warp shuffles, and each lane then sums a float4 of head dims over the splits with
 // independent loads (two round trips to memory in all).
+// Grid: x = group (sequence, KV head, row group), y = blocks of 8 query rows; 32-bit index
+// math only (the kernel is issue-bound when every warp decomposes a 64-bit index).
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const AttnParams p, int N) {
   const int lane = threadIdx.x & 31;
   griddep_wait();
   griddep_launch_dependents();
-  const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int rows = p.rows_per_group;
-  const long long groups = static_cast<long long>(p.B) * p.Hkv * p.row_groups;
-  if (wid >= groups * rows) return;
-  const int n = static_cast<int>(wid % rows);
-  const long long grp = wid / rows;
-  const int rg = static_cast<int>(grp % p.row_groups);
-  const long long bk = grp / p.row_groups;
-  const int kvh = static_cast<int>(bk % p.Hkv);
-  const int b = static_cast<int>(bk / p.Hkv);
+  const int n = static_cast<int>(blockIdx.y) * 8 + (threadIdx.x >> 5);
+  if (n >= p.rows_per_group) return;
+  const unsigned grp = blockIdx.x;
+  const int rg = static_cast<int>(grp % static_cast<unsigned>(p.row_groups));
+  const unsigned bk = grp / static_cast<unsigned>(p.row_groups);
+  const int kvh = static_cast<int>(bk % static_cast<unsigned>(p.Hkv));
+  const int b = static_cast<int>(bk / static_cast<unsigned>(p.Hkv));
   const int i = rg * p.lsub + n / p.G;
   if (i >= p.L) return;
+  const size_t unit = static_cast<size_t>(N) * 130;
+  const float* all = p.part + static_cast<size_t>(grp) * p.max_splits * unit;
+  // lane s fetches split s's (m, l) together with the prefix length (slots of splits that
+  // turn out not to exist are ignored), so the split count costs no extra round trip
+  float ml = -CUDART_INF_F, ll = 0.f;
+  if (lane < p.max_splits && lane < 32) {
+    ml = __ldcg(all + lane * unit + N * 128 + n);
+    ll = __ldcg(all + lane * unit + N * 128 + N + n);
+  }
   const int prefix = p.prefix_lens[b];
   const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
   long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
   if (kvl > max_tok) kvl = max_tok;
   const int ns = static_cast<int>((kvl + p.split_tokens - 1) / p.split_tokens);
   if (ns <= 1) return;
-  const size_t unit = static_cast<size_t>(N) * 130;
-  const float* all = p.part + static_cast<size_t>(grp) * p.max_splits * unit;
   // the row's maximum and normaliser over all splits: lane s holds split s's (m, l); beyond
   // 32 splits the lanes walk the list in steps of 32
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (ns <= 32) {
-    float ml = -CUDART_INF_F, ll = 0.f;
-    if (lane < ns) {
-      ml = __ldcg(all + lane * unit + N * 128 + n);
-      ll = __ldcg(all + lane * unit + N * 128 + N + n);
+    if (lane >= ns) {
+      ml = -CUDART_INF_F;
+      ll = 0.f;
     }
     float M = ml;
 #pragma unroll
@@ -895,8 +906,9 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess || plan.max_splits <= 1) return e;
-  const long long warps = static_cast<long long>(B) * Hkv * plan.row_groups * plan.G * plan.lsub;
-  e = launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0,
+  const long long groups = static_cast<long long>(B) * Hkv * plan.row_groups;
+  const int row_blocks = (plan.G * plan.lsub + 7) / 8;
+  e = launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>(groups), row_blocks), dim3(256), 0,
                  stream, prm, plan.n_mma);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -31,7 +31,8 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRing = 3;              // shared-memory stages per warp
 constexpr int kChunkBytes = 4096;     // bytes per stage
 constexpr int kChunk = kChunkBytes / 2;
-constexpr int kUnroll = 4;            // 16-byte vectors per lane per pass
+constexpr int kUnroll = 4;            // 16-byte vectors per lane per group of 32 logits
+constexpr int kMaskSmem = 8192;       // masks of up to this many rows are copied to smem
 
 struct Acc {
   float m;    // running max (raw logit)
@@ -58,84 +59,122 @@ __device__ __forceinline__ Acc merge(Acc a, Acc b, float c) {
   return o;
 }
 
-// Adds logits x[0..n) (index of x[0] is `base`) to the accumulator: the max of the group is
-// taken with a min/max tree; only when it beats the running max (rare once a row is under
-// way) is the first position of it located and the sum rescaled.
-template <int n>
-__device__ __forceinline__ void absorb(Acc& a, const float* x, int base, float c) {
-  float lm = x[0];
-#pragma unroll
-  for (int k = 1; k < n; ++k) lm = fmaxf(lm, x[k]);
-  if (lm > a.m) {
-    int li = n - 1;
-#pragma unroll
-    for (int k = n - 2; k >= 0; --k)
-      if (x[k] == lm) li = k;
-    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - lm) * c);
-    a.m = lm;
-    a.idx = base + li;
-  }
-  const float mc = a.m * c;
-  float t = 0.f;
-#pragma unroll
-  for (int k = 0; k < n; ++k) t += ex2(fmaf(x[k], c, -mc));
-  a.s += t;
-}
-
-// 2^x on the FMA pipe (for x <= 0), so that part of the exponentials bypass the SFU: x = j + f
-// with j = round(x) and f in [-1/2, 1/2]; 2^f from a degree-5 polynomial fitted here to the
-// relative error on that interval (max relative error about 2.3e-7 in fp32 Horner form);
-// 2^j is added to the exponent bits.  x is clamped at -125 so 2^j stays a normal number.
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -125.0f);
-  const float t = x + 12582912.0f;  // 1.5 * 2^23: the low mantissa bits become round(x)
-  const float f = x - (t - 12582912.0f);
-  float q = 1.3276466634124517e-3f;
-  q = fmaf(q, f, 9.675540961325169e-3f);
-  q = fmaf(q, f, 5.550713464617729e-2f);
-  q = fmaf(q, f, 2.4022120237350464e-1f);
-  q = fmaf(q, f, 6.931469440460205e-1f);
-  q = fmaf(q, f, 1.0000001192092896f);
-  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
-}
-
 constexpr uint32_t kBf16NegInfPair = 0xFF80FF80u;
 
-// Adds 32 logits held as 16 packed bf16 pairs to the accumulator: element e is the low
-// (e even) or high (e odd) half of w[e / 2], and its logit index is idx[e / 8] + e % 8.  The
-// group max is taken on the packed pairs with one branch per group; the 32 exponentials are
-// independent (a quarter of them on the FMA pipe) and summed as a tree.
-__device__ __forceinline__ void absorb32(Acc& a, const uint32_t (&w)[16], const int (&idx)[4],
-                                         float c) {
-  __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
+// Max of the 32 logits held as 16 packed bf16 pairs (a tree of packed maxima).
+__device__ __forceinline__ float group_max(const uint32_t (&w)[16]) {
+  __nv_bfloat162 m[8];
 #pragma unroll
-  for (int i = 1; i < 16; ++i) mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-  const float gm = fmaxf(__low2float(mx), __high2float(mx));
-  if (gm > a.m) {
-    int li = 0x7FFFFFFF;
+  for (int i = 0; i < 8; ++i)
+    m[i] = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w[2 * i]),
+                   *reinterpret_cast<const __nv_bfloat162*>(&w[2 * i + 1]));
 #pragma unroll
-    for (int e = 31; e >= 0; --e) {
-      const float x = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
-      if (x == gm) li = idx[e >> 3] + (e & 7);
-    }
-    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - gm) * c);
-    a.m = gm;
-    a.idx = li;
-  }
-  if (a.m == -CUDART_INF_F) return;  // nothing but padding so far
-  const float mc = a.m * c;
-  float e[32];
+  for (int n = 4; n > 0; n >>= 1)
+#pragma unroll
+    for (int i = 0; i < n; ++i) m[i] = __hmax2(m[2 * i], m[2 * i + 1]);
+  return fmaxf(__low2float(m[0]), __high2float(m[0]));
+}
+
+// 2^x for a pair (x <= 0) on the FMA pipe, so that part of the exponentials bypass the SFU,
+// in packed two-wide fp32 instructions: x = j + f with j = round(x) and f in [-1/2, 1/2];
+// 2^f from a degree-5 polynomial fitted here to the relative error on that interval (max
+// relative error about 2.3e-7 in fp32 Horner form); 2^j is added to the exponent bits.  x is
+// clamped at -125 so 2^j stays a normal number.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 magic = make_float2(12582912.0f, 12582912.0f);
+  const float2 t = __fadd2_rn(x, magic);
+  const float2 f = __fadd2_rn(x, __fadd2_rn(magic, make_float2(-t.x, -t.y)));
+  float2 q = make_float2(1.3276466634124517e-3f, 1.3276466634124517e-3f);
+  q = __ffma2_rn(q, f, make_float2(9.675540961325169e-3f, 9.675540961325169e-3f));
+  q = __ffma2_rn(q, f, make_float2(5.550713464617729e-2f, 5.550713464617729e-2f));
+  q = __ffma2_rn(q, f, make_float2(2.4022120237350464e-1f, 2.4022120237350464e-1f));
+  q = __ffma2_rn(q, f, make_float2(6.931469440460205e-1f, 6.931469440460205e-1f));
+  q = __ffma2_rn(q, f, make_float2(1.0000001192092896f, 1.0000001192092896f));
+  return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
+}
+
+// Which of the 16 logit pairs of a group take their exponentials on the FMA pipe (bit i set:
+// pair i) rather than on the SFU.
+constexpr uint32_t kPolyPairs = 0x0000u;
+
+// Sum of 2^(x c - mc) over the 32 logits: the scaling runs two logits per packed FMA, the
+// exponentials are independent (pairs selected by kPolyPairs on the FMA pipe), and the sum is
+// a tree of packed adds.
+__device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], float c, float mc) {
+  const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+  float2 e[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
-    e[2 * i] = ex2(fmaf(x0, c, -mc));
-    e[2 * i + 1] = (i & 1) ? exp2_fma(fmaf(x1, c, -mc)) : ex2(fmaf(x1, c, -mc));
+    const float2 y = __ffma2_rn(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), cc, nm);
+    e[i] = ((kPolyPairs >> i) & 1u) ? exp2_fma2(y) : make_float2(ex2(y.x), ex2(y.y));
   }
 #pragma unroll
-  for (int step = 1; step < 32; step <<= 1)
+  for (int step = 1; step < 16; step <<= 1)
 #pragma unroll
-    for (int i = 0; i < 32; i += 2 * step) e[i] += e[i + step];
-  a.s += e[0];
+    for (int i = 0; i < 16; i += 2 * step) e[i] = __fadd2_rn(e[i], e[i + step]);
+  return e[0].x + e[0].y;
+}
+
+// A lane's running state over one row segment.  The position of the max is found lazily:
+// when a group of 32 logits raises the max, the lane keeps a copy of that group (its 16
+// packed words and where it starts) and locates the first occurrence only when the segment
+// ends, instead of scanning every group that raises it.
+struct LaneAcc {
+  float m;            // running max (raw logit)
+  float s;            // sum of 2^((x - m) c)
+  int idx;            // first index of the max, or -1 while it lies in the saved group
+  int gbase;          // saved group: vector q covers logits gbase + 256 q .. + 7
+  uint32_t gw[16];    // saved group's packed bf16 pairs
+};
+
+__device__ __forceinline__ void lane_reset(LaneAcc& a) {
+  a.m = -CUDART_INF_F;
+  a.s = 0.f;
+  a.idx = 0x7FFFFFFF;
+}
+
+// Adds the 32 logits of one group (vector q = words 4q .. 4q+3, starting at logit
+// gbase + 256 q).  A lane sees its logits in increasing index order, so a strictly larger
+// max keeps the first occurrence.
+__device__ __forceinline__ void absorb32(LaneAcc& a, const uint32_t (&w)[16], int gbase, float c) {
+  const float gm = group_max(w);
+  if (gm > a.m) {
+    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - gm) * c);
+    a.m = gm;
+    a.idx = -1;
+    a.gbase = gbase;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a.gw[i] = w[i];
+  }
+  if (a.m == -CUDART_INF_F) return;  // nothing but padding so far
+  a.s += exp_sum32(w, c, a.m * c);
+}
+
+// Adds one logit x with index i.
+__device__ __forceinline__ void absorb1(LaneAcc& a, float x, int i, float c) {
+  if (x > a.m) {
+    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - x) * c);
+    a.m = x;
+    a.idx = i;
+  }
+  a.s += ex2(fmaf(x, c, -a.m * c));
+}
+
+// The lane's (max, sum, first index of the max) with the saved group's position resolved.
+__device__ __forceinline__ Acc lane_result(const LaneAcc& a) {
+  int idx = a.idx;
+  if (idx < 0) {
+    idx = 0x7FFFFFFF;
+#pragma unroll
+    for (int e = 31; e >= 0; --e) {
+      const float x = (e & 1) ? bf16_hi(a.gw[e >> 1]) : bf16_lo(a.gw[e >> 1]);
+      if (x == a.m) idx = a.gbase + (e >> 3) * 256 + (e & 7);
+    }
+  }
+  return Acc{a.m, a.s, idx};
 }
 
 __device__ __forceinline__ float bf16f(uint16_t h) {
@@ -216,62 +255,13 @@ __device__ __forceinline__ int warp_of(long long e, long long T, int W) {
   return w;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-commit_kernel(const CommitArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* ring_base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                                  ~static_cast<uintptr_t>(127));
-  __shared__ uint64_t s_bar[kWarps][kRing];
-  __shared__ ChunkMeta s_meta[kWarps][kRing];
-  __shared__ int s_pref[kThreads + 1];
-  __shared__ int s_wsum[kWarps];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  griddep_wait();
-  griddep_launch_dependents();
-
-  // ---- count the mask: s_pref[t] = masked rows before thread t's byte range
-  const int per = (a.R + kThreads - 1) / kThreads;
-  const int r_lo = min(a.R, tid * per), r_hi = min(a.R, r_lo + per);
-  int cnt = 0;
-  for (int r = r_lo; r < r_hi; ++r) cnt += a.mask[r] != 0;
-  int incl = cnt;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
-  }
-  if (lane == 31) s_wsum[warp] = incl;
-  if (tid < kWarps * kRing) mbar_init(&s_bar[tid / kRing][tid % kRing], 1);
-  fence_mbar_init();
-  __syncthreads();
-  int wbase = 0;
-  for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
-  s_pref[tid] = wbase + incl - cnt;
-  if (tid == kThreads - 1) s_pref[kThreads] = wbase + incl;
-  __syncthreads();
-  const long long n_masked = s_pref[kThreads];
-
-  // ---- unmasked rows: tok = -1, conf = -inf, and they count towards their block
-  for (int r = blockIdx.x * kThreads + tid; r < a.R; r += gridDim.x * kThreads) {
-    if (a.mask[r]) continue;
-    const int b = r / a.L;
-    a.tok_out[r] = -1;
-    a.conf_out[r] = -CUDART_INF_F;
-    __threadfence();
-    if (atomicAdd(a.blk_cnt + b, 1) == a.L - 1)
-      decide_block(b, a.L, a.mask, a.conf_out, a.commit_out, a.blk_cnt, a.threshold);
-  }
-
-  // ---- this warp's range of the masked concatenation
-  const long long T = n_masked * a.V;
-  const long long Wcap = static_cast<long long>(gridDim.x) * kWarps;
-  const int W = static_cast<int>(max(1ll, min(Wcap, T / kChunk)));
-  const int w = blockIdx.x * kWarps + warp;
-  if (w >= W || T == 0) return;
-  const long long e0 = range_start(T, W, w);
-  const long long e1 = range_start(T, W, w + 1);
-  if (e0 >= e1) return;
-
+// Streams warp w's range [e0, e1) of the masked concatenation (T logits, W warps) through
+// the warp's ring and finalizes the rows whose element count it completes.
+__device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, int W, int w,
+                                          long long e0, long long e1, int per,
+                                          const int* s_pref, const uint8_t* s_mask,
+                                          uint8_t* ring, uint64_t* bars, ChunkMeta* meta,
+                                          int lane) {
   // row id of masked index k: binary search over the per-thread counts, then a byte scan
   auto row_of = [&](long long k) -> int {
     int lo = 0, hi = kThreads - 1;
@@ -282,13 +272,10 @@ commit_kernel(const CommitArgs a) {
     int left = static_cast<int>(k - s_pref[lo]);
     int r = min(a.R, lo * per);
     for (;; ++r)
-      if (a.mask[r] && left-- == 0) break;
+      if ((s_mask ? s_mask[r] : a.mask[r]) && left-- == 0) break;
     return r;
   };
 
-  uint8_t* ring = ring_base + warp * (kRing * kChunkBytes);
-  uint64_t* bars = s_bar[warp];
-  ChunkMeta* meta = s_meta[warp];
   // producer cursor (lane 0): masked row k, offset in that row, logits left in the range
   long long left = e1 - e0;
   int cur_k = static_cast<int>(e0 / a.V);
@@ -341,7 +328,8 @@ commit_kernel(const CommitArgs a) {
   issued = __shfl_sync(0xffffffffu, issued, 0);
 
   int abort_flag = 0;
-  Acc acc{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+  LaneAcc acc;
+  lane_reset(acc);
   for (int u = 0; u < issued; ++u) {
     const int slot = u % kRing;
     if (!mbar_wait(&bars[slot], (u / kRing) & 1, &abort_flag)) {
@@ -352,39 +340,51 @@ commit_kernel(const CommitArgs a) {
     const uint16_t* row = a.logits + static_cast<size_t>(m.r) * a.V;
     const uint4* vp = reinterpret_cast<const uint4*>(ring + slot * kChunkBytes);
     const int nvec = (m.i1 - m.i0) >> 3;
-    for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
-      uint32_t wv[16];
-      int vi[4];
+    // logits before the aligned interior (at most 7) come first: each lane then sees its
+    // logits in increasing index order
+    if (m.g0 + lane < m.i0) absorb1(acc, bf16f(row[m.g0 + lane]), m.g0 + lane, a.c);
+    if (nvec == kChunk / 8) {
+      // a full stage: no bounds checks
 #pragma unroll
-      for (int q = 0; q < kUnroll; ++q) {
-        const int v = v0 + q * 32 + lane;
-        uint4 t = make_uint4(kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair);
-        if (v < nvec) t = vp[v];
-        wv[4 * q] = t.x;
-        wv[4 * q + 1] = t.y;
-        wv[4 * q + 2] = t.z;
-        wv[4 * q + 3] = t.w;
-        vi[q] = m.i0 + v * 8;
+      for (int v0 = 0; v0 < kChunk / 8; v0 += 32 * kUnroll) {
+        uint32_t wv[16];
+#pragma unroll
+        for (int q = 0; q < kUnroll; ++q) {
+          const uint4 t = vp[v0 + q * 32 + lane];
+          wv[4 * q] = t.x;
+          wv[4 * q + 1] = t.y;
+          wv[4 * q + 2] = t.z;
+          wv[4 * q + 3] = t.w;
+        }
+        absorb32(acc, wv, m.i0 + (v0 + lane) * 8, a.c);
       }
-      absorb32(acc, wv, vi, a.c);
+    } else {
+      for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+        uint32_t wv[16];
+#pragma unroll
+        for (int q = 0; q < kUnroll; ++q) {
+          const int v = v0 + q * 32 + lane;
+          uint4 t = make_uint4(kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair,
+                               kBf16NegInfPair);
+          if (v < nvec) t = vp[v];
+          wv[4 * q] = t.x;
+          wv[4 * q + 1] = t.y;
+          wv[4 * q + 2] = t.z;
+          wv[4 * q + 3] = t.w;
+        }
+        absorb32(acc, wv, m.i0 + (v0 + lane) * 8, a.c);
+      }
     }
-    // logits outside the aligned interior (at most 7 on each side)
-    if (m.g0 + lane < m.i0) {
-      float x = bf16f(row[m.g0 + lane]);
-      absorb<1>(acc, &x, m.g0 + lane, a.c);
-    }
-    if (m.i1 + lane < m.g1) {
-      float x = bf16f(row[m.i1 + lane]);
-      absorb<1>(acc, &x, m.i1 + lane, a.c);
-    }
+    // logits after the aligned interior (at most 7)
+    if (m.i1 + lane < m.g1) absorb1(acc, bf16f(row[m.i1 + lane]), m.i1 + lane, a.c);
     __syncwarp();
     if (lane == 0 && issue(slot)) ++issued;  // refill the stage just read
     issued = __shfl_sync(0xffffffffu, issued, 0);
     if (!m.last) continue;
     // ---- end of a row segment: one partial per (warp, row); the warp that completes the
     // row's element count finalizes it
-    Acc t = warp_merge(acc, a.c);
-    acc = Acc{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    Acc t = warp_merge(lane_result(acc), a.c);
+    lane_reset(acc);
     const long long kv = static_cast<long long>(m.k) * a.V;
     const int seg_len = static_cast<int>(min(kv + a.V, e1) - max(kv, e0));
     int last = 0;
@@ -426,6 +426,72 @@ commit_kernel(const CommitArgs a) {
       int dummy = 0;
       mbar_wait(&bars[u % kRing], (u / kRing) & 1, &dummy);
     }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+commit_kernel(const CommitArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring_base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                  ~static_cast<uintptr_t>(127));
+  __shared__ uint64_t s_bar[kWarps][kRing];
+  __shared__ ChunkMeta s_meta[kWarps][kRing];
+  __shared__ int s_pref[kThreads + 1];
+  __shared__ int s_wsum[kWarps];
+  __shared__ uint8_t s_mask[kMaskSmem];   // copy of the mask when it fits
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();
+  griddep_launch_dependents();
+
+  // ---- count the mask: s_pref[t] = masked rows before thread t's byte range
+  const int per = (a.R + kThreads - 1) / kThreads;
+  const int r_lo = min(a.R, tid * per), r_hi = min(a.R, r_lo + per);
+  const bool mask_in_smem = a.R <= kMaskSmem;
+  int cnt = 0;
+  for (int r = r_lo; r < r_hi; ++r) {
+    const uint8_t mk = a.mask[r];
+    cnt += mk != 0;
+    if (mask_in_smem) s_mask[r] = mk;
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  if (tid < kWarps * kRing) mbar_init(&s_bar[tid / kRing][tid % kRing], 1);
+  fence_mbar_init();
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
+  s_pref[tid] = wbase + incl - cnt;
+  if (tid == kThreads - 1) s_pref[kThreads] = wbase + incl;
+  __syncthreads();
+  const long long n_masked = s_pref[kThreads];
+
+  // ---- this warp's range of the masked concatenation
+  const long long T = n_masked * a.V;
+  const long long Wcap = static_cast<long long>(gridDim.x) * kWarps;
+  const int W = static_cast<int>(max(1ll, min(Wcap, T / kChunk)));
+  const int w = blockIdx.x * kWarps + warp;
+  const long long e0 = range_start(T, W, w);
+  const long long e1 = range_start(T, W, w + 1);
+  if (w < W && T > 0 && e0 < e1)
+    stream_range(a, T, W, w, e0, e1, per, s_pref, mask_in_smem ? s_mask : nullptr,
+                 ring_base + warp * (kRing * kChunkBytes), s_bar[warp], s_meta[warp], lane);
+
+  // ---- unmasked rows: tok = -1, conf = -inf, and they count towards their block.  Done
+  // last, one row per lane over every warp of the grid, so that no warp's streaming waits.
+  const int w_all = gridDim.x * kWarps;
+  for (int r = lane * w_all + w; r < a.R; r += 32 * w_all) {
+    if (mask_in_smem ? s_mask[r] : a.mask[r]) continue;
+    const int b = r / a.L;
+    a.tok_out[r] = -1;
+    a.conf_out[r] = -CUDART_INF_F;
+    __threadfence();
+    if (atomicAdd(a.blk_cnt + b, 1) == a.L - 1)
+      decide_block(b, a.L, a.mask, a.conf_out, a.commit_out, a.blk_cnt, a.threshold);
   }
 }
 
