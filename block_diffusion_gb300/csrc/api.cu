@@ -215,7 +215,7 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
   if (rc) return rc;
   if ((rc = get_encoder())) return rc;
   const AttnPlan plan = bdlm::plan_attention(d.B, d.L, d.Hq, d.Hkv, d.max_pages_per_seq,
-                                             d.page_size);
+                                             d.page_size, st->num_sms);
   if (plan.n_mma == 0) return BDLM_ERR_UNSUPPORTED;
   rc = ensure(reinterpret_cast<void**>(&st->attn_cnt), &st->attn_cnt_cap, plan.cnt_bytes, true);
   if (rc) return rc;

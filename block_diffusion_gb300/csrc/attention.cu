@@ -41,7 +41,18 @@ constexpr int kHalfBytes = 16384;
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMaxSplitTokens = 2048;
-constexpr int kMaxSplitPages = kMaxSplitTokens / kPage;
+// Page ids staged per item: a split of up to kMaxSplitTokens, or a whole sequence of up to
+// kMaxItemPages pages when sequences are processed whole (two CTAs per SM at N = 16 leave
+// no room for more).
+constexpr int kMaxItemPages = kMaxSplitTokens / kPage;
+static_assert(kMaxItemPages >= kMaxSplitTokens / kPage, "a split must fit the page-id buffer");
+// Whole sequences, longest first, replace KV splits when there are at least this many
+// (sequence, KV head, row group) items per CTA and up to kMaxOrderSeqs sequences.
+constexpr int kWholeItemsPerCta = 2;
+constexpr int kMaxOrderSeqs = 1024;
+// A chunk moves a column's running softmax max only when it raises it by more than this
+// (log2 units of the scaled scores), so P never exceeds 2^kLazyRescale.
+constexpr float kLazyRescale = 8.0f;
 constexpr int kItemRing = 4;
 
 struct AttnParams {
@@ -52,6 +63,7 @@ struct AttnParams {
   int* cnt;
   int* err;
   int* work;  // [0] next item, [1] CTAs finished
+  const int* order;  // whole-sequence mode: sequences by decreasing KV length, else null
   int B, L, Hq, Hkv, G, max_pages, num_pages;
   int lsub, row_groups, rows_per_group, split_tokens, max_splits, chunk_tiles;
   int total_items;
@@ -82,6 +94,7 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   idx /= p.Hkv;
   it.b = idx % p.B;
   it.split = idx / p.B;
+  if (p.order) it.b = __ldg(p.order + it.b);  // whole sequences, longest first
   const int prefix = p.prefix_lens[it.b];
   const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
   long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
@@ -114,13 +127,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
   __shared__ uint64_t bar_qfull, bar_qempty, bar_full[STAGES], bar_empty[STAGES];
   __shared__ uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_pempty[2];
-  __shared__ uint64_t bar_oready, bar_ofull, bar_done;
+  __shared__ uint64_t bar_oready, bar_ofull[2], bar_done;  // bar_ofull: PV of chunk u, by parity
   __shared__ uint64_t bar_ifull[kItemRing], bar_iempty[kItemRing];
   __shared__ Item s_item[kItemRing];
-  __shared__ int s_pid[3][kMaxSplitPages];
+  __shared__ int s_pid[3][kMaxItemPages];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float s_m[N], s_mc[N], s_alpha[N], s_l[N];
+  __shared__ int s_need[2];   // chunk u (parity): some column's max rose enough to rescale O^T
+  __shared__ int s_pflag[2];  // P buffer: its tile starts a chunk whose PV waits for a rescale
   __shared__ float s_red[4][N];
 
   const int warp = threadIdx.x >> 5;
@@ -141,13 +156,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(&bar_pempty[i], 1);
     }
     mbar_init(&bar_oready, kSoftmaxThreads);
-    mbar_init(&bar_ofull, 1);
+    mbar_init(&bar_ofull[0], 1);
+    mbar_init(&bar_ofull[1], 1);
     mbar_init(&bar_done, 1);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(&bar_ifull[i], 1);
       mbar_init(&bar_iempty[i], 2);
     }
     abort_flag = 0;
+    s_need[0] = s_need[1] = 0;
+    s_pflag[0] = s_pflag[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -389,14 +407,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (c == it.n_chunks - 1) umma_commit(&bar_qempty);  // Q no longer needed
       };
       // O^T += V^T P^T over the tiles of chunk `c`
-      auto do_pv = [&](const Item& it, int c) {
+      auto do_pv = [&](const Item& it, int c, int u) {
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
           const int pb = pcount & 1;
           if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
           if (!(ok = mbar_wait(&bar_pfull[pb], (pcount >> 1) & 1, &abort_flag))) return;
-          if (c > 0 && j == j0) {
+          if (c > 0 && j == j0 && s_pflag[pb]) {  // the softmax rescales O^T first
             if (!(ok = mbar_wait(&bar_oready, ocount & 1, &abort_flag))) return;
             ++ocount;
           }
@@ -430,7 +448,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             ph ^= 1;
           }
         }
-        umma_commit(&bar_ofull);
+        umma_commit(&bar_ofull[u & 1]);
       };
       int seq = 0;
       Item cur, nxt;
@@ -455,7 +473,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
           if (has_next) do_s(nxt, nc, u + 1, nseq);
           if (!ok) break;
-          do_pv(cur, c);
+          do_pv(cur, c, u);
           if (!ok) break;
           if (c == cur.n_chunks - 1) mbar_arrive(&bar_iempty[seq % kItemRing]);
           if (!has_next) break;
@@ -519,18 +537,31 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
         }
         named_barrier(1, kSoftmaxThreads);
+        if (x == 0) s_need[(u + 1) & 1] = 0;  // every reader of that slot is past this barrier
         if (x < N) {
+          // The running max only moves when the chunk raises it by more than kLazyRescale
+          // (log2 units): below that the exponentials use the older max, P stays below
+          // 2^kLazyRescale, and O^T and l need no rescale at this chunk boundary.
           const float mc = fmaxf(fmaxf(s_red[0][x], s_red[1][x]), fmaxf(s_red[2][x], s_red[3][x]));
           const float mo = s_m[x];
-          const float mn = fmaxf(mo, mc);
-          s_alpha[x] = (mo == -CUDART_INF_F) ? 0.f : exp2f((mo - mn) * cs);
+          float mn = mo, alpha = 1.f;
+          if (mo == -CUDART_INF_F) {
+            mn = mc;
+            alpha = 0.f;
+          } else if ((mc - mo) * cs > kLazyRescale) {
+            mn = mc;
+            alpha = exp2f((mo - mn) * cs);
+            s_need[u & 1] = 1;
+          }
+          s_alpha[x] = alpha;
           s_m[x] = mn;
           s_mc[x] = mn * cs;
         }
         named_barrier(1, kSoftmaxThreads);
-        if (c > 0) {
+        const bool need = s_need[u & 1] != 0;
+        if (c > 0 && need) {
           // rescale the running O^T columns (and l) to the new maxima
-          if (!(ok = mbar_wait(&bar_ofull, (u - 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
           tc_fence_after();
 #pragma unroll
           for (int cg = 0; cg < N / 16; ++cg) {
@@ -590,6 +621,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
               const uint32_t off = n * 128 + ((xc ^ (n & 7)) << 4) + xb;
               *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = __float2bfloat16_rn(pv[n]);
             }
+            if (x == 0) s_pflag[pb] = (j == j0) && need;
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar_pfull[pb]);
@@ -620,6 +652,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = __float2bfloat16_rn(pv);
               }
             }
+            if (x == 0) s_pflag[pb] = (j == j0) && need;
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar_pfull[pb]);
@@ -632,7 +665,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_arrive(&bar_sfree[u & 1]);
         if (c != it.n_chunks - 1) continue;
         // ---- epilogue of the item
-        if (!(ok = mbar_wait(&bar_ofull, u & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int n = 0; n < N; ++n) {
@@ -708,6 +741,34 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   if (threadIdx.x == 0 && abort_flag) record_error(p.err, BDLM_DEVERR_TIMEOUT);
 }
 
+
+// Sequences by decreasing KV length (ties: lower index first), for the whole-sequence mode:
+// the persistent attention CTAs take the longest items first, so the last items handed out
+// are the shortest and the CTAs finish close together without cutting sequences into
+// splits.  One CTA; B <= blockDim.x.
+__global__ void __launch_bounds__(kMaxOrderSeqs)
+attn_order_kernel(const int32_t* __restrict__ prefix_lens, int B, int L, long long max_tok,
+                  int* __restrict__ order) {
+  __shared__ long long s_len[kMaxOrderSeqs];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = threadIdx.x;
+  long long len = 0;
+  if (b < B) {
+    const int prefix = prefix_lens[b];
+    len = static_cast<long long>(prefix < 0 ? 0 : prefix) + L;
+    if (len > max_tok) len = max_tok;
+    s_len[b] = len;
+  }
+  __syncthreads();
+  if (b >= B) return;
+  int rank = 0;
+  for (int j = 0; j < B; ++j) {
+    const long long lj = s_len[j];
+    rank += (lj > len) || (lj == len && j < b);
+  }
+  order[rank] = b;
+}
 
 // Merges the splits of every (sequence, KV head, row group) whose KV range was cut into more
 // than one item: out = sum_s w_s O_s with w_s = exp(m_s - M) / sum_s exp(m_s - M) l_s.
@@ -826,6 +887,10 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
   return launch_pdl(attn_kernel<N, STAGES, CPS>, dim3(num_sms * CPS), dim3(kThreads), smem,
@@ -834,7 +899,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 }  // namespace
 
-AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size) {
+AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size,
+                        int num_sms) {
   AttnPlan pl;
   if (page_size != kPage || Hkv <= 0 || Hq % Hkv != 0) {
     pl.n_mma = 0;
@@ -859,8 +925,19 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
   pl.split_tokens = pl.chunk_tiles * kTile * chunks_per_split;
   if (pl.split_tokens > kMaxSplitTokens) pl.split_tokens = kMaxSplitTokens;
   const long long max_tok = static_cast<long long>(max_pages) * kPage;
-  pl.max_splits = static_cast<int>((max_tok + pl.split_tokens - 1) / pl.split_tokens);
   const size_t groups = static_cast<size_t>(B) * Hkv * pl.row_groups;
+  const long long ctas = static_cast<long long>(num_sms) * ctas_per_sm;
+  pl.whole = B <= kMaxOrderSeqs && max_pages <= kMaxItemPages &&
+             static_cast<long long>(groups) >= kWholeItemsPerCta * ctas;
+  if (pl.whole) {
+    // every item is a whole sequence: no partials, no merge; the workspace holds the order
+    pl.split_tokens = static_cast<int>((max_tok + kTile - 1) / kTile * kTile);
+    pl.max_splits = 1;
+    pl.part_bytes = static_cast<size_t>(B) * sizeof(int);
+    pl.cnt_bytes = groups * sizeof(int) + 2 * sizeof(int);
+    return pl;
+  }
+  pl.max_splits = static_cast<int>((max_tok + pl.split_tokens - 1) / pl.split_tokens);
   pl.part_bytes = groups * pl.max_splits * static_cast<size_t>(pl.n_mma) * 130 * sizeof(float);
   pl.cnt_bytes = groups * sizeof(int) + 2 * sizeof(int);
   return pl;
@@ -879,6 +956,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   prm.part = part;
   prm.work = cnt;  // two words of scheduler state, then the split counters
   prm.cnt = cnt + 2;
+  prm.order = nullptr;
   prm.err = err;
   prm.B = B;
   prm.L = L;
@@ -898,6 +976,14 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   if (items > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   prm.total_items = static_cast<int>(items);
   cudaError_t e;
+  if (plan.whole) {
+    int* order = reinterpret_cast<int*>(part);
+    e = launch_pdl(attn_order_kernel, dim3(1), dim3(kMaxOrderSeqs), 0, stream, prefix_lens, B, L,
+                   static_cast<long long>(max_pages) * kPage, order);
+    if (e != cudaSuccess) return e;
+    prm.order = order;
+    prm.part = nullptr;
+  }
   switch (plan.n_mma) {
     case 16: e = launch_t<16, 3, 2>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
     case 32: e = launch_t<32, 2, 2>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;

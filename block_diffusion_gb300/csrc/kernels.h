@@ -65,11 +65,13 @@ struct AttnPlan {
   int max_splits = 1;    // splits of the longest possible sequence
   int chunk_tiles = 1;   // 128-token tiles per S chunk held in tensor memory
   int tmem_cols = 0;     // tensor-memory columns allocated per CTA
+  bool whole = false;    // whole sequences, longest first, instead of KV splits
   size_t smem_bytes = 0;
   size_t part_bytes = 0, cnt_bytes = 0;
 };
 
-AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size);
+AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size,
+                        int num_sms);
 cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const int32_t* page_table,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,

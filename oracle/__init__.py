@@ -43,10 +43,10 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             P = ctypes.c_void_p
             I = ctypes.c_int
-            lib.oracle_block_attention.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P,
+            lib.oracle_block_attention.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P,
                                                    ctypes.c_double, P, I, P]
             lib.oracle_block_attention.restype = I
-            lib.oracle_attention_probs.argtypes = [I, I, I, I, I, I, P, P, P, P,
+            lib.oracle_attention_probs.argtypes = [I, I, I, I, I, I, I, P, P, P, P,
                                                    ctypes.c_double, I, I, I, P]
             lib.oracle_attention_probs.restype = I
             lib.oracle_lm_head.argtypes = [I, I, I, P, P, P, I, P, I, P]
@@ -84,7 +84,8 @@ def block_attention(q, k_pages, v_pages, page_table, prefix_lens, L, Hq, Hkv, D,
         sm_scale = 1.0 / np.sqrt(D)
     out = np.full((B, L, Hq, D), np.nan, dtype=np.float64)
     sl = None if seqs is None else np.ascontiguousarray(seqs, dtype=np.int32)
-    rc = lib.oracle_block_attention(B, L, Hq, Hkv, D, P, max_pages, _ptr(q), _ptr(k_pages),
+    rc = lib.oracle_block_attention(B, L, Hq, Hkv, D, P, max_pages, k_pages.shape[0], _ptr(q),
+                                    _ptr(k_pages),
                                     _ptr(v_pages), _ptr(page_table), _ptr(prefix_lens),
                                     float(sm_scale), _ptr(sl), 0 if sl is None else len(sl),
                                     _ptr(out))
@@ -103,9 +104,11 @@ def attention_probs(q, k_pages, page_table, prefix_lens, L, Hq, Hkv, D, P, b, i,
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
     out = np.zeros(int(prefix_lens[b]) + L, dtype=np.float64)
-    lib.oracle_attention_probs(L, Hq, Hkv, D, P, page_table.shape[1], _ptr(q), _ptr(k_pages),
-                               _ptr(page_table), _ptr(prefix_lens), float(sm_scale), b, i, h,
-                               _ptr(out))
+    rc = lib.oracle_attention_probs(L, Hq, Hkv, D, P, page_table.shape[1], k_pages.shape[0],
+                                    _ptr(q), _ptr(k_pages), _ptr(page_table), _ptr(prefix_lens),
+                                    float(sm_scale), b, i, h, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_attention_probs: bad arguments")
     return out
 
 

@@ -53,11 +53,13 @@ extern "C" {
 // block, nothing of later blocks exists); query head h uses KV head h / (Hq/Hkv).
 // Layouts: q [B,L,Hq,D]; k_pages, v_pages [num_pages,P,Hkv,D]; page_table [B,max_pages];
 // out [B,L,Hq,D] fp64.  seq_list (n_seq entries) selects the sequences computed; NULL
-// computes all B.  Returns 0, or -1 on an argument error.
+// computes all B.  Returns 0, or -1 on an argument error (including a negative prefix or a
+// page id of a needed token outside [0, num_pages): that sequence is left untouched).
 int oracle_block_attention(int B, int L, int Hq, int Hkv, int D, int P, int max_pages,
-                           const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
-                           const int32_t* page_table, const int32_t* prefix_lens,
-                           double sm_scale, const int32_t* seq_list, int n_seq, double* out) {
+                           int num_pages, const uint16_t* q, const uint16_t* k_pages,
+                           const uint16_t* v_pages, const int32_t* page_table,
+                           const int32_t* prefix_lens, double sm_scale, const int32_t* seq_list,
+                           int n_seq, double* out) {
     if (B < 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || Hq % Hkv != 0) return -1;
     const int G = Hq / Hkv;
     const int count = seq_list ? n_seq : B;
@@ -67,7 +69,16 @@ int oracle_block_attention(int B, int L, int Hq, int Hkv, int D, int P, int max_
         for (int h = 0; h < Hq; ++h) {
             const int b = seq_list ? seq_list[sidx] : sidx;
             const long kv_len = static_cast<long>(prefix_lens[b]) + L;
-            if (kv_len > static_cast<long>(max_pages) * P) { bad = 1; continue; }
+            if (prefix_lens[b] < 0 || kv_len > static_cast<long>(max_pages) * P) {
+                bad = 1;
+                continue;
+            }
+            int bad_page = 0;
+            for (long pg = 0; pg < (kv_len + P - 1) / P; ++pg) {
+                const long id = page_table[static_cast<long>(b) * max_pages + pg];
+                if (id < 0 || id >= num_pages) bad_page = 1;
+            }
+            if (bad_page) { bad = 1; continue; }
             const int kvh = h / G;
             std::vector<double> kk(static_cast<size_t>(kv_len) * D), vv(static_cast<size_t>(kv_len) * D);
             for (long j = 0; j < kv_len; ++j) {
@@ -108,13 +119,18 @@ int oracle_block_attention(int B, int L, int Hq, int Hkv, int D, int P, int max_
 
 // Softmax weights of one (sequence, position, head) of the attention above, written to
 // probs[0..kv_len-1]; used to check that each row sums to one.
-int oracle_attention_probs(int L, int Hq, int Hkv, int D, int P, int max_pages,
+int oracle_attention_probs(int L, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
                            const uint16_t* q, const uint16_t* k_pages, const int32_t* page_table,
                            const int32_t* prefix_lens, double sm_scale, int b, int i, int h,
                            double* probs) {
     if (Hq % Hkv != 0) return -1;
     const int kvh = h / (Hq / Hkv);
     const long kv_len = static_cast<long>(prefix_lens[b]) + L;
+    if (prefix_lens[b] < 0 || kv_len > static_cast<long>(max_pages) * P) return -1;
+    for (long pg = 0; pg < (kv_len + P - 1) / P; ++pg) {
+        const long id = page_table[static_cast<long>(b) * max_pages + pg];
+        if (id < 0 || id >= num_pages) return -1;
+    }
     const size_t qb = ((static_cast<size_t>(b) * L + i) * Hq + h) * D;
     double smax = -std::numeric_limits<double>::infinity();
     for (long j = 0; j < kv_len; ++j) {

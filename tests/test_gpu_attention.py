@@ -67,6 +67,20 @@ def test_multiple_splits_and_chunks(lib, L, prefix):
     check(lib, a)
 
 
+@pytest.mark.parametrize("L,Hq,B,prefix", [(4, 32, 96, (100, 1900)), (8, 32, 160, (0, 1200)),
+                                          (4, 16, 200, (3000, 4100))])
+def test_whole_sequences_longest_first(lib, L, Hq, B, prefix):
+    """Enough (sequence, KV head) items for whole sequences, longest first, with no KV
+    splits: items of several tensor-memory chunks, sequences of equal length (ties in the
+    order), the longest page table the mode takes, and every output checked."""
+    rng = np.random.default_rng(B * 10 + L)
+    lens = rng.integers(prefix[0], prefix[1] + 1, size=B)
+    lens[1] = lens[0]
+    lens[-1] = 0
+    a = W.make_attention(rng, B, L, Hq, 8, 128, prefix_lens=lens)
+    check(lib, a)
+
+
 def test_config1(lib):
     c = W.CONFIGS[1]
     a = W.make_attention(np.random.default_rng(W.seed_for(1)), 1, 4, 16, 8, 128,

@@ -259,3 +259,18 @@ def test_round_logits_to_bf16():
     assert oracle.round_logits_to_bf16(np.array([mid]))[0] == 0x3F80          # tie -> even
     assert oracle.round_logits_to_bf16(np.array([mid + 2.0 ** -40]))[0] == 0x3F81
     assert oracle.round_logits_to_bf16(np.array([-(mid + 2.0 ** -40)]))[0] == 0xBF81
+
+
+def test_attention_oracle_rejects_pages_outside_the_pool():
+    """A page id of a needed token outside the pool is an argument error, not a read."""
+    rng = np.random.default_rng(11)
+    a = make_attention(rng, 2, 4, 8, 8, 128, prefix_range=(20, 40), poison=False)
+    bad = a.page_table_ref.copy()
+    bad[1, 0] = a.k_ref.shape[0]
+    with pytest.raises(ValueError):
+        oracle.block_attention(a.q, a.k_ref, a.v_ref, bad, a.prefix_lens, a.L, a.Hq, a.Hkv,
+                               a.D, a.P)
+    bad[1, 0] = -1
+    with pytest.raises(ValueError):
+        oracle.attention_probs(a.q, a.k_ref, bad, a.prefix_lens, a.L, a.Hq, a.Hkv, a.D, a.P,
+                               1, 0, 0)
