@@ -25,8 +25,6 @@ struct DeviceState {
   int* err = nullptr;            // device error word
   int* attn_cnt = nullptr;       // split-KV arrival counters (zero between calls)
   size_t attn_cnt_cap = 0;
-  int* commit_cnt = nullptr;     // commit row + block counters (zero between calls)
-  size_t commit_cnt_cap = 0;
   void* data = nullptr;          // partial results / gathered rows
   size_t data_cap = 0;
 };
@@ -145,12 +143,10 @@ int bdlm_release(void) {
   if (rc) return rc;
   if (cudaDeviceSynchronize() != cudaSuccess) return BDLM_ERR_CUDA;
   cudaFree(st->attn_cnt);
-  cudaFree(st->commit_cnt);
   cudaFree(st->data);
   st->attn_cnt = nullptr;
-  st->commit_cnt = nullptr;
   st->data = nullptr;
-  st->attn_cnt_cap = st->commit_cnt_cap = st->data_cap = 0;
+  st->attn_cnt_cap = st->data_cap = 0;
   return BDLM_OK;
 }
 
@@ -169,17 +165,12 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
   if (rc) return rc;
   const CommitPlan plan = bdlm::plan_commit(B, L, V, st->num_sms);
   if (plan.total_items > 0x7FFFFFFFll) return BDLM_ERR_INVALID;
-  rc = ensure(reinterpret_cast<void**>(&st->commit_cnt), &st->commit_cnt_cap,
-              plan.work_bytes + plan.row_cnt_bytes + plan.blk_cnt_bytes, true);
-  if (rc) return rc;
   rc = ensure(&st->data, &st->data_cap, plan.part_bytes, false);
   if (rc) return rc;
-  int* row_cnt = st->commit_cnt;
-  int* blk_cnt = row_cnt + static_cast<size_t>(B) * L;
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
                                       conf_out, commit_out, plan,
-                                      static_cast<bdlm::CommitPartial*>(st->data), row_cnt,
-                                      blk_cnt, st->err, static_cast<cudaStream_t>(stream));
+                                      static_cast<bdlm::CommitPartial*>(st->data), st->err,
+                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 

@@ -11,10 +11,10 @@
 // mask to learn n_masked and where each masked row sits).  A warp streams its range through a
 // private ring of three 4 KB shared-memory stages filled by bulk copies (one instruction per
 // stage), keeping a running (max, sum of exp, first argmax) per lane, and at the end of each
-// row segment merges its lanes with shuffles into one partial.  The last warp to finish a row
-// (atomic counter) merges the row's partials in a fixed order and writes tok/conf; the last
-// row to finish a block decides the block's commit.  Nothing waits on another warp or CTA;
-// every counter is reset by whoever consumed it.
+// row segment merges its lanes with shuffles into one partial: that is all it writes.  A second
+// kernel, one CTA per block, then merges each masked row's partials in warp order, writes
+// tok/conf and decides the block's commit after a single round of loads: no counters, fences
+// or atomics sit on the streaming warps' path.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -181,30 +181,6 @@ __device__ __forceinline__ float bf16f(uint16_t h) {
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
-// The last row of block b to finish decides the block's commit (one lane).
-__device__ void decide_block(int b, int L, const uint8_t* __restrict__ mask, const float* conf_out,
-                             uint8_t* __restrict__ commit_out, int* __restrict__ blk_cnt,
-                             float threshold) {
-  __threadfence();
-  const volatile float* cf = conf_out + static_cast<size_t>(b) * L;
-  const uint8_t* mk = mask + static_cast<size_t>(b) * L;
-  uint8_t* co = commit_out + static_cast<size_t>(b) * L;
-  int any_masked = 0, any_commit = 0, best = -1;
-  float best_c = 0.f;
-  for (int i = 0; i < L; ++i) {
-    uint8_t cm = 0;
-    if (mk[i]) {
-      const float ci = cf[i];
-      any_masked = 1;
-      if (ci >= threshold) { cm = 1; any_commit = 1; }
-      if (best < 0 || ci > best_c) { best = i; best_c = ci; }
-    }
-    co[i] = cm;
-  }
-  if (any_masked && !any_commit) co[best] = 1;
-  blk_cnt[b] = 0;
-}
-
 __device__ __forceinline__ Acc warp_merge(Acc a, float c) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -235,8 +211,6 @@ struct CommitArgs {
   float* conf_out;
   uint8_t* commit_out;
   CommitPartial* part;
-  int* row_cnt;
-  int* blk_cnt;
   int* err;  // device error word (may be null)
 };
 
@@ -381,44 +355,11 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
     if (lane == 0 && issue(slot)) ++issued;  // refill the stage just read
     issued = __shfl_sync(0xffffffffu, issued, 0);
     if (!m.last) continue;
-    // ---- end of a row segment: one partial per (warp, row); the warp that completes the
-    // row's element count finalizes it
+    // ---- end of a row segment: one partial per (warp, row) at slot w + k (the ranges are
+    // ordered and contiguous, so the slots are distinct)
     Acc t = warp_merge(lane_result(acc), a.c);
     lane_reset(acc);
-    const long long kv = static_cast<long long>(m.k) * a.V;
-    const int seg_len = static_cast<int>(min(kv + a.V, e1) - max(kv, e0));
-    int last = 0;
-    if (lane == 0) {
-      a.part[w + m.k] = CommitPartial{t.m, t.s, t.idx, 0};
-      __threadfence();
-      last = (atomicAdd(a.row_cnt + m.r, seg_len) + seg_len == a.V);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-    int first_w = 0, n_w = 0;
-    if (lane == 0) {
-      first_w = warp_of(kv, T, W);
-      n_w = warp_of(min(kv + a.V, T) - 1, T, W) - first_w + 1;
-    }
-    first_w = __shfl_sync(0xffffffffu, first_w, 0);
-    n_w = __shfl_sync(0xffffffffu, n_w, 0);
-    __threadfence();
-    const volatile CommitPartial* pr = a.part + first_w + m.k;
-    Acc f{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
-    for (int j0 = 0; j0 < n_w; j0 += 32) {
-      Acc q{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
-      if (j0 + lane < n_w) q = Acc{pr[j0 + lane].m, pr[j0 + lane].s, pr[j0 + lane].idx};
-      f = merge(f, warp_merge(q, a.c), a.c);
-    }
-    if (lane == 0) {
-      a.tok_out[m.r] = f.idx;
-      a.conf_out[m.r] = 1.0f / f.s;
-      a.row_cnt[m.r] = 0;
-      __threadfence();
-      const int b = m.r / a.L;
-      if (atomicAdd(a.blk_cnt + b, 1) == a.L - 1)
-        decide_block(b, a.L, a.mask, a.conf_out, a.commit_out, a.blk_cnt, a.threshold);
-    }
+    if (lane == 0) a.part[w + m.k] = CommitPartial{t.m, t.s, t.idx, 0};
   }
   // drain: nothing may still be landing in this warp's stages when it exits
   if (lane == 0) {
@@ -481,17 +422,108 @@ commit_kernel(const CommitArgs a) {
     stream_range(a, T, W, w, e0, e1, per, s_pref, mask_in_smem ? s_mask : nullptr,
                  ring_base + warp * (kRing * kChunkBytes), s_bar[warp], s_meta[warp], lane);
 
-  // ---- unmasked rows: tok = -1, conf = -inf, and they count towards their block.  Done
-  // last, one row per lane over every warp of the grid, so that no warp's streaming waits.
-  const int w_all = gridDim.x * kWarps;
-  for (int r = lane * w_all + w; r < a.R; r += 32 * w_all) {
-    if (mask_in_smem ? s_mask[r] : a.mask[r]) continue;
-    const int b = r / a.L;
-    a.tok_out[r] = -1;
-    a.conf_out[r] = -CUDART_INF_F;
-    __threadfence();
-    if (atomicAdd(a.blk_cnt + b, 1) == a.L - 1)
-      decide_block(b, a.L, a.mask, a.conf_out, a.commit_out, a.blk_cnt, a.threshold);
+}
+
+// One CTA per block b, min(L, 32) warps: the masked index of each row (from the mask, an input
+// that is complete before the streaming kernel lets this one start), then, once the streaming
+// kernel has finished, one warp per row merges the row's partials in warp order; thread 0
+// decides the block: every masked position with conf >= threshold, else the single most
+// confident one (lowest position on ties).  Unmasked rows get tok = -1, conf = -inf.
+__global__ void __launch_bounds__(1024)
+commit_finalize_kernel(const CommitArgs a, int stream_grid) {
+  __shared__ int s_wsum[32];
+  __shared__ int s_blk_before, s_total;
+  __shared__ float s_conf[64];
+  const int b = blockIdx.x, L = a.L;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  // masked rows before this block, and in all
+  int before = 0, total = 0;
+  for (int r = tid; r < a.R; r += blockDim.x) {
+    const int mk = a.mask[r] != 0;
+    total += mk;
+    before += (r < b * L) ? mk : 0;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, off);
+    total += __shfl_xor_sync(0xffffffffu, total, off);
+  }
+  if (lane == 0) s_wsum[warp] = before;
+  __syncthreads();
+  if (tid == 0) {
+    int sb = 0;
+    for (int i = 0; i < nw; ++i) sb += s_wsum[i];
+    s_blk_before = sb;
+  }
+  __syncthreads();
+  if (lane == 0) s_wsum[warp] = total;
+  __syncthreads();
+  if (tid == 0) {
+    int st = 0;
+    for (int i = 0; i < nw; ++i) st += s_wsum[i];
+    s_total = st;
+  }
+  __syncthreads();
+  const long long T = static_cast<long long>(s_total) * a.V;
+  const long long Wcap = static_cast<long long>(stream_grid) * kWarps;
+  const int W = static_cast<int>(max(1ll, min(Wcap, T / kChunk)));
+  griddep_wait();  // the streaming kernel's partials are complete and visible
+  griddep_launch_dependents();
+  const uint8_t* mk = a.mask + static_cast<size_t>(b) * L;
+  for (int i = warp; i < L; i += nw) {
+    const int r = b * L + i;
+    if (!mk[i]) {
+      if (lane == 0) {
+        a.tok_out[r] = -1;
+        a.conf_out[r] = -CUDART_INF_F;
+        s_conf[i] = -CUDART_INF_F;
+      }
+      continue;
+    }
+    int k = s_blk_before;
+    for (int j = 0; j < i; ++j) k += mk[j] != 0;
+    const long long kv = static_cast<long long>(k) * a.V;
+    const int first_w = warp_of(kv, T, W);
+    const int n_w = warp_of(min(kv + a.V, T) - 1, T, W) - first_w + 1;
+    const CommitPartial* pr = a.part + first_w + k;
+    Acc f{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    for (int j0 = 0; j0 < n_w; j0 += 32) {
+      Acc q{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+      if (j0 + lane < n_w) {
+        const CommitPartial c = pr[j0 + lane];
+        q = Acc{c.m, c.s, c.idx};
+      }
+      f = merge(f, warp_merge(q, a.c), a.c);
+    }
+    if (lane == 0) {
+      const float conf = 1.0f / f.s;
+      a.tok_out[r] = f.idx;
+      a.conf_out[r] = conf;
+      s_conf[i] = conf;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint8_t* co = a.commit_out + static_cast<size_t>(b) * L;
+    int any_masked = 0, any_commit = 0, best = -1;
+    float best_c = 0.f;
+    for (int i = 0; i < L; ++i) {
+      uint8_t cm = 0;
+      if (mk[i]) {
+        const float ci = s_conf[i];
+        any_masked = 1;
+        if (ci >= a.threshold) {
+          cm = 1;
+          any_commit = 1;
+        }
+        if (best < 0 || ci > best_c) {
+          best = i;
+          best_c = ci;
+        }
+      }
+      co[i] = cm;
+    }
+    if (any_masked && !any_commit) co[best] = 1;
   }
 }
 
@@ -515,9 +547,7 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms) {
   p.smem_bytes = static_cast<size_t>(kWarps) * kRing * kChunkBytes + 128;
   // one partial per (warp, masked row segment): slots w + k < warps + rows
   p.part_bytes = static_cast<size_t>(p.grid * kWarps + rows) * sizeof(CommitPartial);
-  p.row_cnt_bytes = static_cast<size_t>(rows) * sizeof(int);
-  p.blk_cnt_bytes = static_cast<size_t>(B) * sizeof(int);
-  p.work_bytes = 0;
+  p.fin_threads = (L < 32 ? L : 32) * 32;
   (void)V;
   return p;
 }
@@ -525,8 +555,7 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms) {
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream,
-                          bool programmatic) {
+                          int* err, cudaStream_t stream, bool programmatic) {
   static size_t attr = 0;
   if (plan.smem_bytes > attr) {
     cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -546,14 +575,17 @@ cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, in
   args.conf_out = conf_out;
   args.commit_out = commit_out;
   args.part = part;
-  args.row_cnt = row_cnt;
-  args.blk_cnt = blk_cnt;
   args.err = err;
+  cudaError_t e;
   if (!programmatic) {
     commit_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(args);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+  } else {
+    e = launch_pdl(commit_kernel, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream, args);
   }
-  return launch_pdl(commit_kernel, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream, args);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(commit_finalize_kernel, dim3(B), dim3(plan.fin_threads), 0, stream, args,
+                    plan.grid);
 }
 
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream) {

@@ -4,20 +4,20 @@
 // GPU's memory up front for its own pools (model weights, the paged KV cache) and hands
 // out nothing else, or a latency-critical decode loop where an allocation's implicit device
 // synchronisation is not acceptable.  This entry point runs the same kernel as
-// bdlm_confidence_commit, but its scratch (split partials and arrival counters) lives in a
+// bdlm_confidence_commit, but its scratch (per-warp partial results and an error word) lives in a
 // fixed file-scope device array that is part of the loaded module, so no call allocates or
 // frees anything.
 //
 // Limits and behaviour (also stated in include/bdlm.h):
 //  * B * L <= kNoAllocMaxRows (2048) and V <= kNoAllocMaxVocab (262144); larger problems are
 //    rejected with BDLM_ERR_UNSUPPORTED before anything is launched.
-//  * The array (about 80 KiB) stays resident on every GPU that loads the library until the
+//  * The array (about 96 KiB) stays resident on every GPU that loads the library until the
 //    process exits.
 //  * The first call on a device looks the array's device address up (cudaGetSymbolAddress)
 //    with that device current; make that first call before any stream capture.
 //  * Every call shares the one array: calls that overlap on the GPU (different streams, or
 //    different host threads without ordering) race and give wrong results.  Each call clears
-//    the counters it needs with cudaMemsetAsync on its own stream before the kernel.
+//    the array's device error word with cudaMemsetAsync on its own stream before the kernels.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -32,9 +32,8 @@ namespace {
 constexpr int kNoAllocMaxRows = 2048;
 constexpr int kNoAllocMaxVocab = 262144;
 constexpr int kNoAllocMaxWarps = 16 * 256;  // the commit kernel runs 16 warps per SM
-// layout: [error word][row counters: max rows][block counters: max rows] ints, then partials
-constexpr size_t kCounterInts = 1 + 2 * static_cast<size_t>(kNoAllocMaxRows);
-constexpr size_t kCounterBytes = ((kCounterInts * sizeof(int)) + 255) / 256 * 256;
+// layout: [error word] padded to 256 bytes, then the per-(warp, row segment) partials
+constexpr size_t kCounterBytes = 256;
 constexpr size_t kPartialBytes =
     static_cast<size_t>(kNoAllocMaxWarps + kNoAllocMaxRows) * sizeof(bdlm::CommitPartial);
 constexpr size_t kScratchBytes = kCounterBytes + kPartialBytes;
@@ -90,16 +89,12 @@ extern "C" int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uin
   const bdlm::CommitPlan plan = bdlm::plan_commit(B, L, V, sms);
   if (plan.part_bytes > kPartialBytes) return BDLM_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int* counters = static_cast<int*>(base);
-  int* err = counters;
-  int* row_cnt = counters + 1;
-  int* blk_cnt = row_cnt + static_cast<size_t>(B) * L;
-  const size_t clear = (1 + static_cast<size_t>(B) * L + B) * sizeof(int);
-  if (cudaMemsetAsync(counters, 0, clear, s) != cudaSuccess) return BDLM_ERR_CUDA;
+  int* err = static_cast<int*>(base);
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return BDLM_ERR_CUDA;
   auto* part = reinterpret_cast<bdlm::CommitPartial*>(static_cast<unsigned char*>(base) +
                                                       kCounterBytes);
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
-                                      conf_out, commit_out, plan, part, row_cnt, blk_cnt, err, s,
+                                      conf_out, commit_out, plan, part, err, s,
                                       /*programmatic=*/false);  // ordered after the memset
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }

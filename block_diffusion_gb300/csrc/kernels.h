@@ -41,17 +41,17 @@ struct CommitPlan {
   int S = 1;                  // partial results per row and warp
   int chunk = 0;              // logits per shared-memory stage
   long long total_items = 0;  // rows
-  int grid = 1;               // CTAs (one per SM, persistent)
+  int grid = 1;               // streaming CTAs (one per SM, persistent)
+  int fin_threads = 32;       // threads of a finalizing CTA (one CTA per block)
   size_t smem_bytes = 0;
-  size_t part_bytes = 0, row_cnt_bytes = 0, blk_cnt_bytes = 0, work_bytes = 0;
+  size_t part_bytes = 0;      // one partial per (streaming warp, masked row segment)
 };
 
 CommitPlan plan_commit(int B, int L, int V, int num_sms);
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* row_cnt, int* blk_cnt, int* err, cudaStream_t stream,
-                          bool programmatic = true);
+                          int* err, cudaStream_t stream, bool programmatic = true);
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention

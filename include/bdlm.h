@@ -19,7 +19,7 @@
  *    skipped (zero data / no write) and recorded in a device error word that
  *    bdlm_device_error() reads and clears.  Every wait inside a kernel is bounded; a
  *    wait that gives up is recorded the same way.
- *  - Scratch (split-KV partial results, cross-CTA counters, the gathered LM-head rows)
+ *  - Scratch (split-KV and commit partial results, scheduler counters, the gathered LM-head rows)
  *    lives in a per-device workspace that the library allocates on first need and grows
  *    when a larger problem arrives (growing synchronises the device).  Calls that share
  *    a device must not run concurrently on different streams: they share that
@@ -148,14 +148,14 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
  * cannot afford an allocation's implicit synchronisation).
  *
  * Same arguments, layouts and results as bdlm_confidence_commit.  Its scratch lives in a
- * fixed device array of about 80 KiB inside the library, resident on every GPU that loads
+ * fixed device array of about 96 KiB inside the library, resident on every GPU that loads
  * it until the process exits; nothing is allocated or freed per call.
  *  - Limits: B*L <= 2048 and V <= 262144; larger problems return BDLM_ERR_UNSUPPORTED
  *    before any launch.
  *  - The first call on a device looks up the array's address with that device current;
  *    make that first call before any stream capture.
  *  - All calls share the array, which keeps the last call's contents: each call clears its
- *    counters on `stream` first, and calls that overlap on the GPU race.
+ *    error word on `stream` first, and calls that overlap on the GPU race.
  */
 int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uint8_t* mask, int B, int L,
                                    int V, float threshold, float temperature, int32_t* tok_out,
