@@ -181,6 +181,7 @@ class ClockSampler:
 # --------------------------------------------------------------------------- workload
 H_LM = 2560          # SDAR-4B hidden size
 REF_SEQS = 16        # sequences per step of the CPU oracle's bounded sample
+REF_SEQS_1CORE = 2   # sequences of the one-core oracle sample
 
 
 def make_workload(seed: int, compact_pool: bool = False):
@@ -432,11 +433,23 @@ def cpu_baseline(a, ci, lm, min_seconds=10.0):
         if el >= min_seconds:
             break
     per = el / reps
-    return {"value": len(seqs) * a.L / per, "unit": UNIT, "cores": oracle.num_threads(),
+    cores = oracle.num_threads()
+    # the same oracle on one core, over a smaller sample
+    one = np.arange(REF_SEQS_1CORE, dtype=np.int32)
+    oracle.set_num_threads(1)
+    try:
+        t1 = time.perf_counter()
+        cpu_oracle_round(a, ci, lm, one)
+        el1 = time.perf_counter() - t1
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": len(seqs) * a.L / per, "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} x the round of {REF_SEQS} of the 128 config-2 sequences "
                       f"(attention, LM head on their masked rows, commit), fp64 C++ OpenMP, "
-                      f"{per:.2f} s each"}
+                      f"{per:.2f} s each",
+            "value_1core": len(one) * a.L / el1,
+            "sample_1core": f"the round of {REF_SEQS_1CORE} sequences on one thread, {el1:.2f} s"}
 
 
 # --------------------------------------------------------------------------- arms

@@ -57,6 +57,8 @@ def _load():
             lib.oracle_apply_commit.argtypes = [I, P, P]
             lib.oracle_apply_commit.restype = None
             lib.oracle_num_threads.restype = I
+            lib.oracle_set_num_threads.argtypes = [I]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
@@ -67,6 +69,11 @@ def _ptr(a):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads for later oracle calls."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def block_attention(q, k_pages, v_pages, page_table, prefix_lens, L, Hq, Hkv, D, P,

@@ -269,4 +269,13 @@ int oracle_num_threads(void) {
 #endif
 }
 
+// Sets the OpenMP thread count of later oracle calls (n >= 1).
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 }  // extern "C"
