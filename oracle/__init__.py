@@ -54,6 +54,9 @@ def _load():
             lib.oracle_confidence_commit.argtypes = [I, I, I, P, P, ctypes.c_double,
                                                      ctypes.c_double, P, I, P, P, P, P, P]
             lib.oracle_confidence_commit.restype = I
+            lib.oracle_confidence_commit_rule.argtypes = [I, I, I, P, P, I, I, ctypes.c_double,
+                                                          ctypes.c_double, P, I, P, P, P, P, P]
+            lib.oracle_confidence_commit_rule.restype = I
             lib.oracle_apply_commit.argtypes = [I, P, P]
             lib.oracle_apply_commit.restype = None
             lib.oracle_num_threads.restype = I
@@ -142,8 +145,15 @@ class CommitResult:
         self.tok, self.conf, self.conf32, self.commit, self.near = tok, conf, conf32, commit, near
 
 
-def confidence_commit(logits, mask, threshold, temperature, blocks=None) -> CommitResult:
-    """Per-position argmax token and confidence, and the per-block commit decision."""
+# Commit rules (JetEngine notes, "Remasking Strategies"): threshold = low_confidence_dynamic,
+# top-k = low_confidence_static, sequential / anti-sequential = left-to-right / right-to-left.
+RULE_THRESHOLD, RULE_TOPK, RULE_SEQUENTIAL, RULE_ANTI_SEQUENTIAL = 0, 1, 2, 3
+
+
+def confidence_commit(logits, mask, threshold, temperature, blocks=None, rule=RULE_THRESHOLD,
+                      k=1) -> CommitResult:
+    """Per-position argmax token and confidence, and the per-block commit decision by `rule`
+    (k positions per block for the top-k and sequential rules)."""
     lib = _load()
     mask = np.ascontiguousarray(mask, dtype=np.uint8)
     B, L = mask.shape
@@ -155,9 +165,10 @@ def confidence_commit(logits, mask, threshold, temperature, blocks=None) -> Comm
     commit = np.zeros((B, L), dtype=np.uint8)
     near = np.zeros((B, L), dtype=np.uint8)
     bl = None if blocks is None else np.ascontiguousarray(blocks, dtype=np.int32)
-    rc = lib.oracle_confidence_commit(B, L, V, _ptr(logits), _ptr(mask), float(threshold),
-                                      float(temperature), _ptr(bl), 0 if bl is None else len(bl),
-                                      _ptr(tok), _ptr(conf), _ptr(conf32), _ptr(commit), _ptr(near))
+    rc = lib.oracle_confidence_commit_rule(B, L, V, _ptr(logits), _ptr(mask), int(rule), int(k),
+                                           float(threshold), float(temperature), _ptr(bl),
+                                           0 if bl is None else len(bl), _ptr(tok), _ptr(conf),
+                                           _ptr(conf32), _ptr(commit), _ptr(near))
     if rc != 0:
         raise ValueError("oracle_confidence_commit: bad arguments")
     return CommitResult(tok, conf, conf32, commit, near)

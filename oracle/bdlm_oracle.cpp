@@ -19,6 +19,7 @@
 //    (dynamic decoding): commit every masked position whose confidence clears a threshold.
 // Readings where the pages are silent are listed beside each function.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -175,35 +176,42 @@ int oracle_lm_head(int n_rows, int H, int V, const uint16_t* hidden, const uint1
     return bad ? -1 : 0;
 }
 
-// Confidence and commit of one denoising step (low_confidence_dynamic / threshold rule).
+// Confidence and commit of one denoising step.
 //
 // For every masked position i of block b, from row b*L+i of the logits:
 //     tok  = argmax_v l_v                (first index of the maximum)
 //     m    = l_tok
 //     conf = 1 / sum_v exp((l_v - m) / T)   (the largest softmax probability at temperature T)
-// Per block: commit = { masked i : conf_i >= threshold }; if that set is empty and the block
-// has a masked position, commit = { the masked i with the largest conf } (lowest i on ties).
-// Readings: the threshold comparison is "at or above"; the fallback commits the single most
-// confident position (JetEngine's notes fall back to left-to-right order instead; this
-// oracle follows the "at least the most confident position" reading); confidences are
-// compared after rounding to float32, the precision the GPU reports them in.
-// Unmasked positions give tok = -1, conf = -inf, commit = 0.
-// near: bit 0 = |conf - threshold| <= 1e-5 * threshold (a decision that may legitimately
-// differ), bit 1 = the block used the fallback and its top two confidences are within
-// 1e-5 relative of each other.
+// Unmasked positions give tok = -1, conf = -inf, commit = 0.  Per block, by rule
+// (JetEngine notes, "Remasking Strategies"):
+//   0 threshold (low_confidence_dynamic): commit = { masked i : conf_i >= threshold }; if that
+//     set is empty and the block has a masked position, the single most confident masked i
+//     (lowest i on ties).  Readings: "at or above"; the fallback commits the most confident
+//     position (the notes fall back to left-to-right order instead).
+//   1 top-k (low_confidence_static): the k masked positions of highest confidence (lowest i
+//     first among equal confidences), or every masked position if there are fewer than k.
+//   2 sequential: the k leftmost masked positions (left-to-right unmasking).
+//   3 anti-sequential: the k rightmost masked positions.
+// Confidences are compared after rounding to float32, the precision the GPU reports them in.
+// near: bit 0 = |conf - threshold| <= 1e-5 * threshold (rule 0; a decision that may
+// legitimately differ), bit 1 = a confidence tie within 1e-5 relative decided the position:
+// the fallback's top two (rule 0) or the last chosen and first unchosen (rule 1).
 // blocks (n_blocks; NULL = all B) selects the blocks computed.
-int oracle_confidence_commit(int B, int L, int V, const uint16_t* logits, const uint8_t* mask,
-                             double threshold, double temperature, const int32_t* blocks,
-                             int n_blocks, int32_t* tok, double* conf, float* conf32,
-                             uint8_t* commit, uint8_t* near) {
+int oracle_confidence_commit_rule(int B, int L, int V, const uint16_t* logits,
+                                  const uint8_t* mask, int rule, int k, double threshold,
+                                  double temperature, const int32_t* blocks, int n_blocks,
+                                  int32_t* tok, double* conf, float* conf32, uint8_t* commit,
+                                  uint8_t* near) {
     if (L <= 0 || V <= 0 || !(temperature > 0.0)) return -1;
+    if (rule < 0 || rule > 3 || (rule > 0 && k < 1)) return -1;
     const int count = blocks ? n_blocks : B;
     const float thr32 = static_cast<float>(threshold);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int bi = 0; bi < count; ++bi) {
         const int b = blocks ? blocks[bi] : bi;
+        const size_t r0 = static_cast<size_t>(b) * L;
         for (int i = 0; i < L; ++i) {
-            const size_t r = static_cast<size_t>(b) * L + i;
+            const size_t r = r0 + i;
             near[r] = 0;
             commit[r] = 0;
             if (!mask[r]) {
@@ -224,35 +232,69 @@ int oracle_confidence_commit(int B, int L, int V, const uint16_t* logits, const 
             tok[r] = best;
             conf[r] = 1.0 / z;
             conf32[r] = static_cast<float>(conf[r]);
-            if (std::fabs(conf[r] - threshold) <= 1e-5 * threshold) near[r] |= 1;
+            if (rule == 0 && std::fabs(conf[r] - threshold) <= 1e-5 * threshold) near[r] |= 1;
         }
-        bool any_masked = false, any_commit = false;
-        for (int i = 0; i < L; ++i) {
-            const size_t r = static_cast<size_t>(b) * L + i;
-            if (!mask[r]) continue;
-            any_masked = true;
-            if (conf32[r] >= thr32) { commit[r] = 1; any_commit = true; }
-        }
-        if (any_masked && !any_commit) {
-            int arg = -1;
-            for (int i = 0; i < L; ++i) {
-                const size_t r = static_cast<size_t>(b) * L + i;
-                if (!mask[r]) continue;
-                if (arg < 0 || conf32[r] > conf32[static_cast<size_t>(b) * L + arg]) arg = i;
-            }
-            commit[static_cast<size_t>(b) * L + arg] = 1;
-            const double top = conf[static_cast<size_t>(b) * L + arg];
-            for (int i = 0; i < L; ++i) {
-                const size_t r = static_cast<size_t>(b) * L + i;
-                if (!mask[r] || i == arg) continue;
-                if (std::fabs(conf[r] - top) <= 1e-5 * top) {
-                    near[r] |= 2;
-                    near[static_cast<size_t>(b) * L + arg] |= 2;
+        std::vector<int> masked;
+        for (int i = 0; i < L; ++i)
+            if (mask[r0 + i]) masked.push_back(i);
+        if (masked.empty()) continue;
+        if (rule == 0) {
+            bool any_commit = false;
+            for (int i : masked)
+                if (conf32[r0 + i] >= thr32) { commit[r0 + i] = 1; any_commit = true; }
+            if (!any_commit) {
+                int arg = -1;
+                for (int i : masked)
+                    if (arg < 0 || conf32[r0 + i] > conf32[r0 + arg]) arg = i;
+                commit[r0 + arg] = 1;
+                const double top = conf[r0 + arg];
+                for (int i : masked) {
+                    if (i == arg) continue;
+                    if (std::fabs(conf[r0 + i] - top) <= 1e-5 * top) {
+                        near[r0 + i] |= 2;
+                        near[r0 + arg] |= 2;
+                    }
                 }
+            }
+        } else if (rule == 1) {
+            // selection by confidence: repeatedly the most confident unchosen position
+            const int n = std::min<int>(k, static_cast<int>(masked.size()));
+            std::vector<char> chosen(L, 0);
+            int last = -1;
+            for (int c = 0; c < n; ++c) {
+                int arg = -1;
+                for (int i : masked)
+                    if (!chosen[i] && (arg < 0 || conf32[r0 + i] > conf32[r0 + arg])) arg = i;
+                chosen[arg] = 1;
+                commit[r0 + arg] = 1;
+                last = arg;
+            }
+            for (int i : masked) {
+                if (chosen[i]) continue;
+                const double lc = conf[r0 + last];
+                if (std::fabs(conf[r0 + i] - lc) <= 1e-5 * lc) {
+                    near[r0 + i] |= 2;
+                    near[r0 + last] |= 2;
+                }
+            }
+        } else {
+            const int n = std::min<int>(k, static_cast<int>(masked.size()));
+            for (int c = 0; c < n; ++c) {
+                const int i = rule == 2 ? masked[c] : masked[masked.size() - 1 - c];
+                commit[r0 + i] = 1;
             }
         }
     }
     return 0;
+}
+
+// The threshold rule (low_confidence_dynamic): oracle_confidence_commit_rule with rule 0.
+int oracle_confidence_commit(int B, int L, int V, const uint16_t* logits, const uint8_t* mask,
+                             double threshold, double temperature, const int32_t* blocks,
+                             int n_blocks, int32_t* tok, double* conf, float* conf32,
+                             uint8_t* commit, uint8_t* near) {
+    return oracle_confidence_commit_rule(B, L, V, logits, mask, 0, 1, threshold, temperature,
+                                         blocks, n_blocks, tok, conf, conf32, commit, near);
 }
 
 // Mask update between steps: mask &= ~commit (JetEngine notes, "Important Patterns":

@@ -42,6 +42,10 @@ def _parse_golden():
             cases.append(dict(name=parts[0].split()[1], mask=[int(c) for c in parts[1]],
                               replace=parts[2], tau=float(parts[3]), T=float(parts[4]),
                               commit=[int(c) for c in parts[5]]))
+        elif parts[0].startswith("rcase"):
+            cases.append(dict(name=parts[0].split()[1], mask=[int(c) for c in parts[1]],
+                              replace=parts[2], rule=parts[3], k=int(parts[4]), tau=0.5, T=1.0,
+                              commit=[int(c) for c in parts[5]]))
     return rows, cases
 
 
@@ -80,6 +84,61 @@ def test_commit_worked_example(case):
         assert res.near[0, 0] & 1  # conf exactly at the threshold is flagged
     if case == "E":
         assert res.near[0, 0] & 2 and res.near[0, 2] & 2  # confidence tie flagged
+
+
+RULES = {"topk": oracle.RULE_TOPK, "sequential": oracle.RULE_SEQUENTIAL,
+         "anti_sequential": oracle.RULE_ANTI_SEQUENTIAL}
+
+
+@pytest.mark.parametrize("case", ["F", "G", "H", "I", "J", "K", "L", "M"])
+def test_commit_rules_worked_example(case):
+    rows, cases = _parse_golden()
+    c = [x for x in cases if x["name"] == case][0]
+    logits = np.array([rows[r]["logits"] for r in range(4)], dtype=np.float32)
+    if c["replace"] != "-":
+        rr, vals = c["replace"].split("=")
+        logits[int(rr)] = [float(x) for x in vals.split(",")]
+    bits = f32_to_bf16_bits(logits)
+    mask = np.array([c["mask"]], dtype=np.uint8)
+    res = oracle.confidence_commit(bits, mask, c["tau"], c["T"], rule=RULES[c["rule"]], k=c["k"])
+    assert list(res.commit[0]) == c["commit"]
+    if case == "I":
+        assert res.near[0, 1] & 2 and res.near[0, 2] & 2  # the tie at the cut is flagged
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 9])
+def test_commit_rules_against_numpy(k):
+    """Top-k against a stable argsort of float32 confidences; sequential rules against the
+    masked positions in order; every rule commits min(k, masked) masked positions."""
+    rng = np.random.default_rng(31 + k)
+    B, L, V = 12, 8, 500
+    bits = make_logits(rng, B * L, V, peak_height=(0.0, 12.0))
+    mask = make_mask_fixed_fraction(rng, B, L, 0.6)
+    mask[3] = 0
+    for rule in (oracle.RULE_TOPK, oracle.RULE_SEQUENTIAL, oracle.RULE_ANTI_SEQUENTIAL):
+        res = oracle.confidence_commit(bits, mask, 0.5, 1.0, rule=rule, k=k)
+        for b in range(B):
+            pos = np.nonzero(mask[b])[0]
+            n = min(k, len(pos))
+            if rule == oracle.RULE_TOPK:
+                order = pos[np.argsort(-res.conf32[b, pos], kind="stable")]
+                want = set(order[:n].tolist())
+            elif rule == oracle.RULE_SEQUENTIAL:
+                want = set(pos[:n].tolist())
+            else:
+                want = set(pos[len(pos) - n:].tolist())
+            got = set(np.nonzero(res.commit[b])[0].tolist())
+            assert got == want, (rule, b)
+        assert np.all(res.commit <= mask)
+
+
+def test_commit_rule_arguments_checked():
+    bits = f32_to_bf16_bits(np.zeros((4, 8), np.float32))
+    mask = np.ones((1, 4), np.uint8)
+    with pytest.raises(ValueError):
+        oracle.confidence_commit(bits, mask, 0.5, 1.0, rule=oracle.RULE_TOPK, k=0)
+    with pytest.raises(ValueError):
+        oracle.confidence_commit(bits, mask, 0.5, 1.0, rule=7)
 
 
 @pytest.mark.parametrize("T", [1.0, 0.5, 1.7])
