@@ -5,8 +5,8 @@ Argument marshalling only.  Every step of the round runs in the CUDA kernels of
 fallback: if the library is missing or the device is not sm_103 the calls raise.
 
 Entry points mirror ``include/bdlm.h``:
-    bdlm_block_attention, bdlm_lm_head, bdlm_confidence_commit, bdlm_apply_commit,
-    bdlm_status_string, bdlm_device_error, bdlm_release
+    bdlm_block_attention, bdlm_lm_head, bdlm_confidence_commit, bdlm_confidence_commit_rule,
+    bdlm_apply_commit, bdlm_status_string, bdlm_device_error, bdlm_release
 """
 from __future__ import annotations
 
@@ -27,8 +27,14 @@ BDLM_DEVERR_LENGTH = 2
 BDLM_DEVERR_TIMEOUT = 4
 BDLM_DEVERR_ROW = 8
 
+BDLM_COMMIT_THRESHOLD = 0
+BDLM_COMMIT_TOPK = 1
+BDLM_COMMIT_SEQUENTIAL = 2
+BDLM_COMMIT_ANTI_SEQUENTIAL = 3
+
 EXPORTS = ("bdlm_block_attention", "bdlm_lm_head", "bdlm_confidence_commit",
-           "bdlm_apply_commit", "bdlm_status_string", "bdlm_device_error", "bdlm_release")
+           "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_status_string",
+           "bdlm_device_error", "bdlm_release")
 
 
 class AttnDesc(ctypes.Structure):
@@ -63,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bdlm_lm_head.restype = I
     lib.bdlm_confidence_commit.argtypes = [P, P, I, I, I, F, F, P, P, P, P]
     lib.bdlm_confidence_commit.restype = I
+    lib.bdlm_confidence_commit_rule.argtypes = [P, P, I, I, I, I, I, F, F, P, P, P, P]
+    lib.bdlm_confidence_commit_rule.restype = I
     lib.bdlm_apply_commit.argtypes = [P, P, I, P]
     lib.bdlm_apply_commit.restype = I
     lib.bdlm_status_string.argtypes = [I]
@@ -129,6 +137,17 @@ def bdlm_confidence_commit(logits, mask, B: int, L: int, V: int, threshold: floa
                                     float(threshold), float(temperature), _ptr(tok_out),
                                     _ptr(conf_out), _ptr(commit_out), _stream(stream))
     _check("bdlm_confidence_commit", rc)
+
+
+def bdlm_confidence_commit_rule(logits, mask, B: int, L: int, V: int, rule: int, k: int,
+                                threshold: float, temperature: float, tok_out, conf_out,
+                                commit_out, stream=None) -> None:
+    lib = load_library()
+    rc = lib.bdlm_confidence_commit_rule(_ptr(logits), _ptr(mask), int(B), int(L), int(V),
+                                         int(rule), int(k), float(threshold), float(temperature),
+                                         _ptr(tok_out), _ptr(conf_out), _ptr(commit_out),
+                                         _stream(stream))
+    _check("bdlm_confidence_commit_rule", rc)
 
 
 def bdlm_apply_commit(mask, commit, n: int, stream=None) -> None:

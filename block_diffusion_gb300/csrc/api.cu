@@ -153,9 +153,20 @@ int bdlm_release(void) {
 int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, int L, int V,
                            float threshold, float temperature, int32_t* tok_out,
                            float* conf_out, uint8_t* commit_out, bdlm_stream stream) {
+  return bdlm_confidence_commit_rule(logits, mask, B, L, V, BDLM_COMMIT_THRESHOLD, 1, threshold,
+                                     temperature, tok_out, conf_out, commit_out, stream);
+}
+
+int bdlm_confidence_commit_rule(const bdlm_bf16* logits, const uint8_t* mask, int B, int L, int V,
+                                int rule, int k, float threshold, float temperature,
+                                int32_t* tok_out, float* conf_out, uint8_t* commit_out,
+                                bdlm_stream stream) {
   if (B < 0 || L < 1 || L > 64 || V < 1) return BDLM_ERR_INVALID;
   if (!(temperature > 0.f) || !isfinite(temperature)) return BDLM_ERR_INVALID;
-  if (!(threshold >= 0.f && threshold <= 1.f)) return BDLM_ERR_INVALID;
+  if (rule < BDLM_COMMIT_THRESHOLD || rule > BDLM_COMMIT_ANTI_SEQUENTIAL) return BDLM_ERR_INVALID;
+  if (rule == BDLM_COMMIT_THRESHOLD && !(threshold >= 0.f && threshold <= 1.f))
+    return BDLM_ERR_INVALID;
+  if (rule != BDLM_COMMIT_THRESHOLD && k < 1) return BDLM_ERR_INVALID;
   if (B == 0) return BDLM_OK;
   if (!logits || !mask || !tok_out || !conf_out || !commit_out) return BDLM_ERR_INVALID;
   if (static_cast<long long>(B) * L > 0x7FFFFFFFll) return BDLM_ERR_INVALID;
@@ -170,7 +181,7 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
                                       conf_out, commit_out, plan,
                                       static_cast<bdlm::CommitPartial*>(st->data), st->err,
-                                      static_cast<cudaStream_t>(stream));
+                                      static_cast<cudaStream_t>(stream), true, rule, k);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 

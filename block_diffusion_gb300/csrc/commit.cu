@@ -212,6 +212,7 @@ struct CommitArgs {
   uint8_t* commit_out;
   CommitPartial* part;
   int* err;  // device error word (may be null)
+  int rule, k;  // block decision: BDLM_COMMIT_* and positions per block
 };
 
 // First logit (in the masked concatenation) of warp w out of W; a multiple of 8.
@@ -505,25 +506,47 @@ commit_finalize_kernel(const CommitArgs a, int stream_grid) {
   __syncthreads();
   if (tid == 0) {
     uint8_t* co = a.commit_out + static_cast<size_t>(b) * L;
-    int any_masked = 0, any_commit = 0, best = -1;
-    float best_c = 0.f;
-    for (int i = 0; i < L; ++i) {
-      uint8_t cm = 0;
-      if (mk[i]) {
+    uint64_t sel = 0;  // bit i: commit position i
+    int n_masked = 0;
+    for (int i = 0; i < L; ++i) n_masked += mk[i] != 0;
+    if (a.rule == BDLM_COMMIT_THRESHOLD) {
+      int best = -1;
+      float best_c = 0.f;
+      for (int i = 0; i < L; ++i) {
+        if (!mk[i]) continue;
         const float ci = s_conf[i];
-        any_masked = 1;
-        if (ci >= a.threshold) {
-          cm = 1;
-          any_commit = 1;
-        }
+        if (ci >= a.threshold) sel |= 1ull << i;
         if (best < 0 || ci > best_c) {
           best = i;
           best_c = ci;
         }
       }
-      co[i] = cm;
+      if (n_masked && !sel) sel = 1ull << best;  // at least the most confident position
+    } else if (a.rule == BDLM_COMMIT_TOPK) {
+      const int n = min(a.k, n_masked);
+      for (int c = 0; c < n; ++c) {  // the most confident position not yet chosen
+        int best = -1;
+        float best_c = 0.f;
+        for (int i = 0; i < L; ++i) {
+          if (!mk[i] || ((sel >> i) & 1)) continue;
+          if (best < 0 || s_conf[i] > best_c) {
+            best = i;
+            best_c = s_conf[i];
+          }
+        }
+        sel |= 1ull << best;
+      }
+    } else {
+      const bool left = a.rule == BDLM_COMMIT_SEQUENTIAL;
+      int n = min(a.k, n_masked);
+      for (int j = 0; j < L && n > 0; ++j) {
+        const int i = left ? j : L - 1 - j;
+        if (!mk[i]) continue;
+        sel |= 1ull << i;
+        --n;
+      }
     }
-    if (any_masked && !any_commit) co[best] = 1;
+    for (int i = 0; i < L; ++i) co[i] = static_cast<uint8_t>((sel >> i) & 1);
   }
 }
 
@@ -555,7 +578,7 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms) {
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* err, cudaStream_t stream, bool programmatic) {
+                          int* err, cudaStream_t stream, bool programmatic, int rule, int k) {
   static size_t attr = 0;
   if (plan.smem_bytes > attr) {
     cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -576,6 +599,8 @@ cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, in
   args.commit_out = commit_out;
   args.part = part;
   args.err = err;
+  args.rule = rule;
+  args.k = k;
   cudaError_t e;
   if (!programmatic) {
     commit_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(args);

@@ -51,7 +51,8 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms);
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* err, cudaStream_t stream, bool programmatic = true);
+                          int* err, cudaStream_t stream, bool programmatic = true,
+                          int rule = BDLM_COMMIT_THRESHOLD, int k = 1);
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
 
 // ------------------------------------------------------------------ attention

@@ -141,6 +141,35 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
                            float threshold, float temperature, int32_t* tok_out,
                            float* conf_out, uint8_t* commit_out, bdlm_stream stream);
 
+/* Commit rules of bdlm_confidence_commit_rule. */
+enum {
+  BDLM_COMMIT_THRESHOLD = 0,       /* low_confidence_dynamic: as bdlm_confidence_commit */
+  BDLM_COMMIT_TOPK = 1,            /* low_confidence_static: the k most confident */
+  BDLM_COMMIT_SEQUENTIAL = 2,      /* the k leftmost masked positions */
+  BDLM_COMMIT_ANTI_SEQUENTIAL = 3  /* the k rightmost masked positions */
+};
+
+/*
+ * Confidence and commit with a selectable rule.
+ * Source: JetEngine notes, "Remasking Strategies" (sequential: unmask left to right;
+ * low_confidence_static: unmask the top-k by confidence; low_confidence_dynamic: unmask above
+ * a threshold; anti_sequential is named beside sequential in the notes' scheduler tree).
+ *
+ * tok_out and conf_out are those of bdlm_confidence_commit for every rule.  Per block:
+ *   BDLM_COMMIT_THRESHOLD        exactly bdlm_confidence_commit (k ignored);
+ *   BDLM_COMMIT_TOPK             the min(k, masked) masked positions of highest confidence
+ *                                (compared as float32; lower position first among equals);
+ *   BDLM_COMMIT_SEQUENTIAL       the min(k, masked) leftmost masked positions;
+ *   BDLM_COMMIT_ANTI_SEQUENTIAL  the min(k, masked) rightmost masked positions.
+ * k >= 1 for the last three (e.g. L / denoising steps); threshold is checked only for the
+ * threshold rule.  Layouts, limits and errors as bdlm_confidence_commit; an unknown rule or
+ * k < 1 returns BDLM_ERR_INVALID.
+ */
+int bdlm_confidence_commit_rule(const bdlm_bf16* logits, const uint8_t* mask, int B, int L, int V,
+                                int rule, int k, float threshold, float temperature,
+                                int32_t* tok_out, float* conf_out, uint8_t* commit_out,
+                                bdlm_stream stream);
+
 /*
  * bdlm_confidence_commit without any device allocation (the pages have no counterpart of
  * this entry point; it exists for callers that cannot let the library allocate: an engine

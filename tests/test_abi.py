@@ -13,8 +13,7 @@ HEADER = os.path.join(ROOT, "include", "bdlm.h")
 @pytest.fixture(scope="module")
 def so():
     from block_diffusion_gb300 import build, load_library
-    if not os.path.exists(build.OUT):
-        build.build()
+    build.build()  # incremental: recompiles only sources newer than their objects
     return load_library()
 
 

@@ -9,7 +9,7 @@ from gpu_util import bf16_tensor, compare_commit, dev, host
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(lib, logits_bits, mask, threshold, temperature):
+def run_gpu(lib, logits_bits, mask, threshold, temperature, rule=None, k=1):
     import torch
     B, L = mask.shape
     V = logits_bits.size // (B * L)
@@ -18,7 +18,11 @@ def run_gpu(lib, logits_bits, mask, threshold, temperature):
     tok = torch.empty((B, L), dtype=torch.int32, device="cuda")
     conf = torch.empty((B, L), dtype=torch.float32, device="cuda")
     com = torch.full((B, L), 7, dtype=torch.uint8, device="cuda")
-    lib.bdlm_confidence_commit(lg, mk, B, L, V, threshold, temperature, tok, conf, com)
+    if rule is None:
+        lib.bdlm_confidence_commit(lg, mk, B, L, V, threshold, temperature, tok, conf, com)
+    else:
+        lib.bdlm_confidence_commit_rule(lg, mk, B, L, V, rule, k, threshold, temperature, tok,
+                                        conf, com)
     torch.cuda.synchronize()
     return host(tok), host(conf), host(com)
 
@@ -85,8 +89,8 @@ def test_ties_go_to_lowest_index_and_position(lib):
     assert np.all(com.sum(1) == 1) and np.all(com[:, 0] == 1)  # equal confidences -> lowest i
 
 
-def test_repeated_calls_reuse_counters(lib):
-    """Counters are reset by the kernel: many calls in a row stay correct."""
+def test_repeated_calls_stay_correct(lib):
+    """Nothing carries over between calls: many calls in a row stay correct."""
     rng = np.random.default_rng(5)
     mask = W.make_mask_fixed_fraction(rng, 16, 4, 0.5)
     logits = W.poison_unmasked_rows(W.make_logits(rng, 64, 20000, peak_height=(0, 12)), mask)
@@ -105,3 +109,62 @@ def test_apply_commit(lib):
     lib.bdlm_apply_commit(m, dev(com), mask.size)
     torch.cuda.synchronize()
     assert np.array_equal(host(m), oracle.apply_commit(mask, com))
+
+
+RULES = [("topk", oracle.RULE_TOPK), ("sequential", oracle.RULE_SEQUENTIAL),
+         ("anti_sequential", oracle.RULE_ANTI_SEQUENTIAL)]
+
+
+@pytest.mark.parametrize("name,rule", RULES)
+@pytest.mark.parametrize("k", [1, 2, 5])
+def test_commit_rules(lib, name, rule, k):
+    """Top-k / sequential / anti-sequential commits against the oracle: config-4-like blocks
+    (L = 64, masked fraction U[0.1, 0.9]) and blocks without any masked position."""
+    rng = np.random.default_rng(100 + 10 * rule + k)
+    B, L, V = 6, 64, 20000
+    mask = np.zeros((B, L), np.uint8)
+    for b in range(B):
+        mask[b] = W.make_mask_fixed_fraction(rng, 1, L, rng.uniform(0.1, 0.9))[0]
+    mask[2] = 0
+    logits = W.poison_unmasked_rows(W.make_logits(rng, B * L, V, peak_height=(0, 16)), mask)
+    ref = oracle.confidence_commit(logits, mask, 0.5, 1.0, rule=rule, k=k)
+    tok, conf, com = run_gpu(lib, logits, mask, 0.5, 1.0, rule=lib.BDLM_COMMIT_TOPK
+                             if name == "topk" else lib.BDLM_COMMIT_SEQUENTIAL
+                             if name == "sequential" else lib.BDLM_COMMIT_ANTI_SEQUENTIAL, k=k)
+    compare_commit(ref, tok, conf, com, mask)
+    assert np.all(com.sum(1) == np.minimum(k, mask.sum(1)))
+    assert lib.bdlm_device_error() == 0
+
+
+def test_topk_full_size_config2(lib):
+    """Config 2 with the top-2 rule (k = L / 2 per step)."""
+    c = W.CONFIGS[2]
+    rng = np.random.default_rng(W.seed_for(2, 3))
+    ci = W.commit_inputs(2, rng, c["B"], c["L"], c["V"], supplementary=True)
+    ref = oracle.confidence_commit(ci.logits, ci.mask, ci.threshold, 1.0, rule=oracle.RULE_TOPK,
+                                   k=2)
+    tok, conf, com = run_gpu(lib, ci.logits, ci.mask, ci.threshold, 1.0,
+                             rule=lib.BDLM_COMMIT_TOPK, k=2)
+    compare_commit(ref, tok, conf, com, ci.mask)
+
+
+def test_threshold_rule_equals_default_entry_point(lib):
+    rng = np.random.default_rng(8)
+    mask = W.make_mask_fixed_fraction(rng, 8, 4, 0.75)
+    logits = W.poison_unmasked_rows(W.make_logits(rng, 32, 9000, peak_height=(0, 14)), mask)
+    a = run_gpu(lib, logits, mask, 0.4, 1.0)
+    b = run_gpu(lib, logits, mask, 0.4, 1.0, rule=lib.BDLM_COMMIT_THRESHOLD, k=3)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_rule_arguments_rejected(lib):
+    import torch
+    lg = torch.zeros((4, 16), dtype=torch.bfloat16, device="cuda")
+    mk = torch.ones((1, 4), dtype=torch.uint8, device="cuda")
+    tok = torch.empty((1, 4), dtype=torch.int32, device="cuda")
+    conf = torch.empty((1, 4), dtype=torch.float32, device="cuda")
+    com = torch.empty((1, 4), dtype=torch.uint8, device="cuda")
+    for rule, k in ((9, 1), (lib.BDLM_COMMIT_TOPK, 0), (-1, 1)):
+        with pytest.raises(lib.BdlmError):
+            lib.bdlm_confidence_commit_rule(lg, mk, 1, 4, 16, rule, k, 0.5, 1.0, tok, conf, com)
