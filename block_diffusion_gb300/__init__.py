@@ -32,7 +32,8 @@ BDLM_COMMIT_TOPK = 1
 BDLM_COMMIT_SEQUENTIAL = 2
 BDLM_COMMIT_ANTI_SEQUENTIAL = 3
 
-EXPORTS = ("bdlm_block_attention", "bdlm_lm_head", "bdlm_confidence_commit",
+EXPORTS = ("bdlm_block_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
+           "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
            "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_status_string",
            "bdlm_device_error", "bdlm_release")
 
@@ -71,6 +72,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bdlm_confidence_commit.restype = I
     lib.bdlm_confidence_commit_rule.argtypes = [P, P, I, I, I, I, I, F, F, P, P, P, P]
     lib.bdlm_confidence_commit_rule.restype = I
+    lib.bdlm_lm_head_device_count.argtypes = [P, P, P, P, I, I, I, I, P, P]
+    lib.bdlm_lm_head_device_count.restype = I
+    lib.bdlm_active_rows.argtypes = [P, P, I, I, P, P, P]
+    lib.bdlm_active_rows.restype = I
+    lib.bdlm_write_block_kv.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P]
+    lib.bdlm_write_block_kv.restype = I
     lib.bdlm_apply_commit.argtypes = [P, P, I, P]
     lib.bdlm_apply_commit.restype = I
     lib.bdlm_status_string.argtypes = [I]
@@ -148,6 +155,32 @@ def bdlm_confidence_commit_rule(logits, mask, B: int, L: int, V: int, rule: int,
                                          _ptr(tok_out), _ptr(conf_out), _ptr(commit_out),
                                          _stream(stream))
     _check("bdlm_confidence_commit_rule", rc)
+
+
+def bdlm_lm_head_device_count(hidden, w, active_idx, n_active_dev, max_active: int, n_rows: int,
+                              H: int, V: int, logits, stream=None) -> None:
+    lib = load_library()
+    rc = lib.bdlm_lm_head_device_count(_ptr(hidden), _ptr(w), _ptr(active_idx),
+                                       _ptr(n_active_dev), int(max_active), int(n_rows), int(H),
+                                       int(V), _ptr(logits), _stream(stream))
+    _check("bdlm_lm_head_device_count", rc)
+
+
+def bdlm_active_rows(mask, denoising, B: int, L: int, active_idx, n_active_dev,
+                     stream=None) -> None:
+    lib = load_library()
+    rc = lib.bdlm_active_rows(_ptr(mask), _ptr(denoising), int(B), int(L), _ptr(active_idx),
+                              _ptr(n_active_dev), _stream(stream))
+    _check("bdlm_active_rows", rc)
+
+
+def bdlm_write_block_kv(desc: AttnDesc, k_new, v_new, k_pages, v_pages, page_table, prefix_lens,
+                        stream=None) -> None:
+    lib = load_library()
+    rc = lib.bdlm_write_block_kv(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(k_pages),
+                                 _ptr(v_pages), _ptr(page_table), _ptr(prefix_lens),
+                                 _stream(stream))
+    _check("bdlm_write_block_kv", rc)
 
 
 def bdlm_apply_commit(mask, commit, n: int, stream=None) -> None:

@@ -250,8 +250,15 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 
-int bdlm_lm_head(const bdlm_bf16* hidden, const bdlm_bf16* w, const int32_t* active_idx,
-                 int n_active, int n_rows, int H, int V, bdlm_bf16* logits, bdlm_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// The LM head planned for n_active rows; n_active_dev (may be null) holds the count the
+// kernels use, read on the device (at most n_active).
+int lm_head_impl(const bdlm_bf16* hidden, const bdlm_bf16* w, const int32_t* active_idx,
+                 int n_active, const int32_t* n_active_dev, int n_rows, int H, int V,
+                 bdlm_bf16* logits, bdlm_stream stream) {
   if (n_active < 0 || n_rows < 0 || H < 8 || V < 8 || H % 8 != 0 || V % 8 != 0 ||
       n_active > n_rows)
     return BDLM_ERR_INVALID;
@@ -282,11 +289,70 @@ int bdlm_lm_head(const bdlm_bf16* hidden, const bdlm_bf16* w, const int32_t* act
     if ((rc = encode(&tm_h, gathered, 2, dims, strides, box))) return rc;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = bdlm::launch_gather_rows(hidden, active_idx, n_active, n_rows, H, gathered,
-                                           st->err, s);
+  cudaError_t e = bdlm::launch_gather_rows(hidden, active_idx, n_active, n_active_dev, n_rows, H,
+                                           gathered, st->err, s);
   if (e != cudaSuccess) return BDLM_ERR_CUDA;
-  e = bdlm::launch_lm_head(tm_w, tm_h, active_idx, n_active, n_rows, H, V, logits, plan, st->err,
-                           s);
+  e = bdlm::launch_lm_head(tm_w, tm_h, active_idx, n_active, n_active_dev, n_rows, H, V, logits,
+                           plan, st->err, s);
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bdlm_lm_head(const bdlm_bf16* hidden, const bdlm_bf16* w, const int32_t* active_idx,
+                 int n_active, int n_rows, int H, int V, bdlm_bf16* logits, bdlm_stream stream) {
+  return lm_head_impl(hidden, w, active_idx, n_active, nullptr, n_rows, H, V, logits, stream);
+}
+
+int bdlm_lm_head_device_count(const bdlm_bf16* hidden, const bdlm_bf16* w,
+                              const int32_t* active_idx, const int32_t* n_active_dev,
+                              int max_active, int n_rows, int H, int V, bdlm_bf16* logits,
+                              bdlm_stream stream) {
+  if (!n_active_dev) return BDLM_ERR_INVALID;
+  return lm_head_impl(hidden, w, active_idx, max_active, n_active_dev, n_rows, H, V, logits,
+                      stream);
+}
+
+int bdlm_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,
+                     int32_t* active_idx, int32_t* n_active_dev, bdlm_stream stream) {
+  if (B < 0 || L < 1 || L > 64 || static_cast<long long>(B) * L > 0x7FFFFFFFll)
+    return BDLM_ERR_INVALID;
+  if (!mask || !active_idx || !n_active_dev) return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  cudaError_t e = bdlm::launch_active_rows(mask, denoising, B, L, active_idx, n_active_dev,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
+int bdlm_write_block_kv(const bdlm_attn_desc* desc, const bdlm_bf16* k_new,
+                        const bdlm_bf16* v_new, bdlm_bf16* k_pages, bdlm_bf16* v_pages,
+                        const int32_t* page_table, const int32_t* prefix_lens, bdlm_stream stream) {
+  if (!desc) return BDLM_ERR_INVALID;
+  const bdlm_attn_desc d = *desc;
+  if (d.B < 0 || d.L < 1 || d.L > 64 || d.Hkv < 1 || d.D != 128 || d.page_size != 16 ||
+      d.max_pages_per_seq < 1 || d.num_pages < 1)
+    return BDLM_ERR_INVALID;
+  if (d.B == 0) return BDLM_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages || !page_table || !prefix_lens)
+    return BDLM_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+    return BDLM_ERR_INVALID;
+  if (static_cast<long long>(d.B) * d.L * d.Hkv > 0x7FFFFFFFll ||
+      static_cast<long long>(d.B) * d.max_pages_per_seq > 0x7FFFFFFFll)
+    return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  cudaError_t e = bdlm::launch_write_block_kv(k_new, v_new, k_pages, v_pages, page_table,
+                                              prefix_lens, d.B, d.L, d.Hkv, d.max_pages_per_seq,
+                                              d.num_pages, st->err,
+                                              static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 

@@ -91,11 +91,22 @@ struct LmHeadPlan {
 
 LmHeadPlan plan_lm_head(int n_active, int H, int V, int num_sms);
 cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* active_idx, int n_active,
-                               int n_rows, int H, uint16_t* gathered, int* err,
-                               cudaStream_t stream);
+                               const int32_t* n_active_dev, int n_rows, int H,
+                               uint16_t* gathered, int* err, cudaStream_t stream);
+// n_active_dev (may be null): the active-row count in device memory, at most n_active (the
+// count the launch is planned for); rows of active_idx past it are ignored.
 cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
-                           const int32_t* active_idx, int n_active, int n_rows, int H, int V,
+                           const int32_t* active_idx, int n_active,
+                           const int32_t* n_active_dev, int n_rows, int H, int V,
                            uint16_t* logits, const LmHeadPlan& plan, int* err,
                            cudaStream_t stream);
+
+// Device-side round pieces (round.cu).
+cudaError_t launch_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,
+                               int32_t* active_idx, int32_t* n_active, cudaStream_t stream);
+cudaError_t launch_write_block_kv(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages,
+                                  uint16_t* v_pages, const int32_t* page_table,
+                                  const int32_t* prefix_lens, int B, int L, int Hkv,
+                                  int max_pages, int num_pages, int* err, cudaStream_t stream);
 
 }  // namespace bdlm

@@ -56,18 +56,27 @@ template <> struct Cfg<256> { static constexpr int kW = 4, kH = 3, kCols = 256, 
 
 struct LmParams {
   const int32_t* active_idx;
+  const int32_t* n_active_dev;  // if set: the active-row count, read on the device (<= n_active)
   uint16_t* logits;
   int* err;
   int n_active, n_rows, H, V, bn, m_tiles, n_tiles, k_blocks;
 };
 
+// Active rows of this launch: the device-side count when there is one (clamped to the
+// planned maximum), else the planned count.  Read after the grid dependency is resolved.
+__device__ __forceinline__ int active_rows(const LmParams& p) {
+  if (p.n_active_dev == nullptr) return p.n_active;
+  return min(max(*p.n_active_dev, 0), p.n_active);
+}
+
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ hidden,
                                    const int32_t* __restrict__ active_idx, int n_active,
-                                   int n_rows, int H, uint16_t* __restrict__ gathered,
-                                   int* __restrict__ err) {
+                                   const int32_t* __restrict__ n_active_dev, int n_rows, int H,
+                                   uint16_t* __restrict__ gathered, int* __restrict__ err) {
   griddep_wait();
   griddep_launch_dependents();
   const int i = blockIdx.y;
+  if (n_active_dev != nullptr && i >= min(max(*n_active_dev, 0), n_active)) return;
   const int r = active_idx[i];
   const bool bad = r < 0 || r >= n_rows;
   if (bad && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, BDLM_DEVERR_ROW);
@@ -96,14 +105,14 @@ struct RingPos {
 // For W, a stage is the kSub boxes of the tile's sub-tiles (box_bytes each, kWBox apart).
 template <int NSTAGES, int STRIDE, bool IS_W>
 __device__ bool produce(const CUtensorMap* tm, uint8_t* ring, uint32_t box_bytes,
-                        uint64_t* full, uint64_t* empty, const LmParams& p, int n_tiles_total,
-                        int* abort_flag) {
+                        uint64_t* full, uint64_t* empty, const LmParams& p, int n_tiles,
+                        int n_tiles_total, int* abort_flag) {
   tma_prefetch_desc(tm);
   RingPos pos;
   bool ok = true;
   constexpr int kBoxes = IS_W ? kSub : 1;
   for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x) {
-    const int row0 = IS_W ? (t / p.n_tiles) * (kSub * kBM) : (t % p.n_tiles) * p.bn;
+    const int row0 = IS_W ? (t / n_tiles) * (kSub * kBM) : (t % n_tiles) * p.bn;
     for (int kb = 0; kb < p.k_blocks; ++kb) {
       if (!(ok = mbar_wait(&empty[pos.slot], pos.phase ^ 1, abort_flag))) break;
       mbar_arrive_expect_tx(&full[pos.slot], kBoxes * box_bytes);
@@ -145,7 +154,6 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_tiles_total = p.m_tiles * p.n_tiles;
   const uint32_t h_bytes = static_cast<uint32_t>(p.bn) * kBK * 2;   // one box of rows
 
   if (threadIdx.x == 0) {
@@ -174,17 +182,21 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
   tc_fence_after();
   griddep_wait();
   const uint32_t tmem = tmem_base;
+  // tiles of the N tiles that hold active rows only
+  const int n_act = active_rows(p);
+  const int n_tiles = (n_act + p.bn - 1) / p.bn;
+  const int n_tiles_total = p.m_tiles * n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
-      produce<kWS, kWBytes, true>(&tm_w, wring, kWBox, w_full, w_empty, p, n_tiles_total,
-                                  &abort_flag);
+      produce<kWS, kWBytes, true>(&tm_w, wring, kWBox, w_full, w_empty, p, n_tiles,
+                                  n_tiles_total, &abort_flag);
       griddep_launch_dependents();  // every W tile of this CTA is being loaded
     }
   } else if (warp == kRowWarp) {
     if (lane == 0)
-      produce<kHS, kHStage, false>(&tm_h, hring, h_bytes, h_full, h_empty, p, n_tiles_total,
-                                   &abort_flag);
+      produce<kHS, kHStage, false>(&tm_h, hring, h_bytes, h_full, h_empty, p, n_tiles,
+                                   n_tiles_total, &abort_flag);
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, p.bn, false, false);
@@ -236,8 +248,8 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     bool ok = true;
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x, ++i) {
-      const int m = t / p.n_tiles;
-      const int n = t % p.n_tiles;
+      const int m = t / n_tiles;
+      const int n = t % n_tiles;
       const int acc = i % kBufs;
       const int r0 = n * p.bn;
       // the tile's logits rows, read once (rows past n_active or out of range: -1, skipped;
@@ -245,7 +257,7 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
       named_barrier(1, kEpiThreads);   // the previous tile's readers are done
       for (int j = et; j < p.bn; j += kEpiThreads) {
         const int rr = r0 + j;
-        const int row = rr < p.n_active ? __ldg(p.active_idx + rr) : -1;
+        const int row = rr < n_act ? __ldg(p.active_idx + rr) : -1;
         s_rows[j] = (row >= 0 && row < p.n_rows) ? row : -1;
       }
       named_barrier(1, kEpiThreads);
@@ -333,21 +345,23 @@ LmHeadPlan plan_lm_head(int n_active, int H, int V, int num_sms) {
 }
 
 cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* active_idx, int n_active,
-                               int n_rows, int H, uint16_t* gathered, int* err,
-                               cudaStream_t stream) {
+                               const int32_t* n_active_dev, int n_rows, int H,
+                               uint16_t* gathered, int* err, cudaStream_t stream) {
   const int nv = H / 8;
   const int threads = nv < 256 ? ((nv + 31) / 32) * 32 : 256;
   dim3 grid((nv + threads - 1) / threads, n_active);
   return launch_pdl(gather_rows_kernel, grid, dim3(threads), 0, stream, hidden, active_idx,
-                    n_active, n_rows, H, gathered, err);
+                    n_active, n_active_dev, n_rows, H, gathered, err);
 }
 
 cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
-                           const int32_t* active_idx, int n_active, int n_rows, int H, int V,
+                           const int32_t* active_idx, int n_active,
+                           const int32_t* n_active_dev, int n_rows, int H, int V,
                            uint16_t* logits, const LmHeadPlan& plan, int* err,
                            cudaStream_t stream) {
   LmParams prm;
   prm.active_idx = active_idx;
+  prm.n_active_dev = n_active_dev;
   prm.logits = logits;
   prm.err = err;
   prm.n_active = n_active;

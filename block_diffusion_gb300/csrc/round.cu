@@ -1,0 +1,110 @@
+// Device-side pieces that let a whole denoising round run without the host: the list of
+// active rows computed from the mask on the device, and the write of a block's new K/V into
+// the paged cache.
+//
+// Source: JetEngine notes (CLAUDE.md), "ModelRunner" (selective logits: the LM head runs for
+// the rows still being denoised), "Important Patterns" (the block's K/V live in the paged
+// cache at the slots after the prefix; a finished block's K/V are written by a SAVING pass)
+// and "Optimization History" (opt18/opt24: the KV-cache write of the block combined with the
+// paged attention); dlmrt page, "Highlights" (a block's rounds run inside one CUDA graph).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bdlm {
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+// Row r = b * L + i is active when mask[r] != 0 and (no flags, or denoising[b] != 0).  The
+// active rows in increasing order go to active_idx and their number to *n_active.  One CTA:
+// a block-wide scan over chunks of kScanThreads rows.
+__global__ void __launch_bounds__(kScanThreads)
+active_rows_kernel(const uint8_t* __restrict__ mask, const uint8_t* __restrict__ denoising,
+                   int R, int L, int32_t* __restrict__ active_idx, int32_t* __restrict__ n_active) {
+  __shared__ int s_warp[kScanThreads / 32];
+  __shared__ int s_base;
+  griddep_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_base = 0;
+  __syncthreads();
+  for (int r0 = 0; r0 < R; r0 += kScanThreads) {
+    const int r = r0 + tid;
+    int a = 0;
+    if (r < R) a = mask[r] != 0 && (denoising == nullptr || denoising[r / L] != 0);
+    const unsigned bal = __ballot_sync(0xffffffffu, a);
+    if (lane == 0) s_warp[warp] = __popc(bal);
+    __syncthreads();
+    int before = s_base;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    if (a) active_idx[before + __popc(bal & ((1u << lane) - 1u))] = r;
+    __syncthreads();
+    if (tid == 0) {
+      int total = 0;
+      for (int w = 0; w < kScanThreads / 32; ++w) total += s_warp[w];
+      s_base += total;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) *n_active = s_base;
+  griddep_launch_dependents();
+}
+
+// k_new, v_new [B, L, Hkv, D=128] -> the cache slots prefix_len .. prefix_len + L - 1 of each
+// sequence.  One warp per (b, i, kvh) row of 128 bf16 (256 B, 8 B per lane).  Page ids and
+// lengths are checked; a bad one skips the row and sets the device error word.
+__global__ void write_block_kv_kernel(const uint16_t* __restrict__ k_new,
+                                      const uint16_t* __restrict__ v_new,
+                                      uint16_t* __restrict__ k_pages, uint16_t* __restrict__ v_pages,
+                                      const int32_t* __restrict__ page_table,
+                                      const int32_t* __restrict__ prefix_lens, int B, int L,
+                                      int Hkv, int max_pages, int num_pages, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(B) * L * Hkv;
+  if (row >= rows) return;
+  const int kvh = static_cast<int>(row % Hkv);
+  const long long bi = row / Hkv;
+  const int i = static_cast<int>(bi % L);
+  const int b = static_cast<int>(bi / L);
+  const int prefix = prefix_lens[b];
+  const long long tok = static_cast<long long>(prefix) + i;
+  if (prefix < 0 || static_cast<long long>(prefix) + L > static_cast<long long>(max_pages) * 16) {
+    if (lane == 0 && i == 0 && kvh == 0) atomicOr(err, BDLM_DEVERR_LENGTH);
+    return;
+  }
+  const int page = page_table[static_cast<size_t>(b) * max_pages + tok / 16];
+  if (page < 0 || page >= num_pages) {
+    if (lane == 0 && kvh == 0) atomicOr(err, BDLM_DEVERR_PAGE);
+    return;
+  }
+  const size_t src = static_cast<size_t>(row) * 128;
+  const size_t dst = ((static_cast<size_t>(page) * 16 + tok % 16) * Hkv + kvh) * 128;
+  reinterpret_cast<uint2*>(k_pages + dst)[lane] = reinterpret_cast<const uint2*>(k_new + src)[lane];
+  reinterpret_cast<uint2*>(v_pages + dst)[lane] = reinterpret_cast<const uint2*>(v_new + src)[lane];
+}
+
+}  // namespace
+
+cudaError_t launch_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,
+                               int32_t* active_idx, int32_t* n_active, cudaStream_t stream) {
+  return launch_pdl(active_rows_kernel, dim3(1), dim3(kScanThreads), 0, stream, mask, denoising,
+                    B * L, L, active_idx, n_active);
+}
+
+cudaError_t launch_write_block_kv(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages,
+                                  uint16_t* v_pages, const int32_t* page_table,
+                                  const int32_t* prefix_lens, int B, int L, int Hkv,
+                                  int max_pages, int num_pages, int* err, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(B) * L * Hkv;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  return launch_pdl(write_block_kv_kernel, dim3(grid), dim3(256), 0, stream, k_new, v_new,
+                    k_pages, v_pages, page_table, prefix_lens, B, L, Hkv, max_pages, num_pages,
+                    err);
+}
+
+}  // namespace bdlm

@@ -118,6 +118,46 @@ int bdlm_lm_head(const bdlm_bf16* hidden, const bdlm_bf16* w, const int32_t* act
                  int n_active, int n_rows, int H, int V, bdlm_bf16* logits, bdlm_stream stream);
 
 /*
+ * bdlm_lm_head with the active-row count in device memory, for rounds that run without the
+ * host (the count comes from bdlm_active_rows).  The launch is planned for max_active rows
+ * (0 < max_active <= n_rows); *n_active_dev (int32, device, read when the kernels run) is
+ * clamped to [0, max_active], and only that many leading entries of active_idx are used.
+ * Otherwise as bdlm_lm_head.
+ */
+int bdlm_lm_head_device_count(const bdlm_bf16* hidden, const bdlm_bf16* w,
+                              const int32_t* active_idx, const int32_t* n_active_dev,
+                              int max_active, int n_rows, int H, int V, bdlm_bf16* logits,
+                              bdlm_stream stream);
+
+/*
+ * The rows a step's LM head must compute, on the device.
+ * Source: JetEngine notes, "ModelRunner" (selective logits: DENOISING sequences only) and
+ * "Optimization History" (opt23: only the still-masked rows).
+ *
+ * Row r = b*L + i is active when mask[r] != 0 and (denoising is NULL or denoising[b] != 0).
+ * active_idx [B*L] int32 receives the active rows in increasing order; *n_active_dev (int32,
+ * device) their number.  mask [B, L] uint8; denoising [B] uint8 or NULL.  1 <= L <= 64.
+ */
+int bdlm_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,
+                     int32_t* active_idx, int32_t* n_active_dev, bdlm_stream stream);
+
+/*
+ * Writes a block's new K/V into the paged cache: k_new, v_new [B, L, Hkv, D] bf16 go to the
+ * slots prefix_lens[b] .. prefix_lens[b]+L-1 of sequence b (token j in page
+ * page_table[b][j / page_size], slot j % page_size), the slots bdlm_block_attention reads the
+ * block's own K/V from.  Used every step while the block is denoised and once more after it
+ * is fully committed (the SAVING pass).
+ * Source: JetEngine notes, "Important Patterns" and "Optimization History" (opt18/opt24: the
+ * KV-cache write of the block combined with the paged attention).
+ * desc as bdlm_block_attention (Hq and sm_scale unused); all pointers device, 16-byte aligned
+ * k_new/v_new/k_pages/v_pages.  A page id outside [0, num_pages) or a length that does not fit
+ * the page table skips the rows it concerns and sets a device error bit.
+ */
+int bdlm_write_block_kv(const bdlm_attn_desc* desc, const bdlm_bf16* k_new,
+                        const bdlm_bf16* v_new, bdlm_bf16* k_pages, bdlm_bf16* v_pages,
+                        const int32_t* page_table, const int32_t* prefix_lens, bdlm_stream stream);
+
+/*
  * Confidence and commit of one denoising step (threshold / low_confidence_dynamic rule).
  * Source: JetEngine notes, "Remasking Strategies" (low_confidence_dynamic: unmask above a
  * threshold); dInfer blog, "Algorithmic Innovations" (threshold decoding); SDAR page,

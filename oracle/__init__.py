@@ -202,3 +202,29 @@ def round_logits_to_bf16(x64: np.ndarray) -> np.ndarray:
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ~lo_even)
     out = np.where(pick_hi, hi, lo) >> 16
     return out.astype(np.uint16)
+
+
+def active_rows(mask, denoising=None) -> np.ndarray:
+    """Rows b*L+i with mask[b, i] != 0 and (no flags or denoising[b] != 0), increasing: the
+    rows a step's selective LM head computes (JetEngine notes, "ModelRunner")."""
+    mask = np.asarray(mask)
+    keep = mask != 0
+    if denoising is not None:
+        keep &= (np.asarray(denoising) != 0)[:, None]
+    return np.nonzero(keep.reshape(-1))[0].astype(np.int32)
+
+
+def write_block_kv(k_pages, v_pages, page_table, prefix_lens, k_new, v_new, P=16):
+    """Copies of the K/V pools with k_new/v_new [B, L, Hkv, D] written to the slots
+    prefix_lens[b] .. prefix_lens[b]+L-1 of sequence b (token j: page page_table[b][j // P],
+    slot j % P)."""
+    k = np.array(k_pages, copy=True)
+    v = np.array(v_pages, copy=True)
+    B, L = k_new.shape[:2]
+    for b in range(B):
+        for i in range(L):
+            j = int(prefix_lens[b]) + i
+            page = int(page_table[b][j // P])
+            k[page, j % P] = k_new[b, i]
+            v[page, j % P] = v_new[b, i]
+    return k, v

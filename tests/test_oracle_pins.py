@@ -333,3 +333,33 @@ def test_attention_oracle_rejects_pages_outside_the_pool():
     with pytest.raises(ValueError):
         oracle.attention_probs(a.q, a.k_ref, bad, a.prefix_lens, a.L, a.Hq, a.Hkv, a.D, a.P,
                                1, 0, 0)
+
+
+def test_active_rows_by_hand():
+    mask = np.array([[1, 0, 1, 0], [0, 0, 0, 0], [1, 1, 0, 1]], np.uint8)
+    assert oracle.active_rows(mask).tolist() == [0, 2, 8, 9, 11]
+    assert oracle.active_rows(mask, np.array([1, 1, 0], np.uint8)).tolist() == [0, 2]
+
+
+def test_written_block_kv_is_what_attention_reads():
+    """After the write, the block's keys are the new ones: with every new key equal to the
+    query (scaled large) and new values constant, the block's output is that constant."""
+    rng = np.random.default_rng(13)
+    a = make_attention(rng, 2, 4, 8, 8, 128, prefix_range=(30, 50), poison=False)
+    k_new = np.zeros((2, 4, 8, 128), np.uint16)
+    v_new = np.zeros((2, 4, 8, 128), np.uint16)
+    big = f32_to_bf16_bits(np.full((2, 4, 8, 128), 4.0, np.float32))
+    k_new[:] = big
+    v_new[:] = f32_to_bf16_bits(np.full((2, 4, 8, 128), 0.75, np.float32))
+    q = f32_to_bf16_bits(np.full(a.q.shape, 4.0, np.float32))
+    k, v = oracle.write_block_kv(a.k_ref, a.v_ref, a.page_table_ref, a.prefix_lens, k_new, v_new)
+    out = oracle.block_attention(q, k, v, a.page_table_ref, a.prefix_lens, a.L, a.Hq, a.Hkv, a.D,
+                                 a.P)
+    # block keys score 4*4*128/sqrt(128) ~ 181 above the prefix keys (N(0, 0.5^2) entries)
+    assert np.allclose(out, 0.75, atol=1e-6)
+    untouched = np.ones(a.k_ref.shape[0], bool)
+    for b in range(2):
+        for i in range(4):
+            j = int(a.prefix_lens[b]) + i
+            untouched[a.page_table_ref[b][j // 16]] = False
+    assert np.array_equal(k[untouched], a.k_ref[untouched])
