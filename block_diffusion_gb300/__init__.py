@@ -34,7 +34,8 @@ BDLM_COMMIT_ANTI_SEQUENTIAL = 3
 
 EXPORTS = ("bdlm_block_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
            "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
-           "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_status_string",
+           "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_round_loop_create",
+           "bdlm_round_loop_launch", "bdlm_round_loop_destroy", "bdlm_status_string",
            "bdlm_device_error", "bdlm_release")
 
 
@@ -44,6 +45,18 @@ class AttnDesc(ctypes.Structure):
                 ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("page_size", ctypes.c_int),
                 ("max_pages_per_seq", ctypes.c_int), ("num_pages", ctypes.c_int),
                 ("sm_scale", ctypes.c_float)]
+
+
+class RoundLoopDesc(ctypes.Structure):
+    """bdlm_round_loop_desc (device pointers as integers)."""
+    _P = ctypes.c_void_p
+    _fields_ = [("attn", AttnDesc), ("steps", ctypes.c_int), ("H", ctypes.c_int),
+                ("V", ctypes.c_int), ("rule", ctypes.c_int), ("k", ctypes.c_int),
+                ("threshold", ctypes.c_float), ("temperature", ctypes.c_float),
+                ("q_steps", _P), ("k_new_steps", _P), ("v_new_steps", _P), ("hidden_steps", _P),
+                ("k_pages", _P), ("v_pages", _P), ("page_table", _P), ("prefix_lens", _P),
+                ("w", _P), ("mask", _P), ("denoising", _P), ("tok_steps", _P),
+                ("conf_steps", _P), ("commit_steps", _P), ("steps_done", _P)]
 
 
 class BdlmError(RuntimeError):
@@ -78,6 +91,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bdlm_active_rows.restype = I
     lib.bdlm_write_block_kv.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P]
     lib.bdlm_write_block_kv.restype = I
+    lib.bdlm_round_loop_create.argtypes = [ctypes.POINTER(RoundLoopDesc),
+                                           ctypes.POINTER(ctypes.c_void_p)]
+    lib.bdlm_round_loop_create.restype = I
+    lib.bdlm_round_loop_launch.argtypes = [P, P]
+    lib.bdlm_round_loop_launch.restype = I
+    lib.bdlm_round_loop_destroy.argtypes = [P]
+    lib.bdlm_round_loop_destroy.restype = I
     lib.bdlm_apply_commit.argtypes = [P, P, I, P]
     lib.bdlm_apply_commit.restype = I
     lib.bdlm_status_string.argtypes = [I]
@@ -181,6 +201,34 @@ def bdlm_write_block_kv(desc: AttnDesc, k_new, v_new, k_pages, v_pages, page_tab
                                  _ptr(v_pages), _ptr(page_table), _ptr(prefix_lens),
                                  _stream(stream))
     _check("bdlm_write_block_kv", rc)
+
+
+def round_loop_desc(attn: AttnDesc, steps: int, H: int, V: int, rule: int, k: int,
+                    threshold: float, temperature: float, **ptrs) -> RoundLoopDesc:
+    """A bdlm_round_loop_desc; ptrs are tensors (or None) for the pointer fields."""
+    d = RoundLoopDesc()
+    d.attn = attn
+    d.steps, d.H, d.V, d.rule, d.k = int(steps), int(H), int(V), int(rule), int(k)
+    d.threshold, d.temperature = float(threshold), float(temperature)
+    for name, t in ptrs.items():
+        setattr(d, name, _ptr(t))
+    return d
+
+
+def bdlm_round_loop_create(desc: RoundLoopDesc) -> int:
+    lib = load_library()
+    out = ctypes.c_void_p()
+    rc = lib.bdlm_round_loop_create(ctypes.byref(desc), ctypes.byref(out))
+    _check("bdlm_round_loop_create", rc)
+    return out.value
+
+
+def bdlm_round_loop_launch(loop: int, stream=None) -> None:
+    _check("bdlm_round_loop_launch", load_library().bdlm_round_loop_launch(loop, _stream(stream)))
+
+
+def bdlm_round_loop_destroy(loop: int) -> None:
+    _check("bdlm_round_loop_destroy", load_library().bdlm_round_loop_destroy(loop))
 
 
 def bdlm_apply_commit(mask, commit, n: int, stream=None) -> None:

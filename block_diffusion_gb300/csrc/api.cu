@@ -31,6 +31,9 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+// Bumped whenever a workspace is reallocated or freed: CUDA graphs that captured the old
+// buffers are re-captured before their next launch.
+unsigned g_workspace_gen = 0;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -66,6 +69,7 @@ int current_device(DeviceState** st) {
 int ensure(void** ptr, size_t* cap, size_t need, bool zero) {
   if (need <= *cap) return BDLM_OK;
   size_t n = need + need / 4 + 4096;
+  ++g_workspace_gen;
   if (*ptr) {
     if (cudaDeviceSynchronize() != cudaSuccess) return BDLM_ERR_CUDA;
     cudaFree(*ptr);
@@ -142,6 +146,7 @@ int bdlm_release(void) {
   int rc = current_device(&st);
   if (rc) return rc;
   if (cudaDeviceSynchronize() != cudaSuccess) return BDLM_ERR_CUDA;
+  ++g_workspace_gen;
   cudaFree(st->attn_cnt);
   cudaFree(st->data);
   st->attn_cnt = nullptr;
@@ -354,6 +359,224 @@ int bdlm_write_block_kv(const bdlm_attn_desc* desc, const bdlm_bf16* k_new,
                                               d.num_pages, st->err,
                                               static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ device-side round loop
+struct bdlm_round_loop {
+  bdlm_round_loop_desc d;
+  int device = 0;
+  void* scratch = nullptr;
+  bdlm_bf16 *q_w = nullptr, *k_w = nullptr, *v_w = nullptr, *h_w = nullptr;
+  bdlm_bf16 *attn_out = nullptr, *logits = nullptr;
+  int32_t *act = nullptr, *n_act = nullptr, *tok = nullptr;
+  float* conf = nullptr;
+  uint8_t* com = nullptr;
+  int* step = nullptr;
+  cudaStream_t cap = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  unsigned gen = 0;
+};
+
+namespace {
+
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Sizes the library workspaces for one round of the loop (nothing may be allocated while the
+// round is being captured).
+int reserve_round(const bdlm_round_loop_desc& d) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  const bdlm_attn_desc& a = d.attn;
+  const AttnPlan ap = bdlm::plan_attention(a.B, a.L, a.Hq, a.Hkv, a.max_pages_per_seq,
+                                           a.page_size, st->num_sms);
+  if (ap.n_mma == 0) return BDLM_ERR_UNSUPPORTED;
+  const CommitPlan cp = bdlm::plan_commit(a.B, a.L, d.V, st->num_sms);
+  const LmHeadPlan lp = bdlm::plan_lm_head(a.B * a.L, d.H, d.V, st->num_sms);
+  size_t data = ap.part_bytes;
+  if (cp.part_bytes > data) data = cp.part_bytes;
+  if (lp.gather_bytes > data) data = lp.gather_bytes;
+  if ((rc = ensure(reinterpret_cast<void**>(&st->attn_cnt), &st->attn_cnt_cap, ap.cnt_bytes,
+                   true)))
+    return rc;
+  if ((rc = ensure(&st->data, &st->data_cap, data, false))) return rc;
+  return get_encoder();
+}
+
+void drop_graph(bdlm_round_loop* lp) {
+  if (lp->exec) cudaGraphExecDestroy(lp->exec);
+  if (lp->graph) cudaGraphDestroy(lp->graph);
+  lp->exec = nullptr;
+  lp->graph = nullptr;
+}
+
+// Builds the graph: step counter := 0, then WHILE(condition) { one round }.
+int capture_round_loop(bdlm_round_loop* lp) {
+  const bdlm_round_loop_desc& d = lp->d;
+  const bdlm_attn_desc& a = d.attn;
+  const int R = a.B * a.L;
+  int rc = reserve_round(d);
+  if (rc) return rc;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    lp->gen = g_workspace_gen;
+  }
+  drop_graph(lp);
+  if (cudaGraphCreate(&lp->graph, 0) != cudaSuccess) return BDLM_ERR_CUDA;
+  cudaMemsetParams ms = {};
+  ms.dst = lp->step;
+  ms.value = 0;
+  ms.elementSize = 4;
+  ms.width = 1;
+  ms.height = 1;
+  cudaGraphNode_t init;
+  if (cudaGraphAddMemsetNode(&init, lp->graph, nullptr, 0, &ms) != cudaSuccess) return BDLM_ERR_CUDA;
+  cudaGraphConditionalHandle handle;
+  if (cudaGraphConditionalHandleCreate(&handle, lp->graph, 1, cudaGraphCondAssignDefault) !=
+      cudaSuccess)
+    return BDLM_ERR_CUDA;
+  cudaGraphNodeParams np = {};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = handle;
+  np.conditional.type = cudaGraphCondTypeWhile;
+  np.conditional.size = 1;
+  cudaGraphNode_t loop;
+  if (cudaGraphAddNode(&loop, lp->graph, &init, nullptr, 1, &np) != cudaSuccess) return BDLM_ERR_CUDA;
+  cudaGraph_t body = np.conditional.phGraph_out[0];
+  if (cudaStreamBeginCaptureToGraph(lp->cap, body, nullptr, nullptr, 0,
+                                    cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    return BDLM_ERR_CUDA;
+  bdlm_stream s = lp->cap;
+  bdlm::StepCopy c = {};
+  c.src[0] = reinterpret_cast<const uint4*>(d.q_steps);
+  c.dst[0] = reinterpret_cast<uint4*>(lp->q_w);
+  c.n_vec[0] = static_cast<long long>(R) * a.Hq * a.D * 2 / 16;
+  c.src[1] = reinterpret_cast<const uint4*>(d.k_new_steps);
+  c.dst[1] = reinterpret_cast<uint4*>(lp->k_w);
+  c.n_vec[1] = static_cast<long long>(R) * a.Hkv * a.D * 2 / 16;
+  c.src[2] = reinterpret_cast<const uint4*>(d.v_new_steps);
+  c.dst[2] = reinterpret_cast<uint4*>(lp->v_w);
+  c.n_vec[2] = c.n_vec[1];
+  c.src[3] = reinterpret_cast<const uint4*>(d.hidden_steps);
+  c.dst[3] = reinterpret_cast<uint4*>(lp->h_w);
+  c.n_vec[3] = static_cast<long long>(R) * d.H * 2 / 16;
+  int r2 = BDLM_OK;
+  if (bdlm::launch_select_step(c, lp->step, d.steps, lp->cap) != cudaSuccess) r2 = BDLM_ERR_CUDA;
+  if (!r2) r2 = bdlm_write_block_kv(&a, lp->k_w, lp->v_w, d.k_pages, d.v_pages, d.page_table,
+                                    d.prefix_lens, s);
+  if (!r2) r2 = bdlm_block_attention(&a, lp->q_w, d.k_pages, d.v_pages, d.page_table,
+                                     d.prefix_lens, a.L, lp->attn_out, s);
+  if (!r2) r2 = bdlm_active_rows(d.mask, d.denoising, a.B, a.L, lp->act, lp->n_act, s);
+  if (!r2) r2 = bdlm_lm_head_device_count(lp->h_w, d.w, lp->act, lp->n_act, R, R, d.H, d.V,
+                                          lp->logits, s);
+  if (!r2) r2 = bdlm_confidence_commit_rule(lp->logits, d.mask, a.B, a.L, d.V, d.rule, d.k,
+                                            d.threshold, d.temperature, lp->tok, lp->conf,
+                                            lp->com, s);
+  if (!r2 && bdlm::launch_record_step(lp->step, d.steps, R, lp->tok, lp->conf, lp->com,
+                                      d.tok_steps, d.conf_steps, d.commit_steps,
+                                      lp->cap) != cudaSuccess)
+    r2 = BDLM_ERR_CUDA;
+  if (!r2) r2 = bdlm_apply_commit(d.mask, lp->com, R, s);
+  if (!r2 && bdlm::launch_loop_condition(handle, d.mask, R, lp->step, d.steps, d.steps_done,
+                                         lp->cap) != cudaSuccess)
+    r2 = BDLM_ERR_CUDA;
+  cudaGraph_t captured = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(lp->cap, &captured);
+  if (r2) return r2;
+  if (ec != cudaSuccess) return BDLM_ERR_CUDA;
+  if (cudaGraphInstantiate(&lp->exec, lp->graph, 0) != cudaSuccess) return BDLM_ERR_CUDA;
+  return BDLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bdlm_round_loop_create(const bdlm_round_loop_desc* desc, bdlm_round_loop** out) {
+  if (!desc || !out) return BDLM_ERR_INVALID;
+  *out = nullptr;
+  const bdlm_round_loop_desc& d = *desc;
+  const bdlm_attn_desc& a = d.attn;
+  if (a.B < 1 || a.L < 1 || a.L > 64 || a.Hq < 1 || a.Hkv < 1 || a.Hq % a.Hkv != 0 ||
+      a.D != 128 || a.page_size != 16 || a.max_pages_per_seq < 1 || a.num_pages < 1)
+    return BDLM_ERR_INVALID;
+  if (d.steps < 1 || d.H < 8 || d.H % 8 != 0 || d.V < 8 || d.V % 8 != 0) return BDLM_ERR_INVALID;
+  if (d.rule < BDLM_COMMIT_THRESHOLD || d.rule > BDLM_COMMIT_ANTI_SEQUENTIAL) return BDLM_ERR_INVALID;
+  if (d.rule != BDLM_COMMIT_THRESHOLD && d.k < 1) return BDLM_ERR_INVALID;
+  if (!(d.temperature > 0.f) || !(d.threshold >= 0.f && d.threshold <= 1.f)) return BDLM_ERR_INVALID;
+  if (!d.q_steps || !d.k_new_steps || !d.v_new_steps || !d.hidden_steps || !d.k_pages ||
+      !d.v_pages || !d.page_table || !d.prefix_lens || !d.w || !d.mask || !d.tok_steps ||
+      !d.conf_steps || !d.commit_steps || !d.steps_done)
+    return BDLM_ERR_INVALID;
+  const long long R = static_cast<long long>(a.B) * a.L;
+  if (R * a.Hq > 0x7FFFFFFFll || R * d.V > (1ll << 40)) return BDLM_ERR_INVALID;
+  auto* lp = new bdlm_round_loop();
+  lp->d = d;
+  cudaGetDevice(&lp->device);
+  // owned scratch: one step's inputs, the attention output, the logits, the active rows,
+  // this step's tok/conf/commit and the step counter
+  const size_t q_b = align256(R * a.Hq * a.D * 2), kv_b = align256(R * a.Hkv * a.D * 2);
+  const size_t h_b = align256(R * d.H * 2), lg_b = align256(R * d.V * 2);
+  const size_t r4 = align256(R * 4), r1 = align256(R);
+  const size_t total = 2 * q_b + 2 * kv_b + h_b + lg_b + 3 * r4 + r1 + 2 * 256;
+  if (cudaMalloc(&lp->scratch, total) != cudaSuccess) {
+    delete lp;
+    return BDLM_ERR_NOMEM;
+  }
+  uint8_t* p = static_cast<uint8_t*>(lp->scratch);
+  lp->q_w = reinterpret_cast<bdlm_bf16*>(p);      p += q_b;
+  lp->attn_out = reinterpret_cast<bdlm_bf16*>(p); p += q_b;
+  lp->k_w = reinterpret_cast<bdlm_bf16*>(p);      p += kv_b;
+  lp->v_w = reinterpret_cast<bdlm_bf16*>(p);      p += kv_b;
+  lp->h_w = reinterpret_cast<bdlm_bf16*>(p);      p += h_b;
+  lp->logits = reinterpret_cast<bdlm_bf16*>(p);   p += lg_b;
+  lp->act = reinterpret_cast<int32_t*>(p);        p += r4;
+  lp->tok = reinterpret_cast<int32_t*>(p);        p += r4;
+  lp->conf = reinterpret_cast<float*>(p);         p += r4;
+  lp->com = p;                                    p += r1;
+  lp->n_act = reinterpret_cast<int32_t*>(p);      p += 256;
+  lp->step = reinterpret_cast<int*>(p);
+  if (cudaStreamCreateWithFlags(&lp->cap, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaFree(lp->scratch);
+    delete lp;
+    return BDLM_ERR_CUDA;
+  }
+  const int rc = capture_round_loop(lp);
+  if (rc) {
+    bdlm_round_loop_destroy(lp);
+    return rc;
+  }
+  *out = lp;
+  return BDLM_OK;
+}
+
+int bdlm_round_loop_launch(bdlm_round_loop* loop, bdlm_stream stream) {
+  if (!loop) return BDLM_ERR_INVALID;
+  unsigned gen = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    gen = g_workspace_gen;
+  }
+  if (gen != loop->gen || !loop->exec) {
+    const int rc = capture_round_loop(loop);  // a workspace moved since the capture
+    if (rc) return rc;
+  }
+  return cudaGraphLaunch(loop->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BDLM_OK
+             : BDLM_ERR_CUDA;
+}
+
+int bdlm_round_loop_destroy(bdlm_round_loop* loop) {
+  if (!loop) return BDLM_OK;
+  drop_graph(loop);
+  if (loop->cap) cudaStreamDestroy(loop->cap);
+  if (loop->scratch) cudaFree(loop->scratch);
+  delete loop;
+  return BDLM_OK;
 }
 
 }  // extern "C"

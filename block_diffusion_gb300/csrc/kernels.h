@@ -102,6 +102,19 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            cudaStream_t stream);
 
 // Device-side round pieces (round.cu).
+struct StepCopy {  // per-step inputs: slice s of src[j] (n_vec[j] 16-byte vectors) -> dst[j]
+  static constexpr int kMax = 4;
+  const uint4* src[kMax];
+  uint4* dst[kMax];
+  long long n_vec[kMax];
+};
+cudaError_t launch_select_step(const StepCopy& c, const int* step, int n_steps,
+                               cudaStream_t stream);
+cudaError_t launch_record_step(const int* step, int n_steps, int R, const int32_t* tok,
+                               const float* conf, const uint8_t* commit, int32_t* tok_s,
+                               float* conf_s, uint8_t* commit_s, cudaStream_t stream);
+cudaError_t launch_loop_condition(cudaGraphConditionalHandle handle, const uint8_t* mask, int R,
+                                  int* step, int n_steps, int* steps_done, cudaStream_t stream);
 cudaError_t launch_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,
                                int32_t* active_idx, int32_t* n_active, cudaStream_t stream);
 cudaError_t launch_write_block_kv(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages,

@@ -88,7 +88,82 @@ __global__ void write_block_kv_kernel(const uint16_t* __restrict__ k_new,
   reinterpret_cast<uint2*>(v_pages + dst)[lane] = reinterpret_cast<const uint2*>(v_new + src)[lane];
 }
 
+// Copies step *step's slice of up to four per-step inputs into their working buffers.
+__global__ void select_step_kernel(StepCopy c, const int* __restrict__ step, int n_steps) {
+  griddep_wait();
+  griddep_launch_dependents();
+  long long s = *step;
+  if (s < 0) s = 0;
+  if (s >= n_steps) s = n_steps - 1;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+#pragma unroll
+  for (int j = 0; j < StepCopy::kMax; ++j) {
+    if (c.dst[j] == nullptr) continue;
+    const uint4* src = c.src[j] + s * c.n_vec[j];
+    for (long long v = tid; v < c.n_vec[j]; v += stride) c.dst[j][v] = src[v];
+  }
+}
+
+// Stores this step's tok/conf/commit into slice *step of the per-step outputs.
+__global__ void record_step_kernel(const int* __restrict__ step, int n_steps, int R,
+                                   const int32_t* __restrict__ tok, const float* __restrict__ conf,
+                                   const uint8_t* __restrict__ commit, int32_t* __restrict__ tok_s,
+                                   float* __restrict__ conf_s, uint8_t* __restrict__ commit_s) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int s = *step;
+  if (s < 0 || s >= n_steps) return;
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < R; r += gridDim.x * blockDim.x) {
+    const size_t o = static_cast<size_t>(s) * R + r;
+    tok_s[o] = tok[r];
+    conf_s[o] = conf[r];
+    commit_s[o] = commit[r];
+  }
+}
+
+// End of a round: counts it, and repeats the loop while some position is still masked and
+// fewer than n_steps rounds have run.  One CTA.
+__global__ void __launch_bounds__(kScanThreads)
+loop_condition_kernel(cudaGraphConditionalHandle handle, const uint8_t* __restrict__ mask, int R,
+                      int* __restrict__ step, int n_steps, int* __restrict__ steps_done) {
+  griddep_wait();
+  int any = 0;
+  for (int r = threadIdx.x; r < R && !any; r += blockDim.x) any = mask[r] != 0;
+  any = __syncthreads_or(any);
+  if (threadIdx.x == 0) {
+    const int s = *step + 1;
+    *step = s;
+    *steps_done = s;
+    cudaGraphSetConditional(handle, (any && s < n_steps) ? 1u : 0u);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_select_step(const StepCopy& c, const int* step, int n_steps,
+                               cudaStream_t stream) {
+  long long most = 0;
+  for (int j = 0; j < StepCopy::kMax; ++j)
+    if (c.dst[j] && c.n_vec[j] > most) most = c.n_vec[j];
+  const long long blocks = (most + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(blocks < 1 ? 1 : (blocks > 1216 ? 1216 : blocks));
+  return launch_pdl(select_step_kernel, dim3(grid), dim3(256), 0, stream, c, step, n_steps);
+}
+
+cudaError_t launch_record_step(const int* step, int n_steps, int R, const int32_t* tok,
+                               const float* conf, const uint8_t* commit, int32_t* tok_s,
+                               float* conf_s, uint8_t* commit_s, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((R + 255) / 256);
+  return launch_pdl(record_step_kernel, dim3(grid), dim3(256), 0, stream, step, n_steps, R, tok,
+                    conf, commit, tok_s, conf_s, commit_s);
+}
+
+cudaError_t launch_loop_condition(cudaGraphConditionalHandle handle, const uint8_t* mask, int R,
+                                  int* step, int n_steps, int* steps_done, cudaStream_t stream) {
+  return launch_pdl(loop_condition_kernel, dim3(1), dim3(kScanThreads), 0, stream, handle, mask,
+                    R, step, n_steps, steps_done);
+}
 
 cudaError_t launch_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,
                                int32_t* active_idx, int32_t* n_active, cudaStream_t stream) {

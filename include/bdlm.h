@@ -237,6 +237,62 @@ int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uint8_t* mask,
  */
 int bdlm_apply_commit(uint8_t* mask, const uint8_t* commit, int n, bdlm_stream stream);
 
+/*
+ * A whole block's denoising on the device: rounds repeat inside one CUDA graph, with a
+ * conditional WHILE node, until no position of any block is masked or `steps` rounds have
+ * run; the host only launches the graph.
+ * Source: dlmrt page, "Highlights" (a block = one CUDA graph with WHILE(not done){round});
+ * JetEngine notes, "Important Patterns" (denoising steps until the block is committed).
+ *
+ * One round (step s, counted on the device):
+ *   the step's inputs: slice s of q_steps [S, B, L, Hq, D], k_new_steps / v_new_steps
+ *   [S, B, L, Hkv, D] and hidden_steps [S, B*L, H] (the model's outputs for that step, which
+ *   this library does not compute) -> bdlm_write_block_kv (the block's K/V into the cache)
+ *   -> bdlm_block_attention -> bdlm_active_rows (mask, denoising) ->
+ *   bdlm_lm_head_device_count -> bdlm_confidence_commit_rule (rule, k, threshold,
+ *   temperature) -> tok/conf/commit stored into slice s of tok_steps, conf_steps,
+ *   commit_steps [S, B, L] -> bdlm_apply_commit on mask.
+ * After the last round *steps_done holds the number of rounds run, and slices at or past it
+ * are untouched.  The attention output is kept in the loop's own scratch (a model would feed
+ * it to its next layer).
+ *
+ * All pointers are device pointers owned by the caller and must stay valid while the loop
+ * exists.  bdlm_round_loop_create allocates the loop's scratch (one step's inputs, the
+ * attention output, the [B*L, V] logits, small per-row arrays) and captures the graph; it sizes
+ * the library workspace first, since nothing may be allocated inside the capture.  If a later
+ * call grows or releases the library workspace, the next launch captures the graph again.
+ * Shapes and limits as the calls it is made of.
+ */
+typedef struct bdlm_round_loop bdlm_round_loop;
+typedef struct {
+  bdlm_attn_desc attn;        /* B, L, Hq, Hkv, D, page_size, max_pages_per_seq, num_pages */
+  int steps;                  /* S: rounds at most, and slices of the per-step arrays */
+  int H, V;                   /* LM head */
+  int rule, k;                /* BDLM_COMMIT_* and positions per block (see _rule) */
+  float threshold, temperature;
+  const bdlm_bf16* q_steps;
+  const bdlm_bf16* k_new_steps;
+  const bdlm_bf16* v_new_steps;
+  const bdlm_bf16* hidden_steps;
+  bdlm_bf16* k_pages;
+  bdlm_bf16* v_pages;
+  const int32_t* page_table;
+  const int32_t* prefix_lens;
+  const bdlm_bf16* w;         /* [V, H] */
+  uint8_t* mask;              /* [B, L], updated in place */
+  const uint8_t* denoising;   /* [B] or NULL */
+  int32_t* tok_steps;
+  float* conf_steps;
+  uint8_t* commit_steps;
+  int32_t* steps_done;        /* one int32 */
+} bdlm_round_loop_desc;
+
+int bdlm_round_loop_create(const bdlm_round_loop_desc* desc, bdlm_round_loop** loop_out);
+/* Enqueues the whole loop on `stream` (asynchronous; one graph launch). */
+int bdlm_round_loop_launch(bdlm_round_loop* loop, bdlm_stream stream);
+/* Frees the loop (the device must be done with it). */
+int bdlm_round_loop_destroy(bdlm_round_loop* loop);
+
 /* Human-readable name of a BDLM_* status code (a static string). */
 const char* bdlm_status_string(int status);
 
