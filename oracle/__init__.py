@@ -228,3 +228,21 @@ def write_block_kv(k_pages, v_pages, page_table, prefix_lens, k_new, v_new, P=16
             k[page, j % P] = k_new[b, i]
             v[page, j % P] = v_new[b, i]
     return k, v
+
+
+def prefill_attention(q, k_new, v_new, k_pages, v_pages, page_table, prefix_lens, L, Hq, Hkv, D,
+                      P=16, sm_scale=None):
+    """Block prefill: the prompt's K/V written after each sequence's cached prefix, then every
+    prompt block j attends to the cache up to the end of block j (prefix + (j+1)*L tokens).
+    q [B, n, Hq, D], k_new/v_new [B, n, Hkv, D] with n a multiple of L.  Returns the fp64
+    output [B, n, Hq, D] and the updated pools."""
+    q = np.asarray(q)
+    B, n = q.shape[:2]
+    k, v = write_block_kv(k_pages, v_pages, page_table, prefix_lens, k_new, v_new, P)
+    out = np.empty((B, n, Hq, D), dtype=np.float64)
+    for j in range(n // L):
+        pre = np.asarray(prefix_lens, dtype=np.int32) + j * L
+        qj = np.ascontiguousarray(q[:, j * L:(j + 1) * L])
+        out[:, j * L:(j + 1) * L] = block_attention(qj, k, v, page_table, pre, L, Hq, Hkv, D, P,
+                                                    sm_scale=sm_scale)
+    return out, k, v

@@ -363,3 +363,21 @@ def test_written_block_kv_is_what_attention_reads():
             j = int(a.prefix_lens[b]) + i
             untouched[a.page_table_ref[b][j // 16]] = False
     assert np.array_equal(k[untouched], a.k_ref[untouched])
+
+
+def test_prefill_oracle_against_dense_block_causal_attention():
+    """A fresh prompt of three blocks: the block-by-block paged prefill equals dense attention
+    with the block-causal mask over the whole prompt."""
+    rng = np.random.default_rng(17)
+    B, L, Hq, Hkv, D, n = 2, 4, 8, 4, 128, 12
+    a = make_attention(rng, B, n - L, Hq, Hkv, D, prefix_lens=np.zeros(B, np.int64),
+                       poison=False)   # pages for n tokens per sequence (n - L + L)
+    q = f32_to_bf16_bits(rng.normal(0, 0.5, (B, n, Hq, D)).astype(np.float32))
+    kn = f32_to_bf16_bits(rng.normal(0, 0.5, (B, n, Hkv, D)).astype(np.float32))
+    vn = f32_to_bf16_bits(rng.normal(0, 0.5, (B, n, Hkv, D)).astype(np.float32))
+    out, _, _ = oracle.prefill_attention(q, kn, vn, a.k_ref, a.v_ref, a.page_table_ref,
+                                         np.zeros(B, np.int32), L, Hq, Hkv, D)
+    for b in range(B):
+        ref = brute.dense_block_causal_attention(bf16_bits_to_f32(q[b]), bf16_bits_to_f32(kn[b]),
+                                                 bf16_bits_to_f32(vn[b]), L, Hq, Hkv)
+        assert np.allclose(out[b], ref, rtol=1e-12, atol=1e-12)
