@@ -32,7 +32,7 @@ BDLM_COMMIT_TOPK = 1
 BDLM_COMMIT_SEQUENTIAL = 2
 BDLM_COMMIT_ANTI_SEQUENTIAL = 3
 
-EXPORTS = ("bdlm_block_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
+EXPORTS = ("bdlm_block_attention", "bdlm_prefill_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
            "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
            "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_round_loop_create",
            "bdlm_round_loop_launch", "bdlm_round_loop_destroy", "bdlm_status_string",
@@ -91,6 +91,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bdlm_active_rows.restype = I
     lib.bdlm_write_block_kv.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P]
     lib.bdlm_write_block_kv.restype = I
+    lib.bdlm_prefill_attention.argtypes = [ctypes.POINTER(AttnDesc), I, P, P, P, P, P, P, P, P,
+                                           P]
+    lib.bdlm_prefill_attention.restype = I
     lib.bdlm_round_loop_create.argtypes = [ctypes.POINTER(RoundLoopDesc),
                                            ctypes.POINTER(ctypes.c_void_p)]
     lib.bdlm_round_loop_create.restype = I
@@ -147,6 +150,15 @@ def bdlm_block_attention(desc: AttnDesc, q, k_pages, v_pages, page_table, prefix
                                   _ptr(page_table), _ptr(prefix_lens), int(L), _ptr(out),
                                   _stream(stream))
     _check("bdlm_block_attention", rc)
+
+
+def bdlm_prefill_attention(desc: AttnDesc, prompt_len: int, q, k_new, v_new, k_pages, v_pages,
+                           page_table, prefix_lens, out, stream=None) -> None:
+    lib = load_library()
+    rc = lib.bdlm_prefill_attention(ctypes.byref(desc), int(prompt_len), _ptr(q), _ptr(k_new),
+                                    _ptr(v_new), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                    _ptr(prefix_lens), _ptr(out), _stream(stream))
+    _check("bdlm_prefill_attention", rc)
 
 
 def bdlm_lm_head(hidden, w, active_idx, n_active: int, n_rows: int, H: int, V: int, logits,

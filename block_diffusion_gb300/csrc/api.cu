@@ -27,6 +27,8 @@ struct DeviceState {
   size_t attn_cnt_cap = 0;
   void* data = nullptr;          // partial results / gathered rows
   size_t data_cap = 0;
+  void* aux = nullptr;           // prompt-block prefix lengths of a prefill
+  size_t aux_cap = 0;
 };
 
 std::mutex g_mu;
@@ -110,6 +112,11 @@ int encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
+                   const bdlm_bf16* k_pages, const bdlm_bf16* v_pages, const int32_t* page_table,
+                   const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream,
+                   int table_div);
+
 }  // namespace
 
 extern "C" {
@@ -149,9 +156,11 @@ int bdlm_release(void) {
   ++g_workspace_gen;
   cudaFree(st->attn_cnt);
   cudaFree(st->data);
+  cudaFree(st->aux);
   st->attn_cnt = nullptr;
   st->data = nullptr;
-  st->attn_cnt_cap = st->data_cap = 0;
+  st->aux = nullptr;
+  st->attn_cnt_cap = st->data_cap = st->aux_cap = 0;
   return BDLM_OK;
 }
 
@@ -220,7 +229,62 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
   DeviceState* st = nullptr;
   int rc = current_device(&st);
   if (rc) return rc;
-  if ((rc = get_encoder())) return rc;
+  return attention_impl(st, d, q, k_pages, v_pages, page_table, prefix_lens, out, stream, 1);
+}
+
+int bdlm_prefill_attention(const bdlm_attn_desc* desc, int prompt_len, const bdlm_bf16* q,
+                           const bdlm_bf16* k_new, const bdlm_bf16* v_new, bdlm_bf16* k_pages,
+                           bdlm_bf16* v_pages, const int32_t* page_table,
+                           const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream) {
+  if (!desc) return BDLM_ERR_INVALID;
+  const bdlm_attn_desc d = *desc;
+  if (d.B < 0 || d.L < 1 || d.L > 64 || d.Hq < 1 || d.Hkv < 1 || d.Hq % d.Hkv != 0 ||
+      d.Hq / d.Hkv > 16 || d.D != 128 || d.page_size != 16 || d.max_pages_per_seq < 1 ||
+      d.num_pages < 1 || !isfinite(d.sm_scale))
+    return BDLM_ERR_INVALID;
+  if (prompt_len < 1 || prompt_len % d.L != 0) return BDLM_ERR_INVALID;
+  if (d.B == 0) return BDLM_OK;
+  if (!q || !k_new || !v_new || !k_pages || !v_pages || !page_table || !prefix_lens || !out)
+    return BDLM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) ||
+      !aligned16(v_pages) || !aligned16(out))
+    return BDLM_ERR_INVALID;
+  const int nb = prompt_len / d.L;
+  if (static_cast<long long>(d.B) * prompt_len * d.Hq > 0x7FFFFFFFll ||
+      static_cast<long long>(d.B) * d.max_pages_per_seq > 0x7FFFFFFFll ||
+      static_cast<long long>(d.max_pages_per_seq) * d.page_size > 0x7FFFFFFFll)
+    return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  rc = ensure(&st->aux, &st->aux_cap, static_cast<size_t>(d.B) * nb * sizeof(int32_t), false);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the prompt's K/V into the cache, then one attention sequence per prompt block
+  if (bdlm::launch_write_block_kv(k_new, v_new, k_pages, v_pages, page_table, prefix_lens, d.B,
+                                  prompt_len, d.Hkv, d.max_pages_per_seq, d.num_pages, st->err,
+                                  s) != cudaSuccess)
+    return BDLM_ERR_CUDA;
+  int32_t* pre = static_cast<int32_t*>(st->aux);
+  if (bdlm::launch_prompt_prefix(prefix_lens, d.B, nb, d.L, pre, s) != cudaSuccess)
+    return BDLM_ERR_CUDA;
+  bdlm_attn_desc dv = d;
+  dv.B = d.B * nb;
+  return attention_impl(st, dv, q, k_pages, v_pages, page_table, pre, out, stream, nb);
+}
+}  // extern "C"
+
+namespace {
+
+// Block attention of d.B sequences (the caller holds g_mu and has validated d); sequence b
+// uses page-table row b / table_div.
+int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
+                   const bdlm_bf16* k_pages, const bdlm_bf16* v_pages, const int32_t* page_table,
+                   const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream,
+                   int table_div) {
+  int rc = get_encoder();
+  if (rc) return rc;
   const AttnPlan plan = bdlm::plan_attention(d.B, d.L, d.Hq, d.Hkv, d.max_pages_per_seq,
                                              d.page_size, st->num_sms);
   if (plan.n_mma == 0) return BDLM_ERR_UNSUPPORTED;
@@ -251,13 +315,9 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
                                          d.L, d.Hq, d.Hkv, d.max_pages_per_seq, d.num_pages,
                                          scale, plan, static_cast<float*>(st->data),
                                          st->attn_cnt, st->err, st->num_sms,
-                                         static_cast<cudaStream_t>(stream));
+                                         static_cast<cudaStream_t>(stream), table_div);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
-
-}  // extern "C"
-
-namespace {
 
 // The LM head planned for n_active rows; n_active_dev (may be null) holds the count the
 // kernels use, read on the device (at most n_active).

@@ -65,6 +65,7 @@ struct AttnParams {
   int* work;  // [0] next item, [1] CTAs finished
   const int* order;  // whole-sequence mode: sequences by decreasing KV length, else null
   int B, L, Hq, Hkv, G, max_pages, num_pages;
+  int table_div;     // sequence b uses page-table row b / table_div (prompt blocks share a row)
   int lsub, row_groups, rows_per_group, split_tokens, max_splits, chunk_tiles;
   int total_items;
   float scale_log2;  // sm_scale * log2(e)
@@ -225,7 +226,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       ++seq;
       int* pid = s_pid[seq % 3];
       const int32_t* pt =
-          p.page_table + static_cast<size_t>(it.b) * p.max_pages + it.t_begin / kPage;
+          p.page_table + static_cast<size_t>(it.b / p.table_div) * p.max_pages + it.t_begin / kPage;
       const int np = (it.t_end - it.t_begin + kPage - 1) / kPage;
       int bad = 0;
       for (int q = lane; q < np; q += 32) {
@@ -899,6 +900,27 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 }  // namespace
 
+namespace {
+// Prompt block j of sequence b becomes sequence b * nb + j of the attention: its prefix is the
+// cached prefix plus the j blocks before it.
+__global__ void prompt_prefix_kernel(const int32_t* __restrict__ prefix_lens, int B, int nb, int L,
+                                     int32_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * nb) return;
+  const int p = prefix_lens[i / nb];
+  out[i] = p < 0 ? p : p + (i % nb) * L;
+}
+}  // namespace
+
+cudaError_t launch_prompt_prefix(const int32_t* prefix_lens, int B, int nb, int L, int32_t* out,
+                                 cudaStream_t stream) {
+  const int n = B * nb;
+  return launch_pdl(prompt_prefix_kernel, dim3((n + 255) / 256), dim3(256), 0, stream,
+                    prefix_lens, B, nb, L, out);
+}
+
 AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size,
                         int num_sms) {
   AttnPlan pl;
@@ -948,9 +970,10 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
                              const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int table_div) {
   AttnParams prm;
   prm.page_table = page_table;
+  prm.table_div = table_div < 1 ? 1 : table_div;
   prm.prefix_lens = prefix_lens;
   prm.out = out;
   prm.part = part;

@@ -78,7 +78,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
                              const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int table_div = 1);
 
 // ------------------------------------------------------------------ LM head
 struct LmHeadPlan {
@@ -100,6 +100,10 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            const int32_t* n_active_dev, int n_rows, int H, int V,
                            uint16_t* logits, const LmHeadPlan& plan, int* err,
                            cudaStream_t stream);
+
+// Prompt block j of sequence b -> attention sequence b * nb + j with prefix prefix[b] + j * L.
+cudaError_t launch_prompt_prefix(const int32_t* prefix_lens, int B, int nb, int L, int32_t* out,
+                                 cudaStream_t stream);
 
 // Device-side round pieces (round.cu).
 struct StepCopy {  // per-step inputs: slice s of src[j] (n_vec[j] 16-byte vectors) -> dst[j]

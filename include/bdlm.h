@@ -102,6 +102,30 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
                          bdlm_bf16* out, bdlm_stream stream);
 
 /*
+ * Block prefill: the prompt's K/V written into the cache and block-causal attention over the
+ * prompt, so that the rounds that follow find the prompt in the paged cache.
+ * Source: JetEngine notes, "Kernels" (block prefill attention and the KV-cache store) and
+ * "ModelRunner" (prefill and denoise have different attention patterns); SDAR page, "What is
+ * SDAR?" (autoregression across blocks, diffusion inside a block).
+ *
+ * The prompt of sequence b is prompt_len tokens (a multiple of desc->L, the block length),
+ * placed after prefix_lens[b] tokens already in the cache (0 for a fresh prompt).  Token t of
+ * the prompt, in prompt block j = t / L, attends to every cached token before the prompt,
+ * every prompt token of blocks before j and every token of block j:
+ *     out[b,t,h,:] = softmax_k(sm_scale * q[b,t,h,:] . K_b[k]) V_b[k],
+ *                    k < prefix_lens[b] + (j+1) * L,  KV head as bdlm_block_attention.
+ * Layouts: q, out [B, prompt_len, Hq, D]; k_new, v_new [B, prompt_len, Hkv, D] (written to
+ * the slots prefix_lens[b] .. + prompt_len - 1); pools, page_table, prefix_lens as
+ * bdlm_block_attention; prefix_lens[b] + prompt_len must fit the page table.  bf16 pointers
+ * 16-byte aligned.  Runs as the K/V write followed by bdlm_block_attention over B *
+ * (prompt_len / L) block sequences that share their sequence's page-table row.
+ */
+int bdlm_prefill_attention(const bdlm_attn_desc* desc, int prompt_len, const bdlm_bf16* q,
+                           const bdlm_bf16* k_new, const bdlm_bf16* v_new, bdlm_bf16* k_pages,
+                           bdlm_bf16* v_pages, const int32_t* page_table,
+                           const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream);
+
+/*
  * Selective LM head.
  * Source: JetEngine notes, "ModelRunner" (selective logits: the LM head runs only for
  * DENOISING sequences) and "Optimization History" (opt23: LM head only on masked rows).
