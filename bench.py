@@ -546,6 +546,50 @@ def chain_config5(bd, device, flush, reps: int, seed: int):
             "gpu_launches_per_block": 1}
 
 
+def prefill_bench(bd, device, flush, reps: int, seed: int, B=128, n=512, L=4):
+    """Block prefill of fresh prompts (B=128 prompts of 512 tokens, SDAR-4B attention shape,
+    block length 4): the prompt's K/V written into a shuffled page pool and block-causal
+    attention over the prompt.  L2 flushed before each call."""
+    import torch
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D = 32, 8, 128
+    a = W.make_attention(rng, B, n, Hq, Hkv, D, prefix_lens=np.zeros(B, np.int64), poison=False)
+    kp = torch.zeros((a.k_ref.shape[0], 16, Hkv, D), dtype=torch.bfloat16, device=device)
+    vp = torch.zeros_like(kp)
+    pt = torch.from_numpy(a.page_table_ref).to(device)
+    pl = torch.zeros((B,), dtype=torch.int32, device=device)
+    q = _bf16(W._normal_bf16(rng, (B, n, Hq, D), 0.5), device)
+    kn = _bf16(W._normal_bf16(rng, (B, n, Hkv, D), 0.5), device)
+    vn = _bf16(W._normal_bf16(rng, (B, n, Hkv, D), 0.5), device)
+    out = torch.empty((B, n, Hq, D), dtype=torch.bfloat16, device=device)
+    desc = bd.attn_desc(B, L, Hq, Hkv, D, a.page_table_ref.shape[1], a.k_ref.shape[0])
+    stream = torch.cuda.Stream(device=device)
+    evs = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + reps):
+            flush(stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bd.bdlm_prefill_attention(desc, n, q, kn, vn, kp, vp, pt, pl, out, stream.cuda_stream)
+            e1.record(stream)
+            if i >= 3:
+                evs.append((e0, e1))
+    torch.cuda.synchronize()
+    assert bd.bdlm_device_error() == 0
+    ms = float(np.mean([x.elapsed_time(y) for x, y in evs]))
+    nb = n // L
+    kv_read = B * Hkv * D * 2 * 2 * L * nb * (nb + 1) // 2      # every block re-reads its prefix
+    qo = B * n * Hq * D * 2 * 2
+    written = B * n * Hkv * D * 2 * 2
+    return {"workload": f"prefill: {B} fresh prompts of {n} tokens, block length {L}, "
+                        "Hq=32 Hkv=8 D=128, shuffled pages",
+            "ms": ms, "tokens_per_s": B * n / (ms / 1e3),
+            "bytes": kv_read + qo + written,
+            "achieved_gbs": (kv_read + qo + written) / (ms / 1e3) / 1e9,
+            "note": "runs the block attention kernel over B * n / L block sequences, so every "
+                    "block re-reads the K/V before it (traffic grows with n^2 / L)"}
+
+
 KERNEL_SOURCES = {"attention": ("attention_config2", "attention.cu"),
                   "lm_head": ("lm_head_config2_256rows", "lm_head.cu"),
                   "commit": ("commit_config2", "commit.cu")}
@@ -666,6 +710,8 @@ def run_ours(args, rank, world, local):
     if not args.quick and rank == 0:
         torch.cuda.empty_cache()
         line["chain"] = chain_config5(bd, device, flush, 20, W.seed_for(5))
+        torch.cuda.empty_cache()
+        line["prefill"] = prefill_bench(bd, device, flush, 10, W.seed_for(2, 9))
         torch.cuda.empty_cache()
     if not args.quick:
         barrier()
