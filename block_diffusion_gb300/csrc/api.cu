@@ -23,9 +23,9 @@ struct DeviceState {
   bool supported = false;
   int num_sms = 0;
   int* err = nullptr;            // device error word
-  int* attn_cnt = nullptr;       // split-KV arrival counters (zero between calls)
+  int* attn_cnt = nullptr;       // attention scheduler counters (zero between calls)
   size_t attn_cnt_cap = 0;
-  void* data = nullptr;          // partial results / gathered rows
+  void* data = nullptr;          // split / commit partials, gathered rows, sequence order
   size_t data_cap = 0;
   void* aux = nullptr;           // prompt-block prefix lengths of a prefill
   size_t aux_cap = 0;

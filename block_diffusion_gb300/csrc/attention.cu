@@ -17,12 +17,14 @@
 //    thread per tensor-memory lane) run the softmax and the epilogue.
 //  * An item is cut into chunks of tiles whose S^T fits in tensor memory.  Softmax per chunk
 //    in two phases: all S^T tiles first, the exact column maximum once, then P^T = exp(S^T-m)
-//    (bf16, shared memory) and O^T += V^T P^T in tensor memory; later chunks of the same
-//    item rescale O^T once.  The ring carries K of chunk u+1 ahead of V of chunk u and S^T
-//    is double-buffered, so the softmax of one chunk overlaps the K stream of the next and
-//    the pipeline never drains between items.
-//  * Splits of a long sequence write (O, m, l) partials that a small second kernel merges, so
-//    no CTA ever waits on another one; every wait inside a CTA is bounded.
+//    (bf16, shared memory) and O^T += V^T P^T in tensor memory; a later chunk moves the
+//    running max (and rescales O^T) only when it raises it by more than 2^kLazyRescale.  The
+//    ring carries K of chunk u+1 ahead of V of chunk u and S^T is double-buffered, so the
+//    softmax of one chunk overlaps the K stream of the next and the pipeline never drains
+//    between items.
+//  * Either whole sequences, longest first (when there are enough items), or splits of a
+//    long sequence that write (O, m, l) partials merged by a small second kernel; no CTA
+//    ever waits on another one, and every wait inside a CTA is bounded.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -60,7 +62,6 @@ struct AttnParams {
   const int32_t* prefix_lens;
   uint16_t* out;
   float* part;
-  int* cnt;
   int* err;
   int* work;  // [0] next item, [1] CTAs finished
   const int* order;  // whole-sequence mode: sequences by decreasing KV length, else null
@@ -956,12 +957,12 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
     pl.split_tokens = static_cast<int>((max_tok + kTile - 1) / kTile * kTile);
     pl.max_splits = 1;
     pl.part_bytes = static_cast<size_t>(B) * sizeof(int);
-    pl.cnt_bytes = groups * sizeof(int) + 2 * sizeof(int);
+    pl.cnt_bytes = 2 * sizeof(int);
     return pl;
   }
   pl.max_splits = static_cast<int>((max_tok + pl.split_tokens - 1) / pl.split_tokens);
   pl.part_bytes = groups * pl.max_splits * static_cast<size_t>(pl.n_mma) * 130 * sizeof(float);
-  pl.cnt_bytes = groups * sizeof(int) + 2 * sizeof(int);
+  pl.cnt_bytes = 2 * sizeof(int);  // the scheduler's next-item and finished-CTA counters
   return pl;
 }
 
@@ -977,8 +978,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   prm.prefix_lens = prefix_lens;
   prm.out = out;
   prm.part = part;
-  prm.work = cnt;  // two words of scheduler state, then the split counters
-  prm.cnt = cnt + 2;
+  prm.work = cnt;  // two words of scheduler state
   prm.order = nullptr;
   prm.err = err;
   prm.B = B;

@@ -564,8 +564,6 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms) {
   CommitPlan p;
   const long long rows = static_cast<long long>(B) * L;
   p.grid = num_sms > 0 ? num_sms : 1;
-  p.S = 1;
-  p.chunk = kChunk;
   p.total_items = rows;
   p.smem_bytes = static_cast<size_t>(kWarps) * kRing * kChunkBytes + 128;
   // one partial per (warp, masked row segment): slots w + k < warps + rows

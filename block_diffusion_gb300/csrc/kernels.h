@@ -38,8 +38,6 @@ struct CommitPartial {
 };
 
 struct CommitPlan {
-  int S = 1;                  // partial results per row and warp
-  int chunk = 0;              // logits per shared-memory stage
   long long total_items = 0;  // rows
   int grid = 1;               // streaming CTAs (one per SM, persistent)
   int fin_threads = 32;       // threads of a finalizing CTA (one CTA per block)
