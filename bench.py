@@ -343,33 +343,38 @@ def time_round_graph(rnd: Round, stream, steps: int, warmup: int, flush, barrier
     return np.array([a.elapsed_time(b) for a, b in evs]), wall
 
 
-def e2e_round(lib, a, ci, lm, device, steps, warmup):
-    """The round through the C-ABI from pinned host buffers: every step copies its inputs
-    host->device (q, the referenced K/V pages as a compact pool, page table, prefix lengths,
-    the hidden rows, the active row ids, the mask), runs attention, LM head, commit and mask
-    update, and copies tok/conf/commit back.  W is model weight: resident on the device."""
+def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
+    """The round through the C-ABI from pinned host buffers.  The paged K/V cache and W are
+    resident device state (the cache holds every sequence's prefix); every step copies its own
+    inputs host->device (q, the block's new K/V, the hidden rows, the active row ids, the
+    mask), writes the block K/V into the cache, runs attention, LM head, commit and mask
+    update, and copies tok/conf/commit back."""
     import torch
     stream = torch.cuda.Stream(device=device)
-    n_ref = a.k_ref.shape[0]
+    rng = np.random.default_rng(seed)
+    B, L = a.B, a.L
+    k_new = W._normal_bf16(rng, (B, L, a.Hkv, a.D), 0.5)
+    v_new = W._normal_bf16(rng, (B, L, a.Hkv, a.D), 0.5)
     h = {
         "q": torch.from_numpy(a.q.view(np.int16)).pin_memory(),
-        "k": torch.from_numpy(a.k_ref.view(np.int16)).pin_memory(),
-        "v": torch.from_numpy(a.v_ref.view(np.int16)).pin_memory(),
-        "pt": torch.from_numpy(a.page_table_ref).pin_memory(),
-        "pl": torch.from_numpy(a.prefix_lens).pin_memory(),
+        "kn": torch.from_numpy(k_new.view(np.int16)).pin_memory(),
+        "vn": torch.from_numpy(v_new.view(np.int16)).pin_memory(),
         "hid": torch.from_numpy(lm.hidden.view(np.int16)).pin_memory(),
         "act": torch.from_numpy(lm.active_idx).pin_memory(),
         "mk": torch.from_numpy(ci.mask).pin_memory(),
     }
     d = {k: torch.empty_like(v, device=device) for k, v in h.items()}
-    w = _bf16(lm.w, device)
-    logits = torch.empty((a.B * a.L, ci.V), dtype=torch.bfloat16, device=device)
-    outs_h = {"tok": torch.empty((a.B, a.L), dtype=torch.int32).pin_memory(),
-              "conf": torch.empty((a.B, a.L), dtype=torch.float32).pin_memory(),
-              "com": torch.empty((a.B, a.L), dtype=torch.uint8).pin_memory()}
+    kp, vp = _bf16(a.k_ref, device), _bf16(a.v_ref, device)      # resident cache
+    pt = torch.from_numpy(a.page_table_ref).to(device)
+    pl = torch.from_numpy(a.prefix_lens).to(device)
+    w = _bf16(lm.w, device)                                       # resident weights
+    logits = torch.empty((B * L, ci.V), dtype=torch.bfloat16, device=device)
+    outs_h = {"tok": torch.empty((B, L), dtype=torch.int32).pin_memory(),
+              "conf": torch.empty((B, L), dtype=torch.float32).pin_memory(),
+              "com": torch.empty((B, L), dtype=torch.uint8).pin_memory()}
     outs_d = {k: torch.empty_like(v, device=device) for k, v in outs_h.items()}
-    out = torch.empty((a.B, a.L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
-    desc = lib.attn_desc(a.B, a.L, a.Hq, a.Hkv, a.D, a.page_table.shape[1], n_ref)
+    out = torch.empty((B, L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
+    desc = lib.attn_desc(B, L, a.Hq, a.Hkv, a.D, a.page_table_ref.shape[1], a.k_ref.shape[0])
     n_act = len(lm.active_idx)
     h2d = sum(v.numel() * v.element_size() for v in h.values())
     d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
@@ -379,12 +384,12 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup):
         for k in h:
             d[k].copy_(h[k], non_blocking=True)
         bf = torch.bfloat16
-        lib.bdlm_block_attention(desc, d["q"].view(bf), d["k"].view(bf), d["v"].view(bf), d["pt"],
-                                 d["pl"], a.L, out, s)
-        lib.bdlm_lm_head(d["hid"].view(bf), w, d["act"], n_act, a.B * a.L, lm.H, ci.V, logits, s)
-        lib.bdlm_confidence_commit(logits, d["mk"], a.B, a.L, ci.V, ci.threshold,
+        lib.bdlm_write_block_kv(desc, d["kn"].view(bf), d["vn"].view(bf), kp, vp, pt, pl, s)
+        lib.bdlm_block_attention(desc, d["q"].view(bf), kp, vp, pt, pl, L, out, s)
+        lib.bdlm_lm_head(d["hid"].view(bf), w, d["act"], n_act, B * L, lm.H, ci.V, logits, s)
+        lib.bdlm_confidence_commit(logits, d["mk"], B, L, ci.V, ci.threshold,
                                    ci.temperature, outs_d["tok"], outs_d["conf"], outs_d["com"], s)
-        lib.bdlm_apply_commit(d["mk"], outs_d["com"], a.B * a.L, s)
+        lib.bdlm_apply_commit(d["mk"], outs_d["com"], B * L, s)
         for k in outs_h:
             outs_h[k].copy_(outs_d[k], non_blocking=True)
 
@@ -399,7 +404,7 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup):
         e1.record(stream)
         stream.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    del w, logits
+    del w, logits, kp, vp
     return ms, h2d, d2h
 
 
@@ -715,13 +720,16 @@ def run_ours(args, rank, world, local):
         torch.cuda.empty_cache()
     if not args.quick:
         barrier()
-        e2e_ms, h2d, d2h = e2e_round(bd, a, ci, lm, device, max(10, args.steps // 20), 3)
+        e2e_ms, h2d, d2h = e2e_round(bd, a, ci, lm, device, max(20, args.steps // 20), 3,
+                                     rank_seed(args.seed, rank) + 2)
         e2e_max = max_over_ranks(e2e_ms, world)
         line["e2e"] = {"value": job_value(a.B * a.L, world, e2e_max), "unit": UNIT,
                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                        "ms_per_step": e2e_max,
-                       "note": "per rank and step; K/V copied as a compact pool of the "
-                               "referenced pages; W resident"}
+                       "note": "per rank and step: q, the block's new K/V, hidden rows, active "
+                               "rows and mask copied in from pinned host memory, the block K/V "
+                               "written into the resident cache, tok/conf/commit copied back; "
+                               "the paged cache (every prefix) and W are resident"}
         if rank == 0:
             line["cpu_baseline"] = cpu_baseline(a, ci, lm)
     if rank == 0:
