@@ -39,7 +39,8 @@ METRIC = "denoised block-positions/s per round (B=128, SDAR-4B shape); % HBM roo
 UNIT = "block-positions/s"
 WORKLOAD = ("config2: B=128 L=4 Hq=32 Hkv=8 D=128 bf16, prefix U[512,4096], page 16, "
             "shuffled 140000-page pool, mask 1/2 per block, tau=0.75 T=1; LM head H=2560 "
-            "V=151936 on the 256 masked rows (hidden N(0,1), W N(0,0.02^2))")
+            "V=151936 on the 256 masked rows (hidden N(0,1), W N(0,0.02^2)) fused with the "
+            "confidence/commit")
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -210,16 +211,30 @@ def algorithmic(a, ci, lm):
         "lm_head": (ci.V * lm.H * 2 + n_act * lm.H * 2 + n_act * ci.V * 2,
                     2 * n_act * lm.H * ci.V),
         "commit": (int(ci.mask.sum()) * ci.V * 2, 0),
+        # fused LM head + confidence: W once and the scored rows in; the logits never leave
+        # the SMs (tok/conf/commit out are a few KB)
+        "lm_head_commit": (ci.V * lm.H * 2 + n_act * lm.H * 2, 2 * n_act * lm.H * ci.V),
     }
 
 
 class Round:
-    """Device-resident inputs and the launch sequence of one round."""
+    """Device-resident inputs and the launch sequence of one round.  Modes:
+    fused     attention -> LM head fused with confidence/commit -> mask update (the headline);
+    unfused   attention -> LM head (logits to HBM) -> confidence/commit -> mask update;
+    supplied  attention -> confidence/commit over the supplied logits -> mask update."""
 
-    def __init__(self, lib, a, ci, lm, device, with_lm_head=True):
+    STAGES = {"fused": ("attention", "lm_head_commit", "mask_update"),
+              "unfused": ("attention", "lm_head", "commit", "mask_update"),
+              "supplied": ("attention", "commit", "mask_update")}
+    # attention + split merge; [scored rows + row gather + fused GEMM + finalize |
+    # row gather + LM head]; commit streaming + finalize; mask update
+    LAUNCHES = {"fused": 2 + 4 + 1, "unfused": 2 + 2 + 2 + 1, "supplied": 2 + 2 + 1}
+
+    def __init__(self, lib, a, ci, lm, device, mode="fused"):
         import torch
         self.torch = torch
         self.lib = lib
+        self.mode = mode
         self.a, self.ci = a, ci
         self.B, self.L, self.V = a.B, a.L, ci.V
         shape = (a.pool_pages, a.P, a.Hkv, a.D)
@@ -232,7 +247,12 @@ class Round:
         self.pt = torch.from_numpy(a.page_table).to(device)
         self.pl = torch.from_numpy(a.prefix_lens).to(device)
         self.out = torch.empty((a.B, a.L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
-        self.logits = _bf16(ci.logits.reshape(a.B * a.L, ci.V), device)
+        if mode == "fused":
+            self.logits = None
+        elif mode == "supplied":
+            self.logits = _bf16(ci.logits.reshape(a.B * a.L, ci.V), device)
+        else:
+            self.logits = torch.empty((a.B * a.L, ci.V), dtype=torch.bfloat16, device=device)
         self.mask0 = torch.from_numpy(ci.mask).to(device)
         self.mask = self.mask0.clone()
         self.tok = torch.empty((a.B, a.L), dtype=torch.int32, device=device)
@@ -240,40 +260,53 @@ class Round:
         self.commit = torch.empty((a.B, a.L), dtype=torch.uint8, device=device)
         self.desc = lib.attn_desc(a.B, a.L, a.Hq, a.Hkv, a.D, a.page_table.shape[1],
                                   a.pool_pages)
-        self.with_lm_head = with_lm_head
-        if with_lm_head:
+        self.n_act = 0
+        if mode != "supplied":
             self.H = lm.H
             self.hidden = _bf16(lm.hidden, device)
             self.w = _bf16(lm.w, device)
             self.act = torch.from_numpy(lm.active_idx).to(device)
             self.n_act = len(lm.active_idx)
 
+    def stages(self):
+        return self.STAGES[self.mode]
+
     def launches_per_step(self):
-        # attention + split merge, [row gather + LM head,] commit, mask update
-        return 6 if self.with_lm_head else 4
+        return self.LAUNCHES[self.mode]
 
     def step(self, stream, events=None):
-        """Enqueue one round on `stream`; events (list) get a record after each stage."""
+        """Enqueue one round on `stream`; events (list) get a record before the first stage
+        and after each stage."""
         lib, s = self.lib, stream.cuda_stream
-        if events is not None:
-            events[0].record(stream)
+        k = 0
+
+        def mark():
+            nonlocal k
+            if events is not None:
+                events[k].record(stream)
+            k += 1
+
+        mark()
         lib.bdlm_block_attention(self.desc, self.q, self.kp, self.vp, self.pt, self.pl, self.L,
                                  self.out, s)
-        if events is not None:
-            events[1].record(stream)
-        if self.with_lm_head:
-            lib.bdlm_lm_head(self.hidden, self.w, self.act, self.n_act, self.B * self.L, self.H,
-                             self.V, self.logits, s)
-        if events is not None:
-            events[2].record(stream)
-        lib.bdlm_confidence_commit(self.logits, self.mask, self.B, self.L, self.V,
-                                   self.ci.threshold, self.ci.temperature, self.tok, self.conf,
-                                   self.commit, s)
-        if events is not None:
-            events[3].record(stream)
+        mark()
+        if self.mode == "fused":
+            lib.bdlm_lm_head_commit(self.hidden, self.w, self.mask, None, self.B, self.L,
+                                    self.H, self.V, lib.BDLM_COMMIT_THRESHOLD, 1,
+                                    self.ci.threshold, self.ci.temperature, self.tok, self.conf,
+                                    self.commit, None, s)
+            mark()
+        else:
+            if self.mode == "unfused":
+                lib.bdlm_lm_head(self.hidden, self.w, self.act, self.n_act, self.B * self.L,
+                                 self.H, self.V, self.logits, s)
+                mark()
+            lib.bdlm_confidence_commit(self.logits, self.mask, self.B, self.L, self.V,
+                                       self.ci.threshold, self.ci.temperature, self.tok,
+                                       self.conf, self.commit, s)
+            mark()
         lib.bdlm_apply_commit(self.mask, self.commit, self.B * self.L, s)
-        if events is not None:
-            events[4].record(stream)
+        mark()
 
     def reset_mask(self, stream):
         with self.torch.cuda.stream(stream):
@@ -295,7 +328,8 @@ def time_round(rnd: Round, stream, steps: int, warmup: int, flush, barrier):
         flush(stream)
         rnd.step(stream)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    ns = len(rnd.stages())
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(steps)]
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -306,9 +340,9 @@ def time_round(rnd: Round, stream, steps: int, warmup: int, flush, barrier):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier()
-    stage = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(4)]
+    stage = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(ns)]
                       for k in range(steps)])
-    total = np.array([evs[k][0].elapsed_time(evs[k][4]) for k in range(steps)])
+    total = np.array([evs[k][0].elapsed_time(evs[k][ns]) for k in range(steps)])
     return total, stage, wall
 
 
@@ -346,8 +380,8 @@ def time_round_graph(rnd: Round, stream, steps: int, warmup: int, flush, barrier
 def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
     """The round through the C-ABI from pinned host buffers.  The paged K/V cache and W are
     resident device state (the cache holds every sequence's prefix); every step copies its own
-    inputs host->device (q, the block's new K/V, the hidden rows, the active row ids, the
-    mask), writes the block K/V into the cache, runs attention, LM head, commit and mask
+    inputs host->device (q, the block's new K/V, the hidden rows, the mask), writes the block
+    K/V into the cache, runs attention, the LM head fused with confidence/commit and the mask
     update, and copies tok/conf/commit back."""
     import torch
     stream = torch.cuda.Stream(device=device)
@@ -360,7 +394,6 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
         "kn": torch.from_numpy(k_new.view(np.int16)).pin_memory(),
         "vn": torch.from_numpy(v_new.view(np.int16)).pin_memory(),
         "hid": torch.from_numpy(lm.hidden.view(np.int16)).pin_memory(),
-        "act": torch.from_numpy(lm.active_idx).pin_memory(),
         "mk": torch.from_numpy(ci.mask).pin_memory(),
     }
     d = {k: torch.empty_like(v, device=device) for k, v in h.items()}
@@ -368,14 +401,12 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
     pt = torch.from_numpy(a.page_table_ref).to(device)
     pl = torch.from_numpy(a.prefix_lens).to(device)
     w = _bf16(lm.w, device)                                       # resident weights
-    logits = torch.empty((B * L, ci.V), dtype=torch.bfloat16, device=device)
     outs_h = {"tok": torch.empty((B, L), dtype=torch.int32).pin_memory(),
               "conf": torch.empty((B, L), dtype=torch.float32).pin_memory(),
               "com": torch.empty((B, L), dtype=torch.uint8).pin_memory()}
     outs_d = {k: torch.empty_like(v, device=device) for k, v in outs_h.items()}
     out = torch.empty((B, L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
     desc = lib.attn_desc(B, L, a.Hq, a.Hkv, a.D, a.page_table_ref.shape[1], a.k_ref.shape[0])
-    n_act = len(lm.active_idx)
     h2d = sum(v.numel() * v.element_size() for v in h.values())
     d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
 
@@ -386,9 +417,9 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
         bf = torch.bfloat16
         lib.bdlm_write_block_kv(desc, d["kn"].view(bf), d["vn"].view(bf), kp, vp, pt, pl, s)
         lib.bdlm_block_attention(desc, d["q"].view(bf), kp, vp, pt, pl, L, out, s)
-        lib.bdlm_lm_head(d["hid"].view(bf), w, d["act"], n_act, B * L, lm.H, ci.V, logits, s)
-        lib.bdlm_confidence_commit(logits, d["mk"], B, L, ci.V, ci.threshold,
-                                   ci.temperature, outs_d["tok"], outs_d["conf"], outs_d["com"], s)
+        lib.bdlm_lm_head_commit(d["hid"].view(bf), w, d["mk"], None, B, L, lm.H, ci.V,
+                                lib.BDLM_COMMIT_THRESHOLD, 1, ci.threshold, ci.temperature,
+                                outs_d["tok"], outs_d["conf"], outs_d["com"], None, s)
         lib.bdlm_apply_commit(d["mk"], outs_d["com"], B * L, s)
         for k in outs_h:
             outs_h[k].copy_(outs_d[k], non_blocking=True)
@@ -404,7 +435,7 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
         e1.record(stream)
         stream.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    del w, logits, kp, vp
+    del w, kp, vp
     return ms, h2d, d2h
 
 
@@ -596,6 +627,7 @@ def prefill_bench(bd, device, flush, reps: int, seed: int, B=128, n=512, L=4):
 
 
 KERNEL_SOURCES = {"attention": ("attention_config2", "attention.cu"),
+                  "lm_head_commit": ("lm_conf_config2_256rows", "lm_head.cu"),
                   "lm_head": ("lm_head_config2_256rows", "lm_head.cu"),
                   "commit": ("commit_config2", "commit.cu")}
 
@@ -613,7 +645,7 @@ def kernel_roofline(name, alg, ms, peaks):
          "peak_source": f"{peaks['source']} (copy bandwidth)"}
     if flops:
         r["tflops"] = flops / (ms / 1e3) / 1e12
-    if name == "lm_head":
+    if name in ("lm_head", "lm_head_commit"):
         r["frac_tensor"] = r["tflops"] / peaks["bf16_tflops"]
     return r
 
@@ -646,7 +678,7 @@ def run_ours(args, rank, world, local):
 
     # each rank denoises its own batch of 128 sequences (data parallel, no collective)
     c, a, ci, lm = make_workload(rank_seed(args.seed, rank), compact_pool=args.compact_pool)
-    rnd = Round(bd, a, ci, lm, device)
+    rnd = Round(bd, a, ci, lm, device, mode="fused")
     stream = torch.cuda.Stream(device=device)
     sampler = ClockSampler(local)
     sampler.start()
@@ -658,21 +690,23 @@ def run_ours(args, rank, world, local):
                                        barrier)
     clocks = sampler.stop()
     assert bd.bdlm_device_error() == 0, "device error during the timed round"
-    eager_total, stage, _ = time_round(rnd, stream, max(20, min(args.steps, 200)), 3, flush,
-                                       barrier)
+    eager_n = max(20, min(args.steps, 200))
+    eager_total, stage, _ = time_round(rnd, stream, eager_n, 3, flush, barrier)
+    n_act = rnd.n_act
+    del rnd
+    torch.cuda.empty_cache()
 
     ms = float(total.mean())
     ms_max = max_over_ranks(ms, world)
     value = job_value(a.B * a.L, world, ms_max)
 
     alg = algorithmic(a, ci, lm)
-    stage_ms = {"attention": float(stage[:, 0].mean()), "lm_head": float(stage[:, 1].mean()),
-                "commit": float(stage[:, 2].mean()), "mask_update": float(stage[:, 3].mean())}
+    stage_ms = {k: float(stage[:, i].mean()) for i, k in enumerate(Round.STAGES["fused"])}
     kernels = {k: kernel_roofline(k, alg, stage_ms[k], peaks)
-               for k in ("attention", "lm_head", "commit")}
-    dominant = max(("attention", "lm_head"), key=lambda k: stage_ms[k])
+               for k in ("attention", "lm_head_commit")}
+    dominant = max(("attention", "lm_head_commit"), key=lambda k: stage_ms[k])
     roofline = dict(kernels[dominant])
-    step_bytes = sum(v[0] for v in alg.values())
+    step_bytes = alg["attention"][0] + alg["lm_head_commit"][0]
     roofline["round_frac"] = step_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -680,23 +714,45 @@ def run_ours(args, rank, world, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": 128 * world, "block_len": 4,
-                       "lm_head_rows": rnd.n_act, "hidden": lm.H,
+                       "lm_head_rows": n_act, "hidden": lm.H,
                        "l2": "flushed before every step (256 MB fill, outside the timed events)",
                        "parallelism": f"dp{world} (independent batches, no collective)",
                        "seed": args.seed},
             "clocks": clocks,
-            "gpu_launches": rnd.launches_per_step() * args.steps,
+            "gpu_launches": Round.LAUNCHES["fused"] * args.steps,
             "launch": "eager" if args.eager else "cuda_graph",
             "eager_ms_per_step": float(eager_total.mean()),
             "stages_ms": dict(stage_ms, note="eager launches; each stage includes its launch "
-                                             "gap; attention includes the split merge"),
+                                             "gap; attention includes the split merge; "
+                                             "lm_head_commit includes the scored-row list, "
+                                             "the row gather and the per-block finalize"),
             "roofline": roofline,
             "kernels": kernels,
             "wall_s": wall}
 
     if rank == 0:
+        # the same round with the logits written to HBM and read back by the commit kernel
+        unf = Round(bd, a, ci, lm, device, mode="unfused")
+        u_steps = max(20, min(args.steps, 500))
+        if args.eager:
+            utotal, _, _ = time_round(unf, stream, u_steps, 3, flush, lambda: None)
+        else:
+            utotal, _ = time_round_graph(unf, stream, u_steps, 3, flush, lambda: None)
+        _, ustage, _ = time_round(unf, stream, eager_n, 3, flush, lambda: None)
+        ustage_ms = {k: float(ustage[:, i].mean()) for i, k in enumerate(Round.STAGES["unfused"])}
+        for k in ("lm_head", "commit"):
+            kernels[k] = kernel_roofline(k, alg, ustage_ms[k], peaks)
+        line["round_unfused"] = {
+            "value": a.B * a.L / (float(utotal.mean()) / 1e3), "unit": UNIT,
+            "ms_per_step": float(utotal.mean()),
+            "workload": "the same round with the LM head's logits stored to HBM and read back "
+                        "by the streaming confidence/commit kernel",
+            "stages_ms": ustage_ms,
+            "gpu_launches": Round.LAUNCHES["unfused"] * u_steps}
+        del unf
+        torch.cuda.empty_cache()
         # config 2 as printed: the commit reads the supplied logits, no LM head
-        sup = Round(bd, a, ci, lm, device, with_lm_head=False)
+        sup = Round(bd, a, ci, lm, device, mode="supplied")
         s_steps = max(20, min(args.steps, 500))
         if args.eager:
             stotal, _, _ = time_round(sup, stream, s_steps, 3, flush, lambda: None)
@@ -709,7 +765,7 @@ def run_ours(args, rank, world, local):
                         "mask update (no LM head)",
             "hbm_frac": (alg["attention"][0] + alg["commit"][0]) / (float(stotal.mean()) / 1e3)
                         / 1e9 / peaks["hbm_gbs"],
-            "gpu_launches": sup.launches_per_step() * s_steps}
+            "gpu_launches": Round.LAUNCHES["supplied"] * s_steps}
         del sup
         torch.cuda.empty_cache()
     if not args.quick and rank == 0:
@@ -726,10 +782,11 @@ def run_ours(args, rank, world, local):
         line["e2e"] = {"value": job_value(a.B * a.L, world, e2e_max), "unit": UNIT,
                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                        "ms_per_step": e2e_max,
-                       "note": "per rank and step: q, the block's new K/V, hidden rows, active "
-                               "rows and mask copied in from pinned host memory, the block K/V "
-                               "written into the resident cache, tok/conf/commit copied back; "
-                               "the paged cache (every prefix) and W are resident"}
+                       "note": "per rank and step: q, the block's new K/V, hidden rows and "
+                               "mask copied in from pinned host memory, the block K/V written "
+                               "into the resident cache, attention, fused LM head + commit, "
+                               "mask update, tok/conf/commit copied back; the paged cache "
+                               "(every prefix) and W are resident"}
         if rank == 0:
             line["cpu_baseline"] = cpu_baseline(a, ci, lm)
     if rank == 0:

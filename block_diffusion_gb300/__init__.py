@@ -33,7 +33,7 @@ BDLM_COMMIT_SEQUENTIAL = 2
 BDLM_COMMIT_ANTI_SEQUENTIAL = 3
 
 EXPORTS = ("bdlm_block_attention", "bdlm_prefill_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
-           "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
+           "bdlm_lm_head_commit", "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
            "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_round_loop_create",
            "bdlm_round_loop_launch", "bdlm_round_loop_destroy", "bdlm_status_string",
            "bdlm_device_error", "bdlm_release")
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bdlm_confidence_commit_rule.restype = I
     lib.bdlm_lm_head_device_count.argtypes = [P, P, P, P, I, I, I, I, P, P]
     lib.bdlm_lm_head_device_count.restype = I
+    lib.bdlm_lm_head_commit.argtypes = [P, P, P, P, I, I, I, I, I, I, F, F, P, P, P, P, P]
+    lib.bdlm_lm_head_commit.restype = I
     lib.bdlm_active_rows.argtypes = [P, P, I, I, P, P, P]
     lib.bdlm_active_rows.restype = I
     lib.bdlm_write_block_kv.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P]
@@ -196,6 +198,17 @@ def bdlm_lm_head_device_count(hidden, w, active_idx, n_active_dev, max_active: i
                                        _ptr(n_active_dev), int(max_active), int(n_rows), int(H),
                                        int(V), _ptr(logits), _stream(stream))
     _check("bdlm_lm_head_device_count", rc)
+
+
+def bdlm_lm_head_commit(hidden, w, mask, denoising, B: int, L: int, H: int, V: int, rule: int,
+                        k: int, threshold: float, temperature: float, tok_out, conf_out,
+                        commit_out, logits=None, stream=None) -> None:
+    lib = load_library()
+    rc = lib.bdlm_lm_head_commit(_ptr(hidden), _ptr(w), _ptr(mask), _ptr(denoising), int(B),
+                                 int(L), int(H), int(V), int(rule), int(k), float(threshold),
+                                 float(temperature), _ptr(tok_out), _ptr(conf_out),
+                                 _ptr(commit_out), _ptr(logits), _stream(stream))
+    _check("bdlm_lm_head_commit", rc)
 
 
 def bdlm_active_rows(mask, denoising, B: int, L: int, active_idx, n_active_dev,

@@ -10,7 +10,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libbdlm.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "attention.cu", "lm_head.cu", "commit.cu", "commit_noalloc.cu", "round.cu"]
+SOURCES = ["api.cu", "attention.cu", "lm_head.cu", "lm_conf.cu", "commit.cu", "commit_noalloc.cu",
+           "round.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]

@@ -112,6 +112,21 @@ int encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Workspace of the fused LM head + commit: gathered rows | partials | scored-row list | count.
+struct LmCommitLayout {
+  size_t off_part, off_act, off_n, total;
+};
+LmCommitLayout lm_commit_layout(const bdlm::LmConfPlan& plan, int rows) {
+  LmCommitLayout l;
+  l.off_part = align256(plan.gather_bytes);
+  l.off_act = l.off_part + align256(plan.part_bytes);
+  l.off_n = l.off_act + align256(static_cast<size_t>(rows) * sizeof(int32_t));
+  l.total = l.off_n + 256;
+  return l;
+}
+
 int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
                    const bdlm_bf16* k_pages, const bdlm_bf16* v_pages, const int32_t* page_table,
                    const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream,
@@ -421,6 +436,65 @@ int bdlm_write_block_kv(const bdlm_attn_desc* desc, const bdlm_bf16* k_new,
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 
+int bdlm_lm_head_commit(const bdlm_bf16* hidden, const bdlm_bf16* w, const uint8_t* mask,
+                        const uint8_t* denoising, int B, int L, int H, int V, int rule, int k,
+                        float threshold, float temperature, int32_t* tok_out, float* conf_out,
+                        uint8_t* commit_out, bdlm_bf16* logits, bdlm_stream stream) {
+  if (B < 0 || L < 1 || L > 64 || H < 8 || V < 8 || H % 8 != 0 || V % 8 != 0)
+    return BDLM_ERR_INVALID;
+  if (!(temperature > 0.f) || !isfinite(temperature)) return BDLM_ERR_INVALID;
+  if (rule < BDLM_COMMIT_THRESHOLD || rule > BDLM_COMMIT_ANTI_SEQUENTIAL) return BDLM_ERR_INVALID;
+  if (rule == BDLM_COMMIT_THRESHOLD && !(threshold >= 0.f && threshold <= 1.f))
+    return BDLM_ERR_INVALID;
+  if (rule != BDLM_COMMIT_THRESHOLD && k < 1) return BDLM_ERR_INVALID;
+  if (B == 0) return BDLM_OK;
+  if (!hidden || !w || !mask || !tok_out || !conf_out || !commit_out) return BDLM_ERR_INVALID;
+  if (!aligned16(hidden) || !aligned16(w) || (logits && !aligned16(logits)))
+    return BDLM_ERR_INVALID;
+  const long long R = static_cast<long long>(B) * L;
+  if (R > 0x7FFFFFFFll || R * V > (1ll << 40)) return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  if ((rc = get_encoder())) return rc;
+  const int rows = static_cast<int>(R);
+  const bdlm::LmConfPlan plan = bdlm::plan_lm_conf(rows, H, V, st->num_sms);
+  if (plan.max_row_tiles > plan.grid) return BDLM_ERR_UNSUPPORTED;
+  const LmCommitLayout lay = lm_commit_layout(plan, rows);
+  rc = ensure(&st->data, &st->data_cap, lay.total, false);
+  if (rc) return rc;
+  uint8_t* base = static_cast<uint8_t*>(st->data);
+  uint16_t* gathered = reinterpret_cast<uint16_t*>(base);
+  bdlm::CommitPartial* part = reinterpret_cast<bdlm::CommitPartial*>(base + lay.off_part);
+  int32_t* act = reinterpret_cast<int32_t*>(base + lay.off_act);
+  int32_t* n_act = reinterpret_cast<int32_t*>(base + lay.off_n);
+  CUtensorMap tm_w, tm_h;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(V)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, 128};
+    if ((rc = encode(&tm_w, w, 2, dims, strides, box))) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, 128};
+    if ((rc = encode(&tm_h, gathered, 2, dims, strides, box))) return rc;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = bdlm::launch_active_rows(mask, denoising, B, L, act, n_act, s);
+  if (e == cudaSuccess)
+    e = bdlm::launch_gather_rows(hidden, act, rows, n_act, rows, H, gathered, st->err, s);
+  if (e == cudaSuccess)
+    e = bdlm::launch_lm_conf(tm_w, tm_h, act, n_act, rows, rows, H, V, temperature, logits, part,
+                             plan, st->err, s);
+  if (e == cudaSuccess)
+    e = bdlm::launch_lm_commit_finalize(mask, denoising, B, L, part, plan, temperature, rule, k,
+                                        threshold, tok_out, conf_out, commit_out, s);
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------ device-side round loop
@@ -429,8 +503,8 @@ struct bdlm_round_loop {
   int device = 0;
   void* scratch = nullptr;
   bdlm_bf16 *q_w = nullptr, *k_w = nullptr, *v_w = nullptr, *h_w = nullptr;
-  bdlm_bf16 *attn_out = nullptr, *logits = nullptr;
-  int32_t *act = nullptr, *n_act = nullptr, *tok = nullptr;
+  bdlm_bf16* attn_out = nullptr;
+  int32_t* tok = nullptr;
   float* conf = nullptr;
   uint8_t* com = nullptr;
   int* step = nullptr;
@@ -441,8 +515,6 @@ struct bdlm_round_loop {
 };
 
 namespace {
-
-size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
 // Sizes the library workspaces for one round of the loop (nothing may be allocated while the
 // round is being captured).
@@ -455,11 +527,12 @@ int reserve_round(const bdlm_round_loop_desc& d) {
   const AttnPlan ap = bdlm::plan_attention(a.B, a.L, a.Hq, a.Hkv, a.max_pages_per_seq,
                                            a.page_size, st->num_sms);
   if (ap.n_mma == 0) return BDLM_ERR_UNSUPPORTED;
-  const CommitPlan cp = bdlm::plan_commit(a.B, a.L, d.V, st->num_sms);
-  const LmHeadPlan lp = bdlm::plan_lm_head(a.B * a.L, d.H, d.V, st->num_sms);
+  const int R = a.B * a.L;
+  const bdlm::LmConfPlan cp = bdlm::plan_lm_conf(R, d.H, d.V, st->num_sms);
+  if (cp.max_row_tiles > cp.grid) return BDLM_ERR_UNSUPPORTED;
   size_t data = ap.part_bytes;
-  if (cp.part_bytes > data) data = cp.part_bytes;
-  if (lp.gather_bytes > data) data = lp.gather_bytes;
+  const size_t fused = lm_commit_layout(cp, R).total;
+  if (fused > data) data = fused;
   if ((rc = ensure(reinterpret_cast<void**>(&st->attn_cnt), &st->attn_cnt_cap, ap.cnt_bytes,
                    true)))
     return rc;
@@ -530,12 +603,9 @@ int capture_round_loop(bdlm_round_loop* lp) {
                                     d.prefix_lens, s);
   if (!r2) r2 = bdlm_block_attention(&a, lp->q_w, d.k_pages, d.v_pages, d.page_table,
                                      d.prefix_lens, a.L, lp->attn_out, s);
-  if (!r2) r2 = bdlm_active_rows(d.mask, d.denoising, a.B, a.L, lp->act, lp->n_act, s);
-  if (!r2) r2 = bdlm_lm_head_device_count(lp->h_w, d.w, lp->act, lp->n_act, R, R, d.H, d.V,
-                                          lp->logits, s);
-  if (!r2) r2 = bdlm_confidence_commit_rule(lp->logits, d.mask, a.B, a.L, d.V, d.rule, d.k,
-                                            d.threshold, d.temperature, lp->tok, lp->conf,
-                                            lp->com, s);
+  if (!r2) r2 = bdlm_lm_head_commit(lp->h_w, d.w, d.mask, d.denoising, a.B, a.L, d.H, d.V, d.rule,
+                                    d.k, d.threshold, d.temperature, lp->tok, lp->conf, lp->com,
+                                    nullptr, s);
   if (!r2 && bdlm::launch_record_step(lp->step, d.steps, R, lp->tok, lp->conf, lp->com,
                                       d.tok_steps, d.conf_steps, d.commit_steps,
                                       lp->cap) != cudaSuccess)
@@ -577,12 +647,12 @@ int bdlm_round_loop_create(const bdlm_round_loop_desc* desc, bdlm_round_loop** o
   auto* lp = new bdlm_round_loop();
   lp->d = d;
   cudaGetDevice(&lp->device);
-  // owned scratch: one step's inputs, the attention output, the logits, the active rows,
-  // this step's tok/conf/commit and the step counter
+  // owned scratch: one step's inputs, the attention output, this step's tok/conf/commit and
+  // the step counter (the logits never leave the fused LM head)
   const size_t q_b = align256(R * a.Hq * a.D * 2), kv_b = align256(R * a.Hkv * a.D * 2);
-  const size_t h_b = align256(R * d.H * 2), lg_b = align256(R * d.V * 2);
+  const size_t h_b = align256(R * d.H * 2);
   const size_t r4 = align256(R * 4), r1 = align256(R);
-  const size_t total = 2 * q_b + 2 * kv_b + h_b + lg_b + 3 * r4 + r1 + 2 * 256;
+  const size_t total = 2 * q_b + 2 * kv_b + h_b + 2 * r4 + r1 + 256;
   if (cudaMalloc(&lp->scratch, total) != cudaSuccess) {
     delete lp;
     return BDLM_ERR_NOMEM;
@@ -593,12 +663,9 @@ int bdlm_round_loop_create(const bdlm_round_loop_desc* desc, bdlm_round_loop** o
   lp->k_w = reinterpret_cast<bdlm_bf16*>(p);      p += kv_b;
   lp->v_w = reinterpret_cast<bdlm_bf16*>(p);      p += kv_b;
   lp->h_w = reinterpret_cast<bdlm_bf16*>(p);      p += h_b;
-  lp->logits = reinterpret_cast<bdlm_bf16*>(p);   p += lg_b;
-  lp->act = reinterpret_cast<int32_t*>(p);        p += r4;
   lp->tok = reinterpret_cast<int32_t*>(p);        p += r4;
   lp->conf = reinterpret_cast<float*>(p);         p += r4;
   lp->com = p;                                    p += r1;
-  lp->n_act = reinterpret_cast<int32_t*>(p);      p += 256;
   lp->step = reinterpret_cast<int*>(p);
   if (cudaStreamCreateWithFlags(&lp->cap, cudaStreamNonBlocking) != cudaSuccess) {
     cudaFree(lp->scratch);

@@ -20,6 +20,7 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include "confidence.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -33,90 +34,6 @@ constexpr int kChunkBytes = 4096;     // bytes per stage
 constexpr int kChunk = kChunkBytes / 2;
 constexpr int kUnroll = 4;            // 16-byte vectors per lane per group of 32 logits
 constexpr int kMaskSmem = 8192;       // masks of up to this many rows are copied to smem
-
-struct Acc {
-  float m;    // running max (raw logit)
-  float s;    // sum of 2^((x - m) * c)
-  int idx;    // first index of the max
-};
-
-// 2^x with the SFU's approximate base-2 exponential (relative error about 2^-22).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ Acc merge(Acc a, Acc b, float c) {
-  if (b.m == -CUDART_INF_F) return a;
-  if (a.m == -CUDART_INF_F) return b;
-  Acc o;
-  o.m = fmaxf(a.m, b.m);
-  o.s = a.s * ex2((a.m - o.m) * c) + b.s * ex2((b.m - o.m) * c);
-  const int ia = (a.m == o.m) ? a.idx : 0x7FFFFFFF;
-  const int ib = (b.m == o.m) ? b.idx : 0x7FFFFFFF;
-  o.idx = min(ia, ib);
-  return o;
-}
-
-constexpr uint32_t kBf16NegInfPair = 0xFF80FF80u;
-
-// Max of the 32 logits held as 16 packed bf16 pairs (a tree of packed maxima).
-__device__ __forceinline__ float group_max(const uint32_t (&w)[16]) {
-  __nv_bfloat162 m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    m[i] = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w[2 * i]),
-                   *reinterpret_cast<const __nv_bfloat162*>(&w[2 * i + 1]));
-#pragma unroll
-  for (int n = 4; n > 0; n >>= 1)
-#pragma unroll
-    for (int i = 0; i < n; ++i) m[i] = __hmax2(m[2 * i], m[2 * i + 1]);
-  return fmaxf(__low2float(m[0]), __high2float(m[0]));
-}
-
-// 2^x for a pair (x <= 0) on the FMA pipe, so that part of the exponentials bypass the SFU,
-// in packed two-wide fp32 instructions: x = j + f with j = round(x) and f in [-1/2, 1/2];
-// 2^f from a degree-5 polynomial fitted here to the relative error on that interval (max
-// relative error about 2.3e-7 in fp32 Horner form); 2^j is added to the exponent bits.  x is
-// clamped at -125 so 2^j stays a normal number.
-__device__ __forceinline__ float2 exp2_fma2(float2 x) {
-  x.x = fmaxf(x.x, -125.0f);
-  x.y = fmaxf(x.y, -125.0f);
-  const float2 magic = make_float2(12582912.0f, 12582912.0f);
-  const float2 t = __fadd2_rn(x, magic);
-  const float2 f = __fadd2_rn(x, __fadd2_rn(magic, make_float2(-t.x, -t.y)));
-  float2 q = make_float2(1.3276466634124517e-3f, 1.3276466634124517e-3f);
-  q = __ffma2_rn(q, f, make_float2(9.675540961325169e-3f, 9.675540961325169e-3f));
-  q = __ffma2_rn(q, f, make_float2(5.550713464617729e-2f, 5.550713464617729e-2f));
-  q = __ffma2_rn(q, f, make_float2(2.4022120237350464e-1f, 2.4022120237350464e-1f));
-  q = __ffma2_rn(q, f, make_float2(6.931469440460205e-1f, 6.931469440460205e-1f));
-  q = __ffma2_rn(q, f, make_float2(1.0000001192092896f, 1.0000001192092896f));
-  return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
-                     __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
-}
-
-// Which of the 16 logit pairs of a group take their exponentials on the FMA pipe (bit i set:
-// pair i) rather than on the SFU.
-constexpr uint32_t kPolyPairs = 0x0000u;
-
-// Sum of 2^(x c - mc) over the 32 logits: the scaling runs two logits per packed FMA, the
-// exponentials are independent (pairs selected by kPolyPairs on the FMA pipe), and the sum is
-// a tree of packed adds.
-__device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], float c, float mc) {
-  const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
-  float2 e[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 y = __ffma2_rn(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), cc, nm);
-    e[i] = ((kPolyPairs >> i) & 1u) ? exp2_fma2(y) : make_float2(ex2(y.x), ex2(y.y));
-  }
-#pragma unroll
-  for (int step = 1; step < 16; step <<= 1)
-#pragma unroll
-    for (int i = 0; i < 16; i += 2 * step) e[i] = __fadd2_rn(e[i], e[i + step]);
-  return e[0].x + e[0].y;
-}
 
 // A lane's running state over one row segment.  The position of the max is found lazily:
 // when a group of 32 logits raises the max, the lane keeps a copy of that group (its 16
@@ -175,22 +92,6 @@ __device__ __forceinline__ Acc lane_result(const LaneAcc& a) {
     }
   }
   return Acc{a.m, a.s, idx};
-}
-
-__device__ __forceinline__ float bf16f(uint16_t h) {
-  return __uint_as_float(static_cast<uint32_t>(h) << 16);
-}
-
-__device__ __forceinline__ Acc warp_merge(Acc a, float c) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    Acc o;
-    o.m = __shfl_xor_sync(0xffffffffu, a.m, off);
-    o.s = __shfl_xor_sync(0xffffffffu, a.s, off);
-    o.idx = __shfl_xor_sync(0xffffffffu, a.idx, off);
-    a = merge(a, o, c);
-  }
-  return a;
 }
 
 struct ChunkMeta {
@@ -505,47 +406,10 @@ commit_finalize_kernel(const CommitArgs a, int stream_grid) {
   }
   __syncthreads();
   if (tid == 0) {
+    uint64_t cand = 0;
+    for (int i = 0; i < L; ++i) cand |= static_cast<uint64_t>(mk[i] != 0) << i;
+    const uint64_t sel = decide_block(a.rule, a.k, a.threshold, L, cand, s_conf);
     uint8_t* co = a.commit_out + static_cast<size_t>(b) * L;
-    uint64_t sel = 0;  // bit i: commit position i
-    int n_masked = 0;
-    for (int i = 0; i < L; ++i) n_masked += mk[i] != 0;
-    if (a.rule == BDLM_COMMIT_THRESHOLD) {
-      int best = -1;
-      float best_c = 0.f;
-      for (int i = 0; i < L; ++i) {
-        if (!mk[i]) continue;
-        const float ci = s_conf[i];
-        if (ci >= a.threshold) sel |= 1ull << i;
-        if (best < 0 || ci > best_c) {
-          best = i;
-          best_c = ci;
-        }
-      }
-      if (n_masked && !sel) sel = 1ull << best;  // at least the most confident position
-    } else if (a.rule == BDLM_COMMIT_TOPK) {
-      const int n = min(a.k, n_masked);
-      for (int c = 0; c < n; ++c) {  // the most confident position not yet chosen
-        int best = -1;
-        float best_c = 0.f;
-        for (int i = 0; i < L; ++i) {
-          if (!mk[i] || ((sel >> i) & 1)) continue;
-          if (best < 0 || s_conf[i] > best_c) {
-            best = i;
-            best_c = s_conf[i];
-          }
-        }
-        sel |= 1ull << best;
-      }
-    } else {
-      const bool left = a.rule == BDLM_COMMIT_SEQUENTIAL;
-      int n = min(a.k, n_masked);
-      for (int j = 0; j < L && n > 0; ++j) {
-        const int i = left ? j : L - 1 - j;
-        if (!mk[i]) continue;
-        sel |= 1ull << i;
-        --n;
-      }
-    }
     for (int i = 0; i < L; ++i) co[i] = static_cast<uint8_t>((sel >> i) & 1);
   }
 }

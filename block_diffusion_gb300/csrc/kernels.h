@@ -99,6 +99,32 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            uint16_t* logits, const LmHeadPlan& plan, int* err,
                            cudaStream_t stream);
 
+// LM head fused with the confidence step: partials of (max, sum of exponentials, first
+// argmax) per (active row, slot); a per-block kernel merges them and decides the commit.
+struct LmConfPlan {
+  int grid = 0;            // persistent CTAs (one per SM)
+  int slots = 0;           // partial slots per active row
+  int m_tiles = 0;         // vocabulary tiles of 256
+  int max_row_tiles = 0;   // row tiles of 256 at the planned maximum of active rows
+  size_t smem_bytes = 0;
+  size_t gather_bytes = 0;
+  size_t part_bytes = 0;
+};
+
+LmConfPlan plan_lm_conf(int max_rows, int H, int V, int num_sms);
+cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
+                           const int32_t* active_idx, const int32_t* n_active_dev, int max_rows,
+                           int n_rows, int H, int V, float temperature, uint16_t* logits,
+                           CommitPartial* part, const LmConfPlan& plan, int* err,
+                           cudaStream_t stream);
+// One CTA per block: tok/conf of the block's scored positions (masked, and in a denoising
+// sequence when `denoising` is given) from their partials, then the block's commit.
+cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denoising, int B, int L,
+                                      const CommitPartial* part, const LmConfPlan& plan,
+                                      float temperature, int rule, int k, float threshold,
+                                      int32_t* tok_out, float* conf_out, uint8_t* commit_out,
+                                      cudaStream_t stream);
+
 // Prompt block j of sequence b -> attention sequence b * nb + j with prefix prefix[b] + j * L.
 cudaError_t launch_prompt_prefix(const int32_t* prefix_lens, int B, int nb, int L, int32_t* out,
                                  cudaStream_t stream);

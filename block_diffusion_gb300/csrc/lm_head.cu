@@ -30,21 +30,13 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "lm_common.cuh"
 #include "ptx.cuh"
 
 namespace bdlm {
 namespace {
 
-constexpr int kBM = 128;         // vocabulary rows per UMMA (one sub-tile)
-constexpr int kSub = 2;          // sub-tiles per CTA tile (256 vocabulary rows)
-constexpr int kBK = 64;          // K per stage (one 128-byte swizzle atom)
-constexpr int kWBox = kBM * kBK * 2;       // 16 KB: one W box
-constexpr int kWBytes = kSub * kWBox;      // 32 KB of W per stage
-constexpr uint32_t kTmemCols = 512;
-constexpr int kEpiWarps = 16;   // a multiple of 4: kEpiWarps / 4 per tensor-memory lane quadrant
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kRowWarp = 2 + kEpiWarps;   // producer of the gathered-row ring
-constexpr int kThreads = (kRowWarp + 1) * 32;
+using namespace lm;
 
 // Per largest tile width: W stages of 32 KB, row stages of BN_MAX x 128 B (225 KB of shared
 // memory in each case), and the tensor-memory columns of one sub-tile accumulator (kCols)
@@ -86,18 +78,6 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ hidden,
   for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < nv; v += gridDim.x * blockDim.x)
     dst[v] = bad ? make_uint4(0, 0, 0, 0) : __ldg(src + v);
 }
-
-// One ring of TMA stages: `n` slots, the slot and phase of the next use.
-struct RingPos {
-  int slot = 0;
-  uint32_t phase = 0;
-  __device__ void advance(int n) {
-    if (++slot == n) {
-      slot = 0;
-      phase ^= 1;
-    }
-  }
-};
 
 // Producer of one ring: loads box (kb * kBK, row0(t)) of `tm` (`box_bytes` each) into slots
 // STRIDE bytes apart, for every tile and K step.  After a timeout it waits (bounded) for the

@@ -255,6 +255,37 @@ int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uint8_t* mask,
                                    float* conf_out, uint8_t* commit_out, bdlm_stream stream);
 
 /*
+ * Selective LM head fused with the confidence and commit step: the logits of a step's scored
+ * rows are reduced to (token, confidence) as they leave the tensor cores, so they never have
+ * to be stored and read back.
+ * Source: JetEngine notes, "ModelRunner" (selective logits for DENOISING sequences),
+ * "Optimization History" (opt23: LM head only on masked rows) and "Remaining Optimization
+ * Avenues" (a fused postprocess kernel); the rules as bdlm_confidence_commit_rule.
+ *
+ * Scored rows: r = b*L + i with mask[r] != 0 and (denoising NULL or denoising[b] != 0), the
+ * rows bdlm_active_rows lists.  For each scored row the results are those of
+ *     bdlm_lm_head (hidden, w, scored rows) followed by bdlm_confidence_commit_rule (rule, k,
+ *     threshold, temperature) over those bf16 logits,
+ * with `mask` restricted to the scored rows: tok_out is the argmax of the row's bf16-rounded
+ * logits (lowest index on ties), conf_out its max probability (the same value up to float32
+ * summation order), and each block commits among its scored positions by the rule.  Positions
+ * that are not scored (unmasked, or in a SAVING sequence) get tok_out = -1, conf_out = -inf,
+ * commit_out = 0.
+ *
+ * Layouts: hidden [B*L, H] bf16 (row b*L+i); w [V, H] bf16; mask [B, L] uint8; denoising [B]
+ * uint8 or NULL; tok_out [B, L] int32; conf_out [B, L] float; commit_out [B, L] uint8; logits
+ * [B*L, V] bf16 or NULL: when given, the scored rows' logits are stored as bdlm_lm_head would
+ * store them (other rows untouched).  H % 8 == 0, V % 8 == 0, 1 <= L <= 64,
+ * B*L <= 256 * (SM count); temperature > 0; 0 <= threshold <= 1 for the threshold rule,
+ * k >= 1 for the others.  Scratch (the scored-row list, gathered rows, partials) comes from the
+ * library workspace.
+ */
+int bdlm_lm_head_commit(const bdlm_bf16* hidden, const bdlm_bf16* w, const uint8_t* mask,
+                        const uint8_t* denoising, int B, int L, int H, int V, int rule, int k,
+                        float threshold, float temperature, int32_t* tok_out, float* conf_out,
+                        uint8_t* commit_out, bdlm_bf16* logits, bdlm_stream stream);
+
+/*
  * Mask update between denoising steps: mask[i] = 0 wherever commit[i] != 0.
  * Source: JetEngine notes, "Important Patterns" (each denoising step moves positions from
  * masked to unmasked).  mask, commit: [n] uint8.  n == 0 is a no-op.
@@ -272,17 +303,16 @@ int bdlm_apply_commit(uint8_t* mask, const uint8_t* commit, int n, bdlm_stream s
  *   the step's inputs: slice s of q_steps [S, B, L, Hq, D], k_new_steps / v_new_steps
  *   [S, B, L, Hkv, D] and hidden_steps [S, B*L, H] (the model's outputs for that step, which
  *   this library does not compute) -> bdlm_write_block_kv (the block's K/V into the cache)
- *   -> bdlm_block_attention -> bdlm_active_rows (mask, denoising) ->
- *   bdlm_lm_head_device_count -> bdlm_confidence_commit_rule (rule, k, threshold,
- *   temperature) -> tok/conf/commit stored into slice s of tok_steps, conf_steps,
- *   commit_steps [S, B, L] -> bdlm_apply_commit on mask.
+ *   -> bdlm_block_attention -> bdlm_lm_head_commit (mask, denoising, rule, k, threshold,
+ *   temperature; no logits stored) -> tok/conf/commit stored into slice s of tok_steps,
+ *   conf_steps, commit_steps [S, B, L] -> bdlm_apply_commit on mask.
  * After the last round *steps_done holds the number of rounds run, and slices at or past it
  * are untouched.  The attention output is kept in the loop's own scratch (a model would feed
  * it to its next layer).
  *
  * All pointers are device pointers owned by the caller and must stay valid while the loop
  * exists.  bdlm_round_loop_create allocates the loop's scratch (one step's inputs, the
- * attention output, the [B*L, V] logits, small per-row arrays) and captures the graph; it sizes
+ * attention output, small per-row arrays) and captures the graph; it sizes
  * the library workspace first, since nothing may be allocated inside the capture.  If a later
  * call grows or releases the library workspace, the next launch captures the graph again.
  * Shapes and limits as the calls it is made of.

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 class Case:
     def __init__(self, seed, B=12, L=4, Hq=8, Hkv=4, H=512, V=4104, S=4, frac=0.75,
-                 prefix=(40, 400)):
+                 prefix=(40, 400), saving_masked=False):
         import torch
         rng = np.random.default_rng(seed)
         self.B, self.L, self.Hq, self.Hkv, self.H, self.V, self.S = B, L, Hq, Hkv, H, V, S
@@ -26,7 +26,8 @@ class Case:
         self.mask0 = W.make_mask_fixed_fraction(rng, B, L, frac)
         self.mask0[1] = 0                               # a block with nothing to do
         self.den = W.denoising_sequences(rng, B, 0.75)
-        self.mask0[self.den == 0] = 0                   # SAVING sequences have no masked slot
+        if not saving_masked:
+            self.mask0[self.den == 0] = 0               # SAVING sequences have no masked slot
         self.k0, self.v0 = bf16_tensor(self.a.k_ref), bf16_tensor(self.a.v_ref)
         self.pt, self.pl = dev(self.a.page_table_ref), dev(self.a.prefix_lens)
         self.torch = torch
@@ -78,12 +79,8 @@ def run_eager(lib, c, rule, k, thr):
     torch = c.torch
     kp, vp = c.k0.clone(), c.v0.clone()
     mask = dev(c.mask0)
-    R = c.B * c.L
     den = dev(c.den)
     out = torch.empty((c.B, c.L, c.Hq, 128), dtype=torch.bfloat16, device="cuda")
-    logits = torch.empty((R, c.V), dtype=torch.bfloat16, device="cuda")
-    act = torch.empty((R,), dtype=torch.int32, device="cuda")
-    n = torch.empty((1,), dtype=torch.int32, device="cuda")
     tok = torch.empty((c.B, c.L), dtype=torch.int32, device="cuda")
     conf = torch.empty((c.B, c.L), dtype=torch.float32, device="cuda")
     com = torch.empty((c.B, c.L), dtype=torch.uint8, device="cuda")
@@ -91,11 +88,9 @@ def run_eager(lib, c, rule, k, thr):
     for s in range(c.S):
         lib.bdlm_write_block_kv(c.desc(lib), c.kn[s], c.vn[s], kp, vp, c.pt, c.pl)
         lib.bdlm_block_attention(c.desc(lib), c.q[s], kp, vp, c.pt, c.pl, c.L, out)
-        lib.bdlm_active_rows(mask, den, c.B, c.L, act, n)
-        lib.bdlm_lm_head_device_count(c.hid[s], c.w, act, n, R, R, c.H, c.V, logits)
-        lib.bdlm_confidence_commit_rule(logits, mask, c.B, c.L, c.V, rule, k, thr, 1.0, tok,
-                                        conf, com)
-        lib.bdlm_apply_commit(mask, com, R)
+        lib.bdlm_lm_head_commit(c.hid[s], c.w, mask, den, c.B, c.L, c.H, c.V, rule, k, thr,
+                                1.0, tok, conf, com)
+        lib.bdlm_apply_commit(mask, com, c.B * c.L)
         torch.cuda.synchronize()
         steps.append((host(tok), host(conf), host(com)))
         if host(mask).sum() == 0:
@@ -130,3 +125,21 @@ def test_loop_stops_early_and_relaunches(lib):
         assert np.array_equal(x, y)
     assert first[3] == again[3]
     assert np.array_equal(first[4], again[4])
+
+
+def test_masked_positions_of_saving_sequences_are_not_scored(lib):
+    """Masked positions of SAVING sequences are never scored or committed: the loop runs every
+    step slot, in step with the host-driven round, and leaves them masked."""
+    c = Case(seed=19, S=3, saving_masked=True)
+    assert (c.mask0[c.den == 0] != 0).any()
+    tok, conf, com, done, mask, kp, vp = run_loop(lib, c, 0, 1, 0.6)
+    steps, mask_e, kp_e, vp_e = run_eager(lib, c, 0, 1, 0.6)
+    assert done == c.S == len(steps)
+    for s, (t, f, m) in enumerate(steps):
+        assert np.array_equal(tok[s], t) and np.array_equal(com[s], m)
+        assert np.array_equal(conf[s], f)
+        saving = c.den == 0
+        assert np.all(t[saving] == -1) and np.all(m[saving] == 0)
+    assert np.array_equal(mask, mask_e)
+    assert np.array_equal(mask[c.den == 0], c.mask0[c.den == 0])
+    assert c.torch.equal(kp, kp_e) and c.torch.equal(vp, vp_e)
