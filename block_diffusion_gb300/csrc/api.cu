@@ -483,9 +483,8 @@ int bdlm_lm_head_commit(const bdlm_bf16* hidden, const bdlm_bf16* w, const uint8
     if ((rc = encode(&tm_h, gathered, 2, dims, strides, box))) return rc;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = bdlm::launch_active_rows(mask, denoising, B, L, act, n_act, s);
-  if (e == cudaSuccess)
-    e = bdlm::launch_gather_rows(hidden, act, rows, n_act, rows, H, gathered, st->err, s);
+  cudaError_t e = bdlm::launch_scored_gather(hidden, mask, denoising, B, L, H, gathered, act,
+                                             n_act, s);
   if (e == cudaSuccess)
     e = bdlm::launch_lm_conf(tm_w, tm_h, act, n_act, rows, rows, H, V, temperature, logits, part,
                              plan, st->err, s);

@@ -777,30 +777,44 @@ attn_order_kernel(const int32_t* __restrict__ prefix_lens, int B, int L, long lo
 // One warp per (group, query row): lane s fetches split s's (m, l), the weights come from
 // warp shuffles, and each lane then sums a float4 of head dims over the splits with
 // independent loads (two round trips to memory in all).
-// Grid: x = group (sequence, KV head, row group), y = blocks of 8 query rows; 32-bit index
-// math only (the kernel is issue-bound when every warp decomposes a 64-bit index).
+// Grid: x = group (sequence, KV head, row group), y = blocks of 8 warps x kMergeRows query
+// rows; 32-bit index math only (the kernel is issue-bound when every warp decomposes a 64-bit
+// index).  A warp merges kMergeRows rows of one group at once, so the loads of both rows are in
+// flight together and the grid fits the GPU in one wave.
+constexpr int kMergeRows = 2;
+
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const AttnParams p, int N) {
   const int lane = threadIdx.x & 31;
   griddep_wait();
   griddep_launch_dependents();
-  const int n = static_cast<int>(blockIdx.y) * 8 + (threadIdx.x >> 5);
-  if (n >= p.rows_per_group) return;
+  const int n0 = (static_cast<int>(blockIdx.y) * 8 + (threadIdx.x >> 5)) * kMergeRows;
+  if (n0 >= p.rows_per_group) return;
   const unsigned grp = blockIdx.x;
   const int rg = static_cast<int>(grp % static_cast<unsigned>(p.row_groups));
   const unsigned bk = grp / static_cast<unsigned>(p.row_groups);
   const int kvh = static_cast<int>(bk % static_cast<unsigned>(p.Hkv));
   const int b = static_cast<int>(bk / static_cast<unsigned>(p.Hkv));
-  const int i = rg * p.lsub + n / p.G;
-  if (i >= p.L) return;
+  bool valid[kMergeRows];
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+    const int n = n0 + r;
+    valid[r] = n < p.rows_per_group && rg * p.lsub + n / p.G < p.L;
+  }
+  if (!valid[0]) return;   // rows of a group are in block order: no later row is valid either
   const size_t unit = static_cast<size_t>(N) * 130;
   const float* all = p.part + static_cast<size_t>(grp) * p.max_splits * unit;
-  // lane s fetches split s's (m, l) together with the prefix length (slots of splits that
-  // turn out not to exist are ignored), so the split count costs no extra round trip
-  float ml = -CUDART_INF_F, ll = 0.f;
-  if (lane < p.max_splits && lane < 32) {
-    ml = __ldcg(all + lane * unit + N * 128 + n);
-    ll = __ldcg(all + lane * unit + N * 128 + N + n);
+  // lane s fetches split s's (m, l) of each row together with the prefix length (slots of
+  // splits that turn out not to exist are ignored), so the split count costs no extra round trip
+  float ml[kMergeRows], ll[kMergeRows];
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+    ml[r] = -CUDART_INF_F;
+    ll[r] = 0.f;
+    if (valid[r] && lane < p.max_splits) {
+      ml[r] = __ldcg(all + lane * unit + N * 128 + n0 + r);
+      ll[r] = __ldcg(all + lane * unit + N * 128 + N + n0 + r);
+    }
   }
   const int prefix = p.prefix_lens[b];
   const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
@@ -808,69 +822,93 @@ attn_merge_kernel(const AttnParams p, int N) {
   if (kvl > max_tok) kvl = max_tok;
   const int ns = static_cast<int>((kvl + p.split_tokens - 1) / p.split_tokens);
   if (ns <= 1) return;
-  // the row's maximum and normaliser over all splits: lane s holds split s's (m, l); beyond
-  // 32 splits the lanes walk the list in steps of 32
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[kMergeRows];
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (ns <= 32) {
-    if (lane >= ns) {
-      ml = -CUDART_INF_F;
-      ll = 0.f;
+    // the rows' maxima and normalisers over all splits: lane s holds split s's (m, l)
+    float wl[kMergeRows];
+#pragma unroll
+    for (int r = 0; r < kMergeRows; ++r) {
+      if (lane >= ns) {
+        ml[r] = -CUDART_INF_F;
+        ll[r] = 0.f;
+      }
+      float M = ml[r];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float e = lane < ns ? exp2f((ml[r] - M) * p.scale_log2) : 0.f;
+      float den = e * ll[r];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      wl[r] = valid[r] ? e / den : 0.f;
     }
-    float M = ml;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float e = lane < ns ? exp2f((ml - M) * p.scale_log2) : 0.f;
-    float den = e * ll;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    const float wl = e / den;
 #pragma unroll 4
     for (int j = 0; j < ns; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, wl, j);
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(all + j * unit + n * 128) + lane);
-      acc.x += wj * o.x;
-      acc.y += wj * o.y;
-      acc.z += wj * o.z;
-      acc.w += wj * o.w;
+#pragma unroll
+      for (int r = 0; r < kMergeRows; ++r) {
+        const float wj = __shfl_sync(0xffffffffu, wl[r], j);
+        if (!valid[r]) continue;
+        const float4 o =
+            __ldcg(reinterpret_cast<const float4*>(all + j * unit + (n0 + r) * 128) + lane);
+        acc[r].x += wj * o.x;
+        acc[r].y += wj * o.y;
+        acc[r].z += wj * o.z;
+        acc[r].w += wj * o.w;
+      }
     }
   } else {
-    float M = -CUDART_INF_F;
-    for (int s0 = 0; s0 < ns; s0 += 32)
-      if (s0 + lane < ns) M = fmaxf(M, __ldcg(all + (s0 + lane) * unit + N * 128 + n));
+    // beyond 32 splits the lanes walk the list in steps of 32, one row at a time
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float den = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += 32)
-      if (s0 + lane < ns) {
-        const float* pm = all + (s0 + lane) * unit + N * 128;
-        den += exp2f((__ldcg(pm + n) - M) * p.scale_log2) * __ldcg(pm + N + n);
-      }
+    for (int r = 0; r < kMergeRows; ++r) {
+      if (!valid[r]) continue;
+      const int n = n0 + r;
+      float M = -CUDART_INF_F;
+      for (int s0 = 0; s0 < ns; s0 += 32)
+        if (s0 + lane < ns) M = fmaxf(M, __ldcg(all + (s0 + lane) * unit + N * 128 + n));
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    const float inv = 1.0f / den;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-      const int cnt = min(32, ns - s0);
-      float wl = 0.f;
-      if (lane < cnt)
-        wl = exp2f((__ldcg(all + (s0 + lane) * unit + N * 128 + n) - M) * p.scale_log2) * inv;
-      for (int j = 0; j < cnt; ++j) {
-        const float wj = __shfl_sync(0xffffffffu, wl, j);
-        const float4 o =
-            __ldcg(reinterpret_cast<const float4*>(all + (s0 + j) * unit + n * 128) + lane);
-        acc.x += wj * o.x;
-        acc.y += wj * o.y;
-        acc.z += wj * o.z;
-        acc.w += wj * o.w;
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float den = 0.f;
+      for (int s0 = 0; s0 < ns; s0 += 32)
+        if (s0 + lane < ns) {
+          const float* pm = all + (s0 + lane) * unit + N * 128;
+          den += exp2f((__ldcg(pm + n) - M) * p.scale_log2) * __ldcg(pm + N + n);
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      const float inv = 1.0f / den;
+      for (int s0 = 0; s0 < ns; s0 += 32) {
+        const int cnt = min(32, ns - s0);
+        float wl = 0.f;
+        if (lane < cnt)
+          wl = exp2f((__ldcg(all + (s0 + lane) * unit + N * 128 + n) - M) * p.scale_log2) * inv;
+        for (int j = 0; j < cnt; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, wl, j);
+          const float4 o =
+              __ldcg(reinterpret_cast<const float4*>(all + (s0 + j) * unit + n * 128) + lane);
+          acc[r].x += wj * o.x;
+          acc[r].y += wj * o.y;
+          acc[r].z += wj * o.z;
+          acc[r].w += wj * o.w;
+        }
       }
     }
   }
-  const size_t o = ((static_cast<size_t>(b) * p.L + i) * p.Hq + static_cast<size_t>(kvh) * p.G +
-                    n % p.G) * 128 + 4 * lane;
-  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
-                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
-  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
-                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-  *reinterpret_cast<uint2*>(p.out + o) = make_uint2(lo, hi);
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+    if (!valid[r]) continue;
+    const int n = n0 + r;
+    const int i = rg * p.lsub + n / p.G;
+    const size_t o = ((static_cast<size_t>(b) * p.L + i) * p.Hq + static_cast<size_t>(kvh) * p.G +
+                      n % p.G) * 128 + 4 * lane;
+    const uint32_t lo =
+        __bfloat16_as_ushort(__float2bfloat16_rn(acc[r].x)) |
+        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[r].y))) << 16);
+    const uint32_t hi =
+        __bfloat16_as_ushort(__float2bfloat16_rn(acc[r].z)) |
+        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[r].w))) << 16);
+    *reinterpret_cast<uint2*>(p.out + o) = make_uint2(lo, hi);
+  }
 }
 
 template <int N, int STAGES>
@@ -1016,7 +1054,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   }
   if (e != cudaSuccess || plan.max_splits <= 1) return e;
   const long long groups = static_cast<long long>(B) * Hkv * plan.row_groups;
-  const int row_blocks = (plan.G * plan.lsub + 7) / 8;
+  const int row_blocks = (plan.G * plan.lsub + 8 * kMergeRows - 1) / (8 * kMergeRows);
   e = launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>(groups), row_blocks), dim3(256), 0,
                  stream, prm, plan.n_mma);
   if (e != cudaSuccess) return e;

@@ -103,7 +103,7 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
 // argmax) per (active row, slot); a per-block kernel merges them and decides the commit.
 struct LmConfPlan {
   int grid = 0;            // persistent CTAs (one per SM)
-  int slots = 0;           // partial slots per active row
+  int slots = 0;           // partial slots per active row (one per CTA)
   int m_tiles = 0;         // vocabulary tiles of 256
   int max_row_tiles = 0;   // row tiles of 256 at the planned maximum of active rows
   size_t smem_bytes = 0;
@@ -117,6 +117,12 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            int n_rows, int H, int V, float temperature, uint16_t* logits,
                            CommitPartial* part, const LmConfPlan& plan, int* err,
                            cudaStream_t stream);
+// The scored rows (masked, in a denoising sequence) listed in act / *n_act and their hidden
+// rows gathered, in one launch of B * L CTAs.
+cudaError_t launch_scored_gather(const uint16_t* hidden, const uint8_t* mask,
+                                 const uint8_t* denoising, int B, int L, int H,
+                                 uint16_t* gathered, int32_t* act, int32_t* n_act,
+                                 cudaStream_t stream);
 // One CTA per block: tok/conf of the block's scored positions (masked, and in a denoising
 // sequence when `denoising` is given) from their partials, then the block's commit.
 cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denoising, int B, int L,

@@ -36,8 +36,9 @@ using namespace lm;
 // Work split: with rt row tiles (256 active rows each), CTA c < (grid / rt) * rt keeps row tile
 // c % rt for its whole life and walks the vocabulary tiles c / rt, c / rt + grid / rt, ...; the
 // CTAs that run together hold the same W tiles for the different row tiles, so W streams from
-// HBM about once.  Each epilogue thread writes one partial per (row, CTA, column share) when
-// its CTA is done; a per-block kernel merges a row's partials.
+// HBM about once.  When its CTA is done, each row's four column shares are merged in shared
+// memory (the rings are idle by then) into one partial per (row, CTA); a per-block kernel
+// merges a row's partials.
 constexpr int kConfWS = 4, kConfHS = 3;     // W and row stages, 32 KB each
 constexpr int kConfN = kSub * kBM;          // vocabulary columns per tile (UMMA N)
 constexpr int kConfShares = kEpiWarps / 4;  // epilogue warps per tensor-memory lane quadrant
@@ -270,12 +271,31 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&acc_empty);   // tensor memory is free for the next tile's MMAs
     }
-    const int slot = (cta / max(rt, 1)) * kConfShares + share;
+    // the four shares of each row, merged in the (now idle) W ring: [share][sub-tile][row]
+    float* sh_m = reinterpret_cast<float*>(wring);
+    float* sh_s = sh_m + kConfShares * kSub * kBM;
+    int* sh_i = reinterpret_cast<int*>(sh_s + kConfShares * kSub * kBM);
 #pragma unroll
-    for (int s = 0; s < kSub; ++s)
-      if (arow[s] >= 0)
-        p.part[static_cast<size_t>(arow[s]) * p.slots + slot] =
-            CommitPartial{acc[s].m, acc[s].s, acc[s].idx, 0};
+    for (int s = 0; s < kSub; ++s) {
+      const int at = (share * kSub + s) * kBM + x;
+      sh_m[at] = acc[s].m;
+      sh_s[at] = acc[s].s;
+      sh_i[at] = acc[s].idx;
+    }
+    named_barrier(1, kEpiThreads);
+    if (share == 0) {
+      const int slot = cta / max(rt, 1);
+#pragma unroll
+      for (int s = 0; s < kSub; ++s) {
+        if (arow[s] < 0) continue;
+        Acc t = acc[s];
+        for (int o = 1; o < kConfShares; ++o) {
+          const int at = (o * kSub + s) * kBM + x;
+          t = merge(t, Acc{sh_m[at], sh_s[at], sh_i[at]}, p.c);
+        }
+        p.part[static_cast<size_t>(arow[s]) * p.slots + slot] = CommitPartial{t.m, t.s, t.idx, 0};
+      }
+    }
   }
 
   tc_fence_before();
@@ -294,6 +314,51 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
 size_t lm_conf_smem() { return 1024 + static_cast<size_t>(kConfWS + kConfHS) * kWBytes; }
 
+// ------------------------------------------------------------------ scored rows
+// Row r = b * L + i is scored when mask[r] != 0 and (den is null or den[b] != 0).  CTA r counts
+// the scored rows before r; if row r is scored it copies hidden[r] to gathered[idx] and records
+// act[idx] = r, idx being that count.  CTA 0 also writes the total to *n_act.  (The row list of
+// bdlm_active_rows and the gather of the LM head in one launch.)
+__global__ void __launch_bounds__(256)
+scored_gather_kernel(const uint16_t* __restrict__ hidden, const uint8_t* __restrict__ mask,
+                     const uint8_t* __restrict__ den, int R, int L, int H,
+                     uint16_t* __restrict__ gathered, int32_t* __restrict__ act,
+                     int32_t* __restrict__ n_act) {
+  __shared__ int s_warp[8];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int r = blockIdx.x;
+  auto is_scored = [&](int q) -> int {
+    return mask[q] != 0 && (den == nullptr || den[q / L] != 0);
+  };
+  const int mine = is_scored(r);
+  if (!mine && r != 0) return;
+  const int limit = r == 0 ? R : r;   // CTA 0 counts every row
+  int before = 0, total = 0;
+  for (int q = threadIdx.x; q < limit; q += blockDim.x) {
+    const int sc = is_scored(q);
+    total += sc;
+    before += q < r ? sc : 0;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, off);
+    total += __shfl_xor_sync(0xffffffffu, total, off);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (lane == 0) s_warp[warp] = r == 0 ? total : before;
+  __syncthreads();
+  int cnt = 0;
+  for (int w = 0; w < nw; ++w) cnt += s_warp[w];
+  if (r == 0 && threadIdx.x == 0) *n_act = cnt;
+  if (!mine) return;
+  const int idx = r == 0 ? 0 : cnt;
+  if (threadIdx.x == 0) act[idx] = r;
+  const uint4* src = reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(r) * H);
+  uint4* dst = reinterpret_cast<uint4*>(gathered + static_cast<size_t>(idx) * H);
+  for (int v = threadIdx.x; v < H / 8; v += blockDim.x) dst[v] = __ldg(src + v);
+}
+
 // ------------------------------------------------------------------ per-block finalize
 struct LmCommitArgs {
   const uint8_t* mask;
@@ -301,7 +366,7 @@ struct LmCommitArgs {
   int R, L;
   const CommitPartial* part; // [scored row][slots]
   int slots;                 // slots allocated per scored row
-  int lm_grid, shares;       // CTAs of the LM head launch, slots each CTA writes per row
+  int lm_grid, shares;       // CTAs of the LM head launch, partials each CTA writes per row
   float c, threshold;
   int rule, k;
   int32_t* tok_out;
@@ -405,7 +470,7 @@ lm_commit_finalize_kernel(const LmCommitArgs a) {
 LmConfPlan plan_lm_conf(int max_rows, int H, int V, int num_sms) {
   LmConfPlan pl;
   pl.grid = num_sms > 0 ? num_sms : 1;
-  pl.slots = pl.grid * kConfShares;
+  pl.slots = pl.grid;
   pl.m_tiles = (V + kConfN - 1) / kConfN;
   pl.max_row_tiles = (max_rows + kConfN - 1) / kConfN;
   pl.smem_bytes = lm_conf_smem();
@@ -444,6 +509,14 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                     tm_w, tm_h, prm);
 }
 
+cudaError_t launch_scored_gather(const uint16_t* hidden, const uint8_t* mask,
+                                 const uint8_t* denoising, int B, int L, int H,
+                                 uint16_t* gathered, int32_t* act, int32_t* n_act,
+                                 cudaStream_t stream) {
+  return launch_pdl(scored_gather_kernel, dim3(static_cast<unsigned>(B * L)), dim3(256), 0,
+                    stream, hidden, mask, denoising, B * L, L, H, gathered, act, n_act);
+}
+
 cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denoising, int B, int L,
                                       const CommitPartial* part, const LmConfPlan& plan,
                                       float temperature, int rule, int k, float threshold,
@@ -457,7 +530,7 @@ cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denois
   a.part = part;
   a.slots = plan.slots;
   a.lm_grid = plan.grid;
-  a.shares = plan.slots / plan.grid;
+  a.shares = 1;
   a.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   a.threshold = threshold;
   a.rule = rule;
