@@ -460,7 +460,7 @@ int bdlm_lm_head_commit(const bdlm_bf16* hidden, const bdlm_bf16* w, const uint8
   if ((rc = get_encoder())) return rc;
   const int rows = static_cast<int>(R);
   const bdlm::LmConfPlan plan = bdlm::plan_lm_conf(rows, H, V, st->num_sms);
-  if (plan.max_row_tiles > plan.grid) return BDLM_ERR_UNSUPPORTED;
+  if (plan.max_row_tiles > plan.units) return BDLM_ERR_UNSUPPORTED;
   const LmCommitLayout lay = lm_commit_layout(plan, rows);
   rc = ensure(&st->data, &st->data_cap, lay.total, false);
   if (rc) return rc;
@@ -528,7 +528,7 @@ int reserve_round(const bdlm_round_loop_desc& d) {
   if (ap.n_mma == 0) return BDLM_ERR_UNSUPPORTED;
   const int R = a.B * a.L;
   const bdlm::LmConfPlan cp = bdlm::plan_lm_conf(R, d.H, d.V, st->num_sms);
-  if (cp.max_row_tiles > cp.grid) return BDLM_ERR_UNSUPPORTED;
+  if (cp.max_row_tiles > cp.units) return BDLM_ERR_UNSUPPORTED;
   size_t data = ap.part_bytes;
   const size_t fused = lm_commit_layout(cp, R).total;
   if (fused > data) data = fused;

@@ -103,7 +103,9 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
 // argmax) per (active row, slot); a per-block kernel merges them and decides the commit.
 struct LmConfPlan {
   int grid = 0;            // persistent CTAs (one per SM)
-  int slots = 0;           // partial slots per active row (one per CTA)
+  int units = 0;           // workers: CTA pairs of the pair kernel, else CTAs
+  bool pair = false;       // the CTA-pair kernel (more than 128 rows planned)
+  int slots = 0;           // partial slots per active row (one per worker, at most)
   int m_tiles = 0;         // vocabulary tiles of 256
   int max_row_tiles = 0;   // row tiles of 256 at the planned maximum of active rows
   size_t smem_bytes = 0;

@@ -314,6 +314,300 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
 size_t lm_conf_smem() { return 1024 + static_cast<size_t>(kConfWS + kConfHS) * kWBytes; }
 
+// ------------------------------------------------------------------ CTA-pair variant
+// Above 128 scored rows the same GEMM runs on CTA pairs (clusters of two, tcgen05
+// cta_group::2): a pair tile is 256 scored rows (128 per CTA, the two halves of one M = 256
+// UMMA) by up to 256 vocabulary columns, and per K step each CTA stages its own 128 rows and
+// its half of the tile's W rows.  A CTA's accumulator is then 128 lanes x 256 columns, half
+// of tensor memory, so two tiles' accumulators alternate and the epilogue of one tile
+// overlaps the MMAs of the next (the single-CTA tile of 256 x 256 fills tensor memory and
+// must be drained first).  Shared-memory fill per MMA FLOP is that of the single-CTA kernel,
+// and each W tile is fetched once per pair.
+//
+// With rt row tiles, pair q < (pairs / rt) * rt keeps row tile q % rt and owns an equal,
+// contiguous share of the vocabulary (slot q / rt of pairs / rt, in units of 16 columns),
+// walked in tiles of 256 columns; the last tile is narrower (the UMMA's N is set per tile),
+// so every pair streams the same number of W bytes.  Each CTA writes one partial per (row,
+// pair).  The even CTA's W and row barriers count both CTAs' bytes; its MMA thread issues
+// every UMMA, and its commits release the stages and signal the accumulators in both CTAs.
+#ifndef BDLM_PAIR_KW
+#define BDLM_PAIR_KW 2
+#endif
+#ifndef BDLM_PAIR_KH
+#define BDLM_PAIR_KH 2
+#endif
+#ifndef BDLM_PAIR_WS
+#define BDLM_PAIR_WS 4
+#endif
+#ifndef BDLM_PAIR_HS
+#define BDLM_PAIR_HS 3
+#endif
+// 64-wide K boxes per W and per row stage: a W stage reads 128 * KW contiguous bytes of each
+// of its rows, which the memory system serves better than one box at a time.
+constexpr int kPairKW = BDLM_PAIR_KW, kPairKH = BDLM_PAIR_KH;
+constexpr int kPairWS = BDLM_PAIR_WS, kPairHS = BDLM_PAIR_HS;   // W and row stages
+constexpr int kPairWStage = kPairKW * kWBox, kPairHStage = kPairKH * kWBox;   // bytes per CTA
+static_assert(kPairKW % kPairKH == 0 || kPairKH % kPairKW == 0, "stage boxes must nest");
+constexpr uint32_t kPairCols = 256;              // tensor-memory columns per accumulator
+constexpr int kPairUnit = 16;                    // vocabulary columns per unit of work
+
+// The vocabulary share of one pair: units [u_lo, u_hi) of 16 columns, in tiles of 256.
+struct PairJobs {
+  int u_lo = 0, u_hi = 0, n_jobs = 0;
+  __device__ int col0(int j) const { return (u_lo + j * (kConfN / kPairUnit)) * kPairUnit; }
+  __device__ int width(int j) const {   // a multiple of 16, 16 .. 256
+    return min(kConfN, (u_hi - u_lo - j * (kConfN / kPairUnit)) * kPairUnit);
+  }
+};
+
+// Streams the stages of every job into a ring: W (rows of the tile's half) or the row tile.
+// The even CTA arms each stage's full barrier with both CTAs' bytes; both CTAs' copies
+// complete on that barrier.
+template <int NSTAGES, int KS, bool IS_W>
+__device__ void produce_pair(const CUtensorMap* tm, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                             bool leader, uint32_t rank, const PairJobs& jobs, int row_tile0,
+                             int k_boxes, int* abort_flag) {
+  constexpr int kStage = KS * kWBox;
+  const int k_stages = (k_boxes + KS - 1) / KS;
+  tma_prefetch_desc(tm);
+  RingPos pos;
+  bool ok = true;
+  for (int j = 0; j < jobs.n_jobs && ok; ++j) {
+    const int row0 = IS_W ? jobs.col0(j) + static_cast<int>(rank) * (jobs.width(j) >> 1)
+                          : row_tile0 + static_cast<int>(rank) * kBM;
+    for (int ks = 0; ks < k_stages; ++ks) {
+      if (!(ok = mbar_wait(&empty[pos.slot], pos.phase ^ 1, abort_flag))) break;
+      if (leader) mbar_arrive_expect_tx(&full[pos.slot], 2 * kStage);
+      const uint32_t bar = cluster_map(&full[pos.slot], 0);
+#pragma unroll
+      for (int b = 0; b < KS; ++b)   // boxes past the tensor read as zeros
+        tma_load_2d_pair(ring + pos.slot * kStage + b * kWBox, tm, bar, (ks * KS + b) * kBK,
+                         row0);
+      pos.advance(NSTAGES);
+    }
+  }
+  if (!ok) {
+    // after a failed wait: copies already issued land within microseconds; give them 200 us
+    // before this CTA may exit (the even CTA's barriers may never see the odd CTA's bytes)
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+lm_conf_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_h, const LmConfParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* wring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t* hring = wring + kPairWS * kPairWStage;
+  __shared__ uint64_t w_full[kPairWS], w_empty[kPairWS], h_full[kPairHS], h_empty[kPairHS];
+  __shared__ uint64_t acc_full[2], acc_empty[2], bar_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairWS; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 1);
+    }
+    for (int s = 0; s < kPairHS; ++s) {
+      mbar_init(&h_full[s], 1);
+      mbar_init(&h_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * kEpiWarps);   // one arrival per epilogue warp of each CTA
+    }
+    mbar_init(&bar_done, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();   // both CTAs' barriers exist before either CTA signals the other's
+  tc_fence_after();
+  griddep_wait();
+  const uint32_t tmem = tmem_base;
+  const int n_act = min(max(*p.n_active_dev, 0), p.n_active);
+  const int pairs = static_cast<int>(gridDim.x) >> 1;
+  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  const int rt = (n_act + kConfN - 1) / kConfN;           // row tiles of 256
+  const int per_tile = rt > 0 ? pairs / rt : 0;           // pairs per row tile
+  const bool working = rt > 0 && pair < per_tile * rt;
+  const int n = working ? pair % rt : 0;
+  const int slot = working ? pair / rt : 0;
+  PairJobs jobs;
+  if (working) {
+    const long long units = (p.V + kPairUnit - 1) / kPairUnit;
+    jobs.u_lo = static_cast<int>(units * slot / per_tile);
+    jobs.u_hi = static_cast<int>(units * (slot + 1) / per_tile);
+    jobs.n_jobs = (jobs.u_hi - jobs.u_lo + kConfN / kPairUnit - 1) / (kConfN / kPairUnit);
+  }
+  const int n_jobs = jobs.n_jobs;
+  // K in boxes of 64, rounded up to whole stages of both rings (boxes past H read as zeros)
+  constexpr int kLcm = kPairKW > kPairKH ? kPairKW : kPairKH;
+  const int k_boxes = (p.k_blocks + kLcm - 1) / kLcm * kLcm;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      produce_pair<kPairWS, kPairKW, true>(&tm_w, wring, w_full, w_empty, leader, rank, jobs, 0,
+                                           k_boxes, &abort_flag);
+      griddep_launch_dependents();
+    }
+  } else if (warp == kRowWarp) {
+    if (lane == 0)
+      produce_pair<kPairHS, kPairKH, false>(&tm_h, hring, h_full, h_empty, leader, rank, jobs,
+                                            n * kConfN, k_boxes, &abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      const uint32_t w0 = smem_u32(wring), h0 = smem_u32(hring);
+      RingPos wp, hp;
+      bool ok = true;
+      for (int j = 0; j < n_jobs && ok; ++j) {
+        const int buf = j & 1;
+        const uint32_t idesc = idesc_bf16_f32(2 * kBM, jobs.width(j), false, false);
+        if (!(ok = mbar_wait_cluster(&acc_empty[buf], ((j >> 1) & 1) ^ 1, &abort_flag))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf) * kPairCols;
+        for (int kb = 0; kb < k_boxes; ++kb) {
+          const int bw = kb % kPairKW, bh = kb % kPairKH;   // box within the W / row stage
+          if (bw == 0 && !(ok = mbar_wait_cluster(&w_full[wp.slot], wp.phase, &abort_flag))) break;
+          if (bh == 0 && !(ok = mbar_wait_cluster(&h_full[hp.slot], hp.phase, &abort_flag))) break;
+          tc_fence_after();
+          const uint32_t sw = w0 + wp.slot * kPairWStage + bw * kWBox;
+          const uint32_t sh = h0 + hp.slot * kPairHStage + bh * kWBox;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_pair(d, smem_desc(sh + kk * 32, 16, 1024), smem_desc(sw + kk * 32, 16, 1024),
+                           idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          if (bw == kPairKW - 1) {
+            umma_commit_pair(&w_empty[wp.slot], 3);
+            wp.advance(kPairWS);
+          }
+          if (bh == kPairKH - 1) {
+            umma_commit_pair(&h_empty[hp.slot], 3);
+            hp.advance(kPairHS);
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&acc_full[buf], 3);
+      }
+      umma_commit_pair(&bar_done, 3);
+    }
+  } else {
+    const int q4 = warp & 3;                 // tensor-memory lanes 32*q4 .. 32*q4+31
+    const int share = (warp - 2) >> 2;       // columns share*64 .. share*64+63 of a tile
+    const int x = (q4 << 5) | lane;          // row within this CTA's half of the tile
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int col0 = share * kConfShareCols;
+    const uint32_t empty0 = cluster_map(&acc_empty[0], 0), empty1 = cluster_map(&acc_empty[1], 0);
+    int arow = n * kConfN + static_cast<int>(rank) * kBM + x;   // active index
+    const bool valid = working && arow < n_act;
+    int lrow = -1;                                               // logits row to store
+    if (valid && p.logits != nullptr) {
+      const int r = __ldg(p.active_idx + arow);
+      lrow = (r >= 0 && r < p.n_rows) ? r : -1;   // a bad id is flagged by the gather
+    }
+    if (!valid) arow = -1;
+    Acc acc{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    bool ok = true;
+    for (int j = 0; j < n_jobs; ++j) {
+      const int buf = j & 1;
+      if (!ok || !(ok = mbar_wait(&acc_full[buf], (j >> 1) & 1, &abort_flag))) break;
+      tc_fence_after();
+      const int vbase = jobs.col0(j) + col0;
+      const int vend = min(jobs.col0(j) + jobs.width(j), p.V);   // the tile's last column + 1
+      __syncwarp();         // the tensor-memory loads below are warp-collective
+      uint32_t wv[2][16];   // the share's 64 logits of the row as bf16 pairs
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_off + static_cast<uint32_t>(buf) * kPairCols +
+                      static_cast<uint32_t>(col0 + g * 16), r);
+        tmem_wait_ld();
+        tmem_regs_ready(r);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const __nv_bfloat162 h =
+              __floats2bfloat162_rn(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+          wv[g >> 1][(g & 1) * 8 + k] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
+      // this warp's columns are in registers: the accumulator may take the tile after next
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(buf ? empty1 : empty0);
+      if (arow < 0) continue;
+      if (vbase + kConfShareCols > vend) {
+        // a narrow tile or the end of V: columns past the tile take no part
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int v = vbase + h * 32 + 2 * e;
+            uint32_t t = wv[h][e];
+            if (v >= vend) t = (t & 0xFFFF0000u) | 0xFF80u;
+            if (v + 1 >= vend) t = (t & 0x0000FFFFu) | 0xFF800000u;
+            wv[h][e] = t;
+          }
+      }
+      if (lrow >= 0) {
+        uint4* dst = reinterpret_cast<uint4*>(p.logits + static_cast<size_t>(lrow) * p.V + vbase);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)   // tile ends and V are multiples of 8
+          if (vbase + 8 * q < vend)
+            dst[q] = make_uint4(wv[q >> 2][(q & 3) * 4], wv[q >> 2][(q & 3) * 4 + 1],
+                                wv[q >> 2][(q & 3) * 4 + 2], wv[q >> 2][(q & 3) * 4 + 3]);
+      }
+      fold32(acc, wv[0], vbase, p.c);
+      fold32(acc, wv[1], vbase + 32, p.c);
+    }
+    // the four shares of each row, merged in the (now idle) W ring: [share][row]
+    float* sh_m = reinterpret_cast<float*>(wring);
+    float* sh_s = sh_m + kConfShares * kBM;
+    int* sh_i = reinterpret_cast<int*>(sh_s + kConfShares * kBM);
+    sh_m[share * kBM + x] = acc.m;
+    sh_s[share * kBM + x] = acc.s;
+    sh_i[share * kBM + x] = acc.idx;
+    named_barrier(1, kEpiThreads);
+    if (share == 0 && arow >= 0) {
+      Acc t = acc;
+      for (int o = 1; o < kConfShares; ++o)
+        t = merge(t, Acc{sh_m[o * kBM + x], sh_s[o * kBM + x], sh_i[o * kBM + x]}, p.c);
+      p.part[static_cast<size_t>(arow) * p.slots + slot] =
+          CommitPartial{t.m, t.s, t.idx, 0};
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1 && lane == 0) {
+    int dummy = 0;
+    mbar_wait(&bar_done, 0, &dummy);   // every UMMA writing this CTA's tensor memory is done
+  }
+  tc_fence_before();
+  cluster_sync();   // neither CTA exits or frees tensor memory while the other may signal it
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && abort_flag) atomicOr(p.err, BDLM_DEVERR_TIMEOUT);
+}
+
+size_t lm_conf_pair_smem() {
+  return 1024 + static_cast<size_t>(kPairWS) * kPairWStage + static_cast<size_t>(kPairHS) * kPairHStage;
+}
+
 // ------------------------------------------------------------------ scored rows
 // Row r = b * L + i is scored when mask[r] != 0 and (den is null or den[b] != 0).  CTA r counts
 // the scored rows before r; if row r is scored it copies hidden[r] to gathered[idx] and records
@@ -366,7 +660,7 @@ struct LmCommitArgs {
   int R, L;
   const CommitPartial* part; // [scored row][slots]
   int slots;                 // slots allocated per scored row
-  int lm_grid, shares;       // CTAs of the LM head launch, partials each CTA writes per row
+  int lm_grid, shares;       // LM head workers (CTAs or CTA pairs), partials each writes per row
   float c, threshold;
   int rule, k;
   int32_t* tok_out;
@@ -382,7 +676,8 @@ __device__ __forceinline__ int scored(const LmCommitArgs& a, int r) {
 
 // One CTA per block b.  The scored rows (masked, in a denoising sequence) are numbered in row
 // order, as the active-row list of the LM head numbers them; with rt = ceil(scored / 256) row
-// tiles, the LM head ran grid / rt CTAs per row tile and each wrote `shares` partials per row.
+// tiles, the LM head ran lm_grid / rt workers (CTAs, or CTA pairs) per row tile and each wrote
+// `shares` partials per row.
 // Up to 32 rows at a time, 32 / rows warps per row merge a row's partials; then thread 0
 // decides the block over its scored positions.
 __global__ void __launch_bounds__(kFinThreads)
@@ -467,13 +762,60 @@ lm_commit_finalize_kernel(const LmCommitArgs a) {
 
 }  // namespace
 
+namespace {
+
+// Clusters of two pair-kernel CTAs that fit the current device at once (0: none, or the
+// query failed), queried once per device.
+int pair_capacity() {
+  constexpr int kMaxDev = 64;
+  static int cap[kMaxDev];
+  static bool known[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  if (!known[dev]) {
+    int n = 0;
+    const size_t smem = lm_conf_pair_smem();
+    if (cudaFuncSetAttribute(lm_conf_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, lm_conf_pair_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();   // a failed query leaves no sticky error: the single-CTA kernel runs
+    cap[dev] = n;
+    known[dev] = true;
+  }
+  return cap[dev];
+}
+
+}  // namespace
+
 LmConfPlan plan_lm_conf(int max_rows, int H, int V, int num_sms) {
   LmConfPlan pl;
   pl.grid = num_sms > 0 ? num_sms : 1;
+  pl.units = pl.grid;
   pl.slots = pl.grid;
   pl.m_tiles = (V + kConfN - 1) / kConfN;
   pl.max_row_tiles = (max_rows + kConfN - 1) / kConfN;
   pl.smem_bytes = lm_conf_smem();
+  if (max_rows > kBM) {
+    const int pairs = min(pair_capacity(), pl.grid / 2);
+    if (pairs >= 1) {
+      pl.pair = true;
+      pl.grid = 2 * pairs;
+      pl.units = pairs;
+      pl.smem_bytes = lm_conf_pair_smem();
+    }
+  }
   pl.gather_bytes = static_cast<size_t>(max_rows) * H * 2;
   pl.part_bytes = static_cast<size_t>(max_rows) * pl.slots * sizeof(CommitPartial);
   return pl;
@@ -487,7 +829,7 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(lm_conf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(plan.smem_bytes));
+                                         static_cast<int>(lm_conf_smem()));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -505,6 +847,23 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
   prm.k_blocks = (H + kBK - 1) / kBK;
   prm.slots = plan.slots;
   prm.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  if (plan.pair) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, lm_conf_pair_kernel, tm_w, tm_h, prm);
+  }
   return launch_pdl(lm_conf_kernel, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream,
                     tm_w, tm_h, prm);
 }
@@ -529,7 +888,7 @@ cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denois
   a.L = L;
   a.part = part;
   a.slots = plan.slots;
-  a.lm_grid = plan.grid;
+  a.lm_grid = plan.units;
   a.shares = 1;
   a.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   a.threshold = threshold;
