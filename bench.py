@@ -627,7 +627,7 @@ def prefill_bench(bd, device, flush, reps: int, seed: int, B=128, n=512, L=4):
 
 
 KERNEL_SOURCES = {"attention": ("attention_config2", "attention.cu"),
-                  "lm_head_commit": ("lm_conf_config2_256rows", "lm_head.cu"),
+                  "lm_head_commit": ("lm_conf_config2_256rows", "lm_conf.cu"),
                   "lm_head": ("lm_head_config2_256rows", "lm_head.cu"),
                   "commit": ("commit_config2", "commit.cu")}
 
