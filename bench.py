@@ -613,8 +613,15 @@ def prefill_bench(bd, device, flush, reps: int, seed: int, B=128, n=512, L=4):
     torch.cuda.synchronize()
     assert bd.bdlm_device_error() == 0
     ms = float(np.mean([x.elapsed_time(y) for x, y in evs]))
-    nb = n // L
-    kv_read = B * Hkv * D * 2 * 2 * L * nb * (nb + 1) // 2      # every block re-reads its prefix
+    # the library cuts the prompt into chunks of Lq queries (the largest multiple of L dividing n
+    # with Lq * G <= 128 rows), block-causal inside a chunk; chunk c reads the K/V of the
+    # (c + 1) * Lq tokens up to its end once per KV head
+    G = Hq // Hkv
+    Lq = max([c for c in range(L, n + 1, L) if n % c == 0 and c * G <= 128] or [L])
+    if Lq * G <= 32:
+        Lq = L
+    nq = n // Lq
+    kv_read = B * Hkv * D * 2 * 2 * Lq * nq * (nq + 1) // 2
     qo = B * n * Hq * D * 2 * 2
     written = B * n * Hkv * D * 2 * 2
     return {"workload": f"prefill: {B} fresh prompts of {n} tokens, block length {L}, "
@@ -622,8 +629,9 @@ def prefill_bench(bd, device, flush, reps: int, seed: int, B=128, n=512, L=4):
             "ms": ms, "tokens_per_s": B * n / (ms / 1e3),
             "bytes": kv_read + qo + written,
             "achieved_gbs": (kv_read + qo + written) / (ms / 1e3) / 1e9,
-            "note": "runs the block attention kernel over B * n / L block sequences, so every "
-                    "block re-reads the K/V before it (traffic grows with n^2 / L)"}
+            "note": f"the prompt's K/V written into the cache, then block-causal attention over "
+                    f"chunks of {Lq} queries (query rows on the UMMA M side), each chunk reading "
+                    f"the K/V before its end once"}
 
 
 KERNEL_SOURCES = {"attention": ("attention_config2", "attention.cu"),

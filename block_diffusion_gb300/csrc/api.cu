@@ -130,7 +130,7 @@ LmCommitLayout lm_commit_layout(const bdlm::LmConfPlan& plan, int rows) {
 int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
                    const bdlm_bf16* k_pages, const bdlm_bf16* v_pages, const int32_t* page_table,
                    const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream,
-                   int table_div);
+                   int table_div, int mask_block = 0);
 
 }  // namespace
 
@@ -264,7 +264,16 @@ int bdlm_prefill_attention(const bdlm_attn_desc* desc, int prompt_len, const bdl
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) ||
       !aligned16(v_pages) || !aligned16(out))
     return BDLM_ERR_INVALID;
-  const int nb = prompt_len / d.L;
+  // Queries go to the attention in chunks of Lq positions (a multiple of L dividing the prompt,
+  // Lq * G <= 128 query rows per KV head, the most that fit) with the block-causal mask inside
+  // a chunk, so each chunk reads the K/V before it once; chunks of one block (Lq = L) need no
+  // mask.  Narrow chunks (Lq * G <= 32 rows) stay one block per attention sequence.
+  const int G = d.Hq / d.Hkv;
+  int Lq = d.L;
+  for (int c = d.L; c * G <= 128 && c <= prompt_len; c += d.L)
+    if (prompt_len % c == 0) Lq = c;
+  if (Lq * G <= 32) Lq = d.L;
+  const int nb = prompt_len / Lq;
   if (static_cast<long long>(d.B) * prompt_len * d.Hq > 0x7FFFFFFFll ||
       static_cast<long long>(d.B) * d.max_pages_per_seq > 0x7FFFFFFFll ||
       static_cast<long long>(d.max_pages_per_seq) * d.page_size > 0x7FFFFFFFll)
@@ -276,28 +285,31 @@ int bdlm_prefill_attention(const bdlm_attn_desc* desc, int prompt_len, const bdl
   rc = ensure(&st->aux, &st->aux_cap, static_cast<size_t>(d.B) * nb * sizeof(int32_t), false);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the prompt's K/V into the cache, then one attention sequence per prompt block
+  // the prompt's K/V into the cache, then one attention sequence per chunk of Lq queries
   if (bdlm::launch_write_block_kv(k_new, v_new, k_pages, v_pages, page_table, prefix_lens, d.B,
                                   prompt_len, d.Hkv, d.max_pages_per_seq, d.num_pages, st->err,
                                   s) != cudaSuccess)
     return BDLM_ERR_CUDA;
   int32_t* pre = static_cast<int32_t*>(st->aux);
-  if (bdlm::launch_prompt_prefix(prefix_lens, d.B, nb, d.L, pre, s) != cudaSuccess)
+  if (bdlm::launch_prompt_prefix(prefix_lens, d.B, nb, Lq, pre, s) != cudaSuccess)
     return BDLM_ERR_CUDA;
   bdlm_attn_desc dv = d;
   dv.B = d.B * nb;
-  return attention_impl(st, dv, q, k_pages, v_pages, page_table, pre, out, stream, nb);
+  dv.L = Lq;
+  return attention_impl(st, dv, q, k_pages, v_pages, page_table, pre, out, stream, nb,
+                        Lq > d.L ? d.L : 0);
 }
 }  // extern "C"
 
 namespace {
 
 // Block attention of d.B sequences (the caller holds g_mu and has validated d); sequence b
-// uses page-table row b / table_div.
+// uses page-table row b / table_div; mask_block > 0 makes each sequence's queries
+// block-causal in blocks of mask_block.
 int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
                    const bdlm_bf16* k_pages, const bdlm_bf16* v_pages, const int32_t* page_table,
                    const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream,
-                   int table_div) {
+                   int table_div, int mask_block) {
   int rc = get_encoder();
   if (rc) return rc;
   const AttnPlan plan = bdlm::plan_attention(d.B, d.L, d.Hq, d.Hkv, d.max_pages_per_seq,
@@ -330,7 +342,8 @@ int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
                                          d.L, d.Hq, d.Hkv, d.max_pages_per_seq, d.num_pages,
                                          scale, plan, static_cast<float*>(st->data),
                                          st->attn_cnt, st->err, st->num_sms,
-                                         static_cast<cudaStream_t>(stream), table_div);
+                                         static_cast<cudaStream_t>(stream), table_div,
+                                         mask_block);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 

@@ -42,6 +42,9 @@ constexpr int kStageBytes = 32768;  // one K or V tile: 2 halves x 8 pages x 16 
 constexpr int kHalfBytes = 16384;
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
+// the rows-on-M kernel: two softmax warps per tensor-memory lane quadrant
+constexpr int kRowSoftmaxThreads = 256;
+constexpr int kRowThreads = 64 + kRowSoftmaxThreads;
 constexpr int kMaxSplitTokens = 2048;
 // Page ids staged per item: a split of up to kMaxSplitTokens, or a whole sequence of up to
 // kMaxItemPages pages when sequences are processed whole (two CTAs per SM at N = 16 leave
@@ -69,12 +72,14 @@ struct AttnParams {
   int table_div;     // sequence b uses page-table row b / table_div (prompt blocks share a row)
   int lsub, row_groups, rows_per_group, split_tokens, max_splits, chunk_tiles;
   int total_items;
+  int mask_block;    // > 0: query i of a sequence sees keys < prefix + (i / mask_block + 1) * mask_block
   float scale_log2;  // sm_scale * log2(e)
 };
 
 struct Item {
   int b, kvh, split, rg;
   int t_begin, t_end, n_splits;
+  int q0;  // key position of the sequence's first query (its prefix length)
   int n_tiles, n_chunks;
   int end;
 };
@@ -104,6 +109,7 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   const int kv_len = static_cast<int>(kvl);
   it.t_begin = it.split * p.split_tokens;
   if (it.t_begin >= kv_len) return false;
+  it.q0 = kv_len - p.L;
   it.t_end = min(kv_len, it.t_begin + p.split_tokens);
   it.n_splits = (kv_len + p.split_tokens - 1) / p.split_tokens;
   it.n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
@@ -115,8 +121,8 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   return true;
 }
 
-template <int N, int STAGES, int CTAS_PER_SM>
-__global__ void __launch_bounds__(kThreads, CTAS_PER_SM)
+template <int N, int STAGES, int CTAS_PER_SM, bool MASKED, bool ROWS>
+__global__ void __launch_bounds__(ROWS ? kRowThreads : kThreads, CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   constexpr uint32_t kTmemCols = 512 / CTAS_PER_SM;
@@ -125,7 +131,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = base;                          // 2 halves x N rows x 128 B
   uint8_t* sKV = sQ + N * 256;                 // STAGES x 32 KB
-  uint8_t* sP = sKV + STAGES * kStageBytes;    // 2 buffers x (2 K-atoms x N rows x 128 B)
+  uint8_t* sP = sKV + STAGES * kStageBytes;    // 1 or 2 buffers x (2 K-atoms x N rows x 128 B)
 
   __shared__ uint64_t bar_qfull, bar_qempty, bar_full[STAGES], bar_empty[STAGES];
   __shared__ uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_pempty[2];
@@ -135,10 +141,21 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ int s_pid[3][kMaxItemPages];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ float s_m[N], s_mc[N], s_alpha[N], s_l[N];
+  constexpr int kCols = ROWS ? 1 : N;   // per-column state of the transposed softmax
+  __shared__ float s_m[kCols], s_mc[kCols], s_alpha[kCols], s_l[kCols];
   __shared__ int s_need[2];   // chunk u (parity): some column's max rose enough to rescale O^T
   __shared__ int s_pflag[2];  // P buffer: its tile starts a chunk whose PV waits for a rescale
-  __shared__ float s_red[4][N];
+  __shared__ float s_red[4][kCols];
+  __shared__ float s_hmax[ROWS ? 2 : 1][2][ROWS ? N : 1];   // half-row maxima by tile parity
+  __shared__ float s_hsum[2][ROWS ? N : 1];                 // half-row sums at an item's end
+  __shared__ uint64_t bar_pair[ROWS ? 4 : 1][2], bar_pair_end[ROWS ? 4 : 1];   // halves of a row
+  constexpr int kSoftmax = ROWS ? kRowSoftmaxThreads : kSoftmaxThreads;
+  // P buffers: the transposed softmax double-buffers P^T; with rows on M one buffer suffices
+  // (a thread writes P(u + 1) only after its tile's math, long after PV(u) has read P(u))
+  constexpr int kPBufs = ROWS ? 1 : 2;
+  static_assert(!MASKED || ROWS, "the block-causal mask is applied by the row-per-thread softmax");
+  static_assert(!ROWS || N == 128, "rows on M: one UMMA of 128 query rows");
+  static_assert(ROWS || N <= 32, "keys on M: at most 32 query rows on N");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -153,8 +170,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_sfull[i], 1);
-      mbar_init(&bar_sfree[i], kSoftmaxThreads);
-      mbar_init(&bar_pfull[i], kSoftmaxThreads);
+      mbar_init(&bar_sfree[i], kSoftmax);
+      mbar_init(&bar_pfull[i], kSoftmax);
       mbar_init(&bar_pempty[i], 1);
     }
     mbar_init(&bar_oready, kSoftmaxThreads);
@@ -163,7 +180,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     mbar_init(&bar_done, 1);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(&bar_ifull[i], 1);
-      mbar_init(&bar_iempty[i], 2);
+      // the MMA warp, and one softmax thread (every softmax thread with rows on M)
+      mbar_init(&bar_iempty[i], ROWS ? 1 + kRowSoftmaxThreads : 2);
+    }
+    if constexpr (ROWS) {
+      for (int q = 0; q < 4; ++q) {
+        mbar_init(&bar_pair[q][0], 64);
+        mbar_init(&bar_pair[q][1], 64);
+        mbar_init(&bar_pair_end[q], 64);
+      }
     }
     abort_flag = 0;
     s_need[0] = s_need[1] = 0;
@@ -178,7 +203,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // zero the padding rows of the Q operand (rows >= rows_per_group); TMA never writes them
     const int rows = p.rows_per_group;
     const int t = threadIdx.x - 64;
-    for (int o = t * 16; o < (N - rows) * 128; o += kSoftmaxThreads * 16) {
+    for (int o = t * 16; o < (N - rows) * 128; o += kSoftmax * 16) {
       *reinterpret_cast<uint4*>(sQ + rows * 128 + o) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(sQ + N * 128 + rows * 128 + o) = make_uint4(0, 0, 0, 0);
     }
@@ -261,7 +286,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     };
     // Streams the K (pass 0) or V (pass 1) tiles of chunk c of item `it` (page ids in
     // s_pid[pbuf]).  Whole warp: lane 0 waits for a free stage and posts the byte count, then
-    // lane q issues the two boxes of page q, so a stage's 16 copies go out in one instruction.
+    // lanes 0-15 issue the stage's 16 boxes (two halves of 8 pages), one each.
     auto emit = [&](const Item& it, int c, int pbuf, int pass, Item* gi = nullptr,
                     bool* gh = nullptr, int* gs = nullptr) {
       const CUtensorMap* tm = pass == 0 ? &tm_k : &tm_v;
@@ -280,8 +305,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (!ok) break;
         const int tok0 = it.t_begin + j * kTile;
         const int npg = min(kTile / kPage, (it.t_end - tok0 + kPage - 1) / kPage);
-        const int id = lane < npg ? s_pid[pbuf][j * (kTile / kPage) + lane] : -1;
-        const uint32_t have = __ballot_sync(0xffffffffu, id >= 0);
+        // lane q < 16 copies half q / 8 of page q % 8 of the tile: one box per lane, so the
+        // stage's 16 copies issue in parallel (a thread's copies issue one after another)
+        const int pg = lane & 7, hf = (lane >> 3) & 1;
+        const int id = (lane < 16 && pg < npg) ? s_pid[pbuf][j * (kTile / kPage) + pg] : -1;
+        const uint32_t have = __ballot_sync(0xffffffffu, lane < 8 && id >= 0);
         uint8_t* stage = sKV + st * kStageBytes;
         if (lane == 0) {
           if (have)
@@ -290,11 +318,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             mbar_arrive(&bar_full[st]);
         }
         __syncwarp();
-        if (id >= 0) {
-          tma_load_4d_hint(stage + lane * 2048, tm, &bar_full[st], 0, it.kvh, 0, id, kv_policy);
-          tma_load_4d_hint(stage + kHalfBytes + lane * 2048, tm, &bar_full[st], 64, it.kvh, 0, id,
-                           kv_policy);
-        }
+        if (id >= 0)
+          tma_load_4d_hint(stage + hf * kHalfBytes + pg * 2048, tm, &bar_full[st], hf * 64, it.kvh,
+                           0, id, kv_policy);
         if (++st == STAGES) {
           st = 0;
           ph ^= 1;
@@ -371,8 +397,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   } else if (warp == 1) {
     // =================================================================== MMA issuer
     if (lane == 0) {
+      // S^T = K Q^T and O^T += V^T P^T (keys / head dims on M), or with ROWS S = Q K^T and
+      // O += P V (query rows on M): the same shared-memory operands, A and B swapped
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, N, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(128, N, true, false);
+      constexpr uint32_t kIdescO = ROWS ? idesc_bf16_f32(128, 128, false, true)
+                                        : idesc_bf16_f32(128, N, true, false);
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t kv_addr = smem_u32(sKV);
       const uint32_t p_addr = smem_u32(sP);
@@ -397,7 +426,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const uint64_t ad = smem_desc(ka + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
             const uint64_t bd =
                 smem_desc(q_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-            umma_bf16(tS + (j - j0) * N, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            if constexpr (ROWS)
+              umma_bf16(tS + (j - j0) * N, bd, ad, kIdescS, kk > 0 ? 1u : 0u);
+            else
+              umma_bf16(tS + (j - j0) * N, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bar_empty[st]);
           if (++st == STAGES) {
@@ -413,9 +445,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
-          const int pb = pcount & 1;
+          const int pb = pcount % kPBufs;
           if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
-          if (!(ok = mbar_wait(&bar_pfull[pb], (pcount >> 1) & 1, &abort_flag))) return;
+          if (!(ok = mbar_wait(&bar_pfull[pb], (pcount / kPBufs) & 1, &abort_flag))) return;
           if (c > 0 && j == j0 && s_pflag[pb]) {  // the softmax rescales O^T first
             if (!(ok = mbar_wait(&bar_oready, ocount & 1, &abort_flag))) return;
             ++ocount;
@@ -440,7 +472,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           for (int q = 0; q < npg; ++q) {
             const uint64_t ad = smem_desc(va + q * 2048, kHalfBytes, 1024);
             const uint64_t bd = smem_desc(pa + (q >> 2) * (N * 128) + (q & 3) * 32, 16, 1024);
-            umma_bf16(tO, ad, bd, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
+            if constexpr (ROWS)
+              umma_bf16(tO, bd, ad, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
+            else
+              umma_bf16(tO, ad, bd, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
           }
           umma_commit(&bar_empty[st]);
           umma_commit(&bar_pempty[pb]);
@@ -486,6 +521,178 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
       }
       umma_commit(&bar_done);
+    }
+  } else if constexpr (ROWS) {
+    // ====================================================== softmax/epilogue, a row per 2 threads
+    // Query row n of the item is tensor-memory lane n: row n of S(u) holds its 128 scores of
+    // tile u, row n of O its 128 head dims.  Two warps share each lane quadrant, so each row
+    // has two threads: half 0 takes columns 0-63, half 1 columns 64-127 (of S, then of O).
+    // They exchange the half-row maxima every tile and the half sums at the end; one tile per
+    // chunk (N = 128 leaves room for two S buffers and O).
+    const int q4 = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int n = (q4 << 5) | lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half * 64);
+    const float cs = p.scale_log2;
+    bool ok = true;
+    int pcount = 0, u = 0, pair_ends = 0;
+    for (int seq = 0; ok; ++seq) {
+      const int rs = seq % kItemRing;
+      if (!(ok = mbar_wait(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      const Item it = s_item[rs];
+      mbar_arrive(&bar_iempty[rs]);   // the descriptor is in registers: its slot may be reused
+      if (it.end) break;
+      const int i_row = it.rg * p.lsub + n / p.G;   // block position of the row
+      int lim = 0x7FFFFFFF;                         // keys past q0 the row may see
+      if constexpr (MASKED) lim = (i_row / p.mask_block + 1) * p.mask_block;
+      float m_run = -CUDART_INF_F, l_run = 0.f;     // l_run: this half's sum
+      for (int c = 0; c < it.n_chunks && ok; ++c, ++u) {
+        const uint32_t tS = tmem + lane_off + static_cast<uint32_t>((u & 1) * N) + col0;
+        if (!(ok = mbar_wait(&bar_sfull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        tc_fence_after();
+        uint32_t r[64];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          tmem_ld16(tS + g * 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * g));
+        tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + 16 * g));
+        tc_fence_before();
+        mbar_arrive(&bar_sfree[u & 1]);   // S(u) is in registers: the buffer may take S(u + 2)
+        // keys of the tile the row sees: a prefix of it (sequence end, block-causal limit);
+        // the others read as -inf
+        const int key0 = it.t_begin + c * kTile;
+        int nvalid = min(kTile, it.t_end - key0);
+        if constexpr (MASKED) nvalid = min(nvalid, lim - (key0 - it.q0));
+        nvalid -= half * 64;   // of this half's columns
+        if (nvalid < 64) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k >= nvalid) r[k] = 0xFF800000u;
+        }
+        // half-row max (a tree, so the warp has work in flight), then the row max
+        float t[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          t[k] = fmaxf(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+#pragma unroll
+        for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+        s_hmax[u & 1][half][n] = t[0];
+        mbar_arrive(&bar_pair[q4][u & 1]);
+        if (!(ok = mbar_wait(&bar_pair[q4][u & 1], (u >> 1) & 1, &abort_flag))) break;
+        const float mx = fmaxf(s_hmax[u & 1][0][n], s_hmax[u & 1][1][n]);
+        // the running max moves only when the tile raises it by more than 2^kLazyRescale
+        // (both halves of a row take the same decision)
+        float alpha = 1.f;
+        bool resc = false;
+        if (m_run == -CUDART_INF_F) {
+          m_run = mx;
+        } else if ((mx - m_run) * cs > kLazyRescale) {
+          alpha = ex2((m_run - mx) * cs);
+          m_run = mx;
+          resc = true;
+        }
+        // p = 2^(s cs - m cs): scaling two scores per packed FMA, the exponentials independent,
+        // the sum a tree of packed adds (a row that has seen no key yet has m = -inf: p = 0)
+        const float mc = m_run == -CUDART_INF_F ? 0.f : m_run * cs;
+        const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-mc, -mc);
+        float2 e[32];
+        uint32_t pk[32];   // this half of the row's P as bf16 pairs
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 y = __ffma2_rn(
+              make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), cs2, nm2);
+          e[k] = make_float2(ex2(y.x), ex2(y.y));
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[k].x, e[k].y);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+#pragma unroll
+        for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) e[k] = __fadd2_rn(e[k], e[k + w]);
+        l_run = l_run * alpha + (e[0].x + e[0].y);
+        if (__any_sync(0xffffffffu, resc)) {
+          // bring this warp's half of its rows of O to the new maxima once the previous
+          // tile's PV is done
+          if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t o[16];
+            tmem_ld16(tO + lane_off + col0 + g * 16, o);
+            tmem_wait_ld();
+            tmem_regs_ready(o);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st16(tO + lane_off + col0 + g * 16, o);
+          }
+          tmem_wait_st();
+        }
+        // this half of P row n into the K-major, 128-byte-swizzled operand: keys 64h ..
+        // 64h+63 are its half h
+        const int pb = pcount % kPBufs;
+        if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount / kPBufs) & 1) ^ 1, &abort_flag))) break;
+        uint8_t* prow = sP + pb * (N * 256) + half * (N * 128) + n * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (n & 7)) << 4)) =
+              make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar_pfull[pb]);
+        ++pcount;
+        if (c != it.n_chunks - 1) continue;
+        // ---- epilogue of the item: this half of row n of O, divided by the row's sum or as a
+        // split partial
+        s_hsum[half][n] = l_run;
+        mbar_arrive(&bar_pair_end[q4]);
+        if (!(ok = mbar_wait(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
+        ++pair_ends;
+        const float l_row = s_hsum[0][n] + s_hsum[1][n];
+        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        tc_fence_after();
+        const bool live = n < p.rows_per_group && i_row < p.L;
+        const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
+        float* mine = p.part + (grp * p.max_splits + it.split) * static_cast<size_t>(N) * 130;
+        uint16_t* dst = live ? p.out + ((static_cast<size_t>(it.b) * p.L + i_row) * p.Hq +
+                                        static_cast<size_t>(it.kvh) * p.G + n % p.G) * 128 + col0
+                             : p.out;
+        const float inv = 1.f / l_row;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t o[16];
+          tmem_ld16(tO + lane_off + col0 + g * 16, o);
+          tmem_wait_ld();
+          tmem_regs_ready(o);
+          if (!live) continue;
+          if (it.n_splits == 1) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[2 * k]) * inv,
+                                                              __uint_as_float(o[2 * k + 1]) * inv);
+              w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + g * 16);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            float4* d4 = reinterpret_cast<float4*>(mine + n * 128 + col0 + g * 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                  __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+          }
+        }
+        if (live && it.n_splits > 1 && half == 0) {
+          mine[N * 128 + n] = m_run;
+          mine[N * 128 + N + n] = l_row;
+        }
+        tc_fence_before();   // O is read: the next item's first PV (after its P) may overwrite it
+      }
     }
   } else {
     // =================================================================== softmax/epilogue
@@ -583,7 +790,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           for (int n = 0; n < N; ++n) l[n] *= s_alpha[n];
         }
         // phase B: P^T = exp(S^T - m) to shared memory, tile by tile
-        if constexpr (N <= 32) {
+        {
           // narrow N: maxima in registers, the next tile's S^T read from tensor memory
           // while this one is exponentiated
           float mcr[N];
@@ -630,38 +837,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             ++pcount;
           }
           if (!ok) tmem_wait_ld();
-        } else {
-          // phase B (wide N): column groups of 16, maxima read from shared memory
-          for (int j = j0; j < j1 && ok; ++j) {
-            const int pb = pcount & 1;
-            if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1, &abort_flag))) break;
-            uint8_t* pbuf = sP + pb * (N * 256) + (x >> 6) * (N * 128);
-            const bool valid = it.t_begin + j * kTile + x < it.t_end;
-            const uint32_t xc = (x & 63) >> 3;
-            const uint32_t xb = (x & 7) * 2;
-  #pragma unroll
-            for (int cg = 0; cg < N / 16; ++cg) {
-              uint32_t r[16];
-              tmem_ld16(tS + (j - j0) * N + cg * 16, r);
-              tmem_wait_ld();
-              tmem_regs_ready(r);
-  #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const int n = cg * 16 + k;
-                const float pv = valid ? exp2f(fmaf(__uint_as_float(r[k]), cs, -s_mc[n])) : 0.f;
-                l[n] += pv;
-                const uint32_t off = n * 128 + ((xc ^ (n & 7)) << 4) + xb;
-                *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = __float2bfloat16_rn(pv);
-              }
-            }
-            if (x == 0) s_pflag[pb] = (j == j0) && need;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar_pfull[pb]);
-            ++pcount;
-          }
         }
-        if (!ok) break;
         if (!ok) break;
         tc_fence_before();
         mbar_arrive(&bar_sfree[u & 1]);
@@ -911,37 +1087,38 @@ attn_merge_kernel(const AttnParams p, int N) {
   }
 }
 
-template <int N, int STAGES>
+template <int N, int STAGES, bool ROWS>
 constexpr size_t smem_bytes() {
   return 1024 + static_cast<size_t>(N) * 256 + static_cast<size_t>(STAGES) * kStageBytes +
-         static_cast<size_t>(2) * N * 256;
+         static_cast<size_t>(ROWS ? 1 : 2) * N * 256;
 }
 
-template <int N, int STAGES, int CPS>
+template <int N, int STAGES, int CPS, bool MASKED, bool ROWS>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const AttnParams& prm, int num_sms, cudaStream_t stream) {
-  constexpr size_t smem = smem_bytes<N, STAGES>();
+  constexpr size_t smem = smem_bytes<N, STAGES, ROWS>();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS>,
+    e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(attn_kernel<N, STAGES, CPS>, dim3(num_sms * CPS), dim3(kThreads), smem,
+  return launch_pdl(attn_kernel<N, STAGES, CPS, MASKED, ROWS>, dim3(num_sms * CPS),
+                    dim3(ROWS ? kRowThreads : kThreads), smem,
                     stream, tq, tk, tv, prm);
 }
 
 }  // namespace
 
 namespace {
-// Prompt block j of sequence b becomes sequence b * nb + j of the attention: its prefix is the
-// cached prefix plus the j blocks before it.
+// Prompt chunk j (L queries) of sequence b becomes sequence b * nb + j of the attention: its
+// prefix is the cached prefix plus the j chunks before it.
 __global__ void prompt_prefix_kernel(const int32_t* __restrict__ prefix_lens, int B, int nb, int L,
                                      int32_t* __restrict__ out) {
   griddep_wait();
@@ -977,12 +1154,13 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
     pl.row_groups = (L + pl.lsub - 1) / pl.lsub;
   }
   const int rpg = pl.G * pl.lsub;
-  pl.n_mma = rpg <= 16 ? 16 : rpg <= 32 ? 32 : rpg <= 64 ? 64 : 128;
+  // up to 32 query rows: S^T = K Q^T with the rows on N; more: S = Q K^T, 128 rows on M
+  pl.n_mma = rpg <= 16 ? 16 : rpg <= 32 ? 32 : 128;
   // tensor memory per CTA holds two S^T chunks and O^T
   const int ctas_per_sm = pl.n_mma <= 32 ? 2 : 1;
   pl.tmem_cols = 512 / ctas_per_sm;
   pl.chunk_tiles = (pl.tmem_cols - pl.n_mma) / (2 * pl.n_mma);
-  const int chunks_per_split = pl.n_mma == 16 ? 1 : pl.n_mma == 32 ? 3 : pl.n_mma == 64 ? 4 : 16;
+  const int chunks_per_split = pl.n_mma == 16 ? 1 : pl.n_mma == 32 ? 3 : 16;
   pl.split_tokens = pl.chunk_tiles * kTile * chunks_per_split;
   if (pl.split_tokens > kMaxSplitTokens) pl.split_tokens = kMaxSplitTokens;
   const long long max_tok = static_cast<long long>(max_pages) * kPage;
@@ -1009,8 +1187,9 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
                              const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
-                             cudaStream_t stream, int table_div) {
+                             cudaStream_t stream, int table_div, int mask_block) {
   AttnParams prm;
+  prm.mask_block = mask_block > 0 ? mask_block : 0;
   prm.page_table = page_table;
   prm.table_div = table_div < 1 ? 1 : table_div;
   prm.prefix_lens = prefix_lens;
@@ -1046,10 +1225,18 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
     prm.part = nullptr;
   }
   switch (plan.n_mma) {
-    case 16: e = launch_t<16, 3, 2>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
-    case 32: e = launch_t<32, 2, 2>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
-    case 64: e = launch_t<64, 5, 1>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
-    case 128: e = launch_t<128, 3, 1>(tm_q, tm_k, tm_v, prm, num_sms, stream); break;
+    case 16:
+      if (mask_block > 0) return cudaErrorInvalidValue;   // the mask needs rows on M
+      e = launch_t<16, 3, 2, false, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      break;
+    case 32:
+      if (mask_block > 0) return cudaErrorInvalidValue;
+      e = launch_t<32, 2, 2, false, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      break;
+    case 128:
+      e = mask_block > 0 ? launch_t<128, 4, 1, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream)
+                         : launch_t<128, 4, 1, false, true>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess || plan.max_splits <= 1) return e;

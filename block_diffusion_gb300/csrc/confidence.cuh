@@ -23,13 +23,6 @@ struct Acc {
   int idx;    // first index of the max
 };
 
-// 2^x with the SFU's approximate base-2 exponential (relative error about 2^-22).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // The state of the union of two disjoint sets of logits; on equal maxima the lower index.
 __device__ __forceinline__ Acc merge(Acc a, Acc b, float c) {
   if (b.m == -CUDART_INF_F) return a;

@@ -71,12 +71,15 @@ struct AttnPlan {
 
 AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size,
                         int num_sms);
+// Sequence b uses page-table row b / table_div.  mask_block > 0 makes the queries of a
+// sequence block-causal: query i sees the prefix and the sequence's keys up to the end of its
+// own block of mask_block queries (chunked prefill); else every query sees all L.
 cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const int32_t* page_table,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
                              const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
-                             cudaStream_t stream, int table_div = 1);
+                             cudaStream_t stream, int table_div = 1, int mask_block = 0);
 
 // ------------------------------------------------------------------ LM head
 struct LmHeadPlan {
@@ -133,7 +136,7 @@ cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denois
                                       int32_t* tok_out, float* conf_out, uint8_t* commit_out,
                                       cudaStream_t stream);
 
-// Prompt block j of sequence b -> attention sequence b * nb + j with prefix prefix[b] + j * L.
+// Prompt chunk j of sequence b -> attention sequence b * nb + j with prefix prefix[b] + j * L.
 cudaError_t launch_prompt_prefix(const int32_t* prefix_lens, int B, int nb, int L, int32_t* out,
                                  cudaStream_t stream);
 
