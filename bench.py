@@ -58,6 +58,10 @@ def parse_args(argv=None):
                     help="time eager launches instead of one CUDA graph per round")
     ap.add_argument("--compact-pool", action="store_true",
                     help="pool of exactly the referenced pages x1.25 (smaller device footprint)")
+    ap.add_argument("--attention-shapes", action="store_true",
+                    help="time the block attention alone at the config 2-4 shapes and exit")
+    ap.add_argument("--shape", choices=["c2", "c3_L16", "c3_L32", "c4"], default=None,
+                    help="with --attention-shapes: only this shape")
     return ap.parse_args(argv)
 
 
@@ -804,9 +808,71 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
+ATTN_SHAPES = {"c2": (2, 4), "c3_L16": (3, 16), "c3_L32": (3, 32), "c4": (4, 64)}
+
+
+def attention_shapes(args):
+    """The block attention alone at the config 2-4 shapes (B, L and prefix range of each
+    config, 32 q / 8 KV heads, D = 128, pools of the referenced pages x1.25): CUDA events
+    around each call, L2 flushed before it; one JSON line."""
+    import torch
+    import block_diffusion_gb300 as bd
+    from block_diffusion_gb300 import build as bbuild
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    if not os.path.exists(bbuild.OUT):
+        bbuild.build()
+    bd.load_library()
+    peaks = load_peaks()
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device=device)
+    out_rows = []
+    for name, (cfg, L) in ATTN_SHAPES.items():
+        if args.shape is not None and name != args.shape:
+            continue
+        c = W.CONFIGS[cfg]
+        rng = np.random.default_rng(W.seed_for(cfg))
+        a = W.make_attention(rng, c["B"], L, c["Hq"], c["Hkv"], c["D"], prefix_range=c["prefix"],
+                             poison=False)
+        kp, vp = _bf16(a.k_ref, device), _bf16(a.v_ref, device)
+        q = _bf16(a.q, device)
+        pt = torch.from_numpy(a.page_table_ref).to(device)
+        pl = torch.from_numpy(a.prefix_lens).to(device)
+        out = torch.empty((a.B, L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
+        desc = bd.attn_desc(a.B, L, a.Hq, a.Hkv, a.D, a.page_table_ref.shape[1], a.k_ref.shape[0])
+        evs = []
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup) + args.steps):
+                flush_buf.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                bd.bdlm_block_attention(desc, q, kp, vp, pt, pl, L, out, stream.cuda_stream)
+                e1.record(stream)
+                if i >= max(3, args.warmup):
+                    evs.append((e0, e1))
+        torch.cuda.synchronize()
+        assert bd.bdlm_device_error() == 0
+        us = float(np.mean([x.elapsed_time(y) for x, y in evs])) * 1e3
+        kv_tok = int((a.prefix_lens.astype(np.int64) + L).sum())
+        nbytes = kv_tok * a.Hkv * a.D * 2 * 2 + a.B * L * a.Hq * a.D * 2 * 2
+        flops = 4 * L * a.Hq * a.D * kv_tok
+        out_rows.append({"shape": name, "B": a.B, "L": L, "us": us, "algorithmic_bytes": nbytes,
+                         "achieved_gbs": nbytes / us / 1e3,
+                         "frac_hbm": nbytes / us / 1e3 / peaks["hbm_gbs"],
+                         "tflops": flops / us / 1e6})
+        del kp, vp, q, out, a
+        torch.cuda.empty_cache()
+    print(json.dumps({"attention_shapes": out_rows, "steps": args.steps,
+                      "peak_hbm_gbs": peaks["hbm_gbs"], "l2": "flushed before every call"}),
+          flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
+    if args.attention_shapes:
+        attention_shapes(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:
