@@ -44,7 +44,9 @@ constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 // the rows-on-M kernel: two softmax warps per tensor-memory lane quadrant
 constexpr int kRowSoftmaxThreads = 256;
-constexpr int kRowThreads = 64 + kRowSoftmaxThreads;
+// warps 0-1 producer and MMA, 2-9 softmax, 10 a second K/V copy issuer
+constexpr int kRowIssueWarp = 2 + kRowSoftmaxThreads / 32;
+constexpr int kRowThreads = 32 * (kRowIssueWarp + 1);
 constexpr int kMaxSplitTokens = 2048;
 // Page ids staged per item: a split of up to kMaxSplitTokens, or a whole sequence of up to
 // kMaxItemPages pages when sequences are processed whole (two CTAs per SM at N = 16 leave
@@ -74,6 +76,12 @@ struct AttnParams {
   int total_items;
   int mask_block;    // > 0: query i of a sequence sees keys < prefix + (i / mask_block + 1) * mask_block
   float scale_log2;  // sm_scale * log2(e)
+};
+
+// What the second copy issuer of the rows-on-M kernel needs for one ring stage.
+struct StageInfo {
+  int pass, kvh, end;
+  int id[kTile / kPage];   // page ids of the tile (-1: past the sequence)
 };
 
 struct Item {
@@ -149,6 +157,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ float s_hmax[ROWS ? 2 : 1][2][ROWS ? N : 1];   // half-row maxima by tile parity
   __shared__ float s_hsum[2][ROWS ? N : 1];                 // half-row sums at an item's end
   __shared__ uint64_t bar_pair[ROWS ? 4 : 1][2], bar_pair_end[ROWS ? 4 : 1];   // halves of a row
+  // rows on M: the producer issues half 0 of each stage's page boxes and hands the stage to a
+  // second issuer warp for half 1 (one warp's copies issue at about 1 us per 16 boxes)
+  __shared__ StageInfo s_sinfo[ROWS ? STAGES : 1];
+  __shared__ uint64_t bar_sready[ROWS ? STAGES : 1];
   constexpr int kSoftmax = ROWS ? kRowSoftmaxThreads : kSoftmaxThreads;
   // P buffers: the transposed softmax double-buffers P^T; with rows on M one buffer suffices
   // (a thread writes P(u + 1) only after its tile's math, long after PV(u) has read P(u))
@@ -184,6 +196,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(&bar_iempty[i], ROWS ? 1 + kRowSoftmaxThreads : 2);
     }
     if constexpr (ROWS) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(&bar_sready[s], 1);
       for (int q = 0; q < 4; ++q) {
         mbar_init(&bar_pair[q][0], 64);
         mbar_init(&bar_pair[q][1], 64);
@@ -199,7 +212,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     tmem_alloc(&tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 2 + kSoftmax / 32) {
     // zero the padding rows of the Q operand (rows >= rows_per_group); TMA never writes them
     const int rows = p.rows_per_group;
     const int t = threadIdx.x - 64;
@@ -307,15 +320,26 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int npg = min(kTile / kPage, (it.t_end - tok0 + kPage - 1) / kPage);
         // lane q < 16 copies half q / 8 of page q % 8 of the tile: one box per lane, so the
         // stage's 16 copies issue in parallel (a thread's copies issue one after another)
-        const int pg = lane & 7, hf = (lane >> 3) & 1;
-        const int id = (lane < 16 && pg < npg) ? s_pid[pbuf][j * (kTile / kPage) + pg] : -1;
+        const int pg = lane & 7, hf = ROWS ? 0 : (lane >> 3) & 1;
+        const int id = (lane < (ROWS ? 8 : 16) && pg < npg) ? s_pid[pbuf][j * (kTile / kPage) + pg]
+                                                            : -1;
         const uint32_t have = __ballot_sync(0xffffffffu, lane < 8 && id >= 0);
         uint8_t* stage = sKV + st * kStageBytes;
+        if constexpr (ROWS) {
+          if (lane < 8) s_sinfo[st].id[lane] = id;
+          if (lane == 0) {
+            s_sinfo[st].pass = pass;
+            s_sinfo[st].kvh = it.kvh;
+            s_sinfo[st].end = 0;
+          }
+          __syncwarp();
+        }
         if (lane == 0) {
           if (have)
             mbar_arrive_expect_tx(&bar_full[st], static_cast<uint32_t>(__popc(have)) * 4096u);
           else
             mbar_arrive(&bar_full[st]);
+          if constexpr (ROWS) mbar_arrive(&bar_sready[st]);   // half 1 to the second issuer
         }
         __syncwarp();
         if (id >= 0)
@@ -381,6 +405,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         have_pend = have_pend2;
       }
     }
+    if constexpr (ROWS) {
+      // tell the second issuer that no stage follows (once the next stage is free)
+      if (lane == 0 && ok && mbar_wait(&bar_empty[st], ph ^ 1, &abort_flag)) {
+        s_sinfo[st].end = 1;
+        mbar_arrive(&bar_sready[st]);
+      }
+      __syncwarp();
+    }
     if (lane == 0) {
       griddep_launch_dependents();  // this CTA takes no more work
       // the last CTA to finish taking work resets the counter for the next launch
@@ -392,6 +424,29 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       if (!ok) {
         for (int s = 0; s < STAGES; ++s) mbar_wait_drain(&bar_full[s], ph ^ (s < st ? 0 : 1));
         if (q_loads > 0) mbar_wait_drain(&bar_qfull, (q_loads - 1) & 1);
+      }
+    }
+  } else if (ROWS && warp == kRowIssueWarp) {
+    // ================================================= second K/V copy issuer (rows on M)
+    // Follows the ring stage by stage: once the producer has armed a stage and described it,
+    // lanes 0-7 copy half 1 (head dims 64-127) of its pages.
+    const uint64_t kv_policy = l2_policy_evict_first();
+    int st = 0;
+    uint32_t ph = 0;
+    while (mbar_wait(&bar_sready[st], ph, &abort_flag)) {
+      const StageInfo& si = s_sinfo[st];
+      if (si.end) break;
+      if (lane < kTile / kPage) {
+        const int id = si.id[lane];
+        if (id >= 0)
+          tma_load_4d_hint(sKV + st * kStageBytes + kHalfBytes + lane * 2048,
+                           si.pass == 0 ? &tm_k : &tm_v, &bar_full[st], 64, si.kvh, 0, id,
+                           kv_policy);
+      }
+      __syncwarp();
+      if (++st == STAGES) {
+        st = 0;
+        ph ^= 1;
       }
     }
   } else if (warp == 1) {
