@@ -386,9 +386,12 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
     resident device state (the cache holds every sequence's prefix); every step copies its own
     inputs host->device (q, the block's new K/V, the hidden rows, the mask), writes the block
     K/V into the cache, runs attention, the LM head fused with confidence/commit and the mask
-    update, and copies tok/conf/commit back."""
+    update, and copies tok/conf/commit back.  As in a serving loop, the inputs are
+    double-buffered on the device and step k+1's host->device copies run on a copy stream while
+    step k computes (events order each buffer's copy after the step that last read it)."""
     import torch
     stream = torch.cuda.Stream(device=device)
+    copy_stream = torch.cuda.Stream(device=device)
     rng = np.random.default_rng(seed)
     B, L = a.B, a.L
     k_new = W._normal_bf16(rng, (B, L, a.Hkv, a.D), 0.5)
@@ -400,7 +403,9 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
         "hid": torch.from_numpy(lm.hidden.view(np.int16)).pin_memory(),
         "mk": torch.from_numpy(ci.mask).pin_memory(),
     }
-    d = {k: torch.empty_like(v, device=device) for k, v in h.items()}
+    dbuf = [{k: torch.empty_like(v, device=device) for k, v in h.items()} for _ in range(2)]
+    copied = [torch.cuda.Event(), torch.cuda.Event()]   # buffer i holds its step's inputs
+    used = [None, None]                                 # the step that last read buffer i
     kp, vp = _bf16(a.k_ref, device), _bf16(a.v_ref, device)      # resident cache
     pt = torch.from_numpy(a.page_table_ref).to(device)
     pl = torch.from_numpy(a.prefix_lens).to(device)
@@ -414,30 +419,47 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
     h2d = sum(v.numel() * v.element_size() for v in h.values())
     d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
 
-    def one():
-        s = stream.cuda_stream
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
-        bf = torch.bfloat16
-        lib.bdlm_write_block_kv(desc, d["kn"].view(bf), d["vn"].view(bf), kp, vp, pt, pl, s)
-        lib.bdlm_block_attention(desc, d["q"].view(bf), kp, vp, pt, pl, L, out, s)
-        lib.bdlm_lm_head_commit(d["hid"].view(bf), w, d["mk"], None, B, L, lm.H, ci.V,
-                                lib.BDLM_COMMIT_THRESHOLD, 1, ci.threshold, ci.temperature,
-                                outs_d["tok"], outs_d["conf"], outs_d["com"], None, s)
-        lib.bdlm_apply_commit(d["mk"], outs_d["com"], B * L, s)
-        for k in outs_h:
-            outs_h[k].copy_(outs_d[k], non_blocking=True)
+    def upload(i):
+        if used[i] is not None:
+            copy_stream.wait_event(used[i])
+        with torch.cuda.stream(copy_stream):
+            for k in h:
+                dbuf[i][k].copy_(h[k], non_blocking=True)
+        copied[i].record(copy_stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            one()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            one()
-        e1.record(stream)
-        stream.synchronize()
+    def compute(i):
+        d = dbuf[i]
+        s = stream.cuda_stream
+        stream.wait_event(copied[i])
+        with torch.cuda.stream(stream):
+            bf = torch.bfloat16
+            lib.bdlm_write_block_kv(desc, d["kn"].view(bf), d["vn"].view(bf), kp, vp, pt, pl, s)
+            lib.bdlm_block_attention(desc, d["q"].view(bf), kp, vp, pt, pl, L, out, s)
+            lib.bdlm_lm_head_commit(d["hid"].view(bf), w, d["mk"], None, B, L, lm.H, ci.V,
+                                    lib.BDLM_COMMIT_THRESHOLD, 1, ci.threshold, ci.temperature,
+                                    outs_d["tok"], outs_d["conf"], outs_d["com"], None, s)
+            lib.bdlm_apply_commit(d["mk"], outs_d["com"], B * L, s)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            used[i] = ev
+            for k in outs_h:
+                outs_h[k].copy_(outs_d[k], non_blocking=True)
+
+    def run(n):
+        upload(0)
+        for t in range(n):
+            if t + 1 < n:
+                upload((t + 1) % 2)
+            compute(t % 2)
+
+    run(warmup)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_event(e0)   # the first step's copies start inside the timed region
+    run(steps)
+    e1.record(stream)            # after the last step's compute and its device->host read
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     del w, kp, vp
     return ms, h2d, d2h
@@ -795,7 +817,9 @@ def run_ours(args, rank, world, local):
                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                        "ms_per_step": e2e_max,
                        "note": "per rank and step: q, the block's new K/V, hidden rows and "
-                               "mask copied in from pinned host memory, the block K/V written "
+                               "mask copied in from pinned host memory (double-buffered on a "
+                               "copy stream, overlapping the previous step's compute), the "
+                               "block K/V written "
                                "into the resident cache, attention, fused LM head + commit, "
                                "mask update, tok/conf/commit copied back; the paged cache "
                                "(every prefix) and W are resident"}
