@@ -117,8 +117,10 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
  * Layouts: q, out [B, prompt_len, Hq, D]; k_new, v_new [B, prompt_len, Hkv, D] (written to
  * the slots prefix_lens[b] .. + prompt_len - 1); pools, page_table, prefix_lens as
  * bdlm_block_attention; prefix_lens[b] + prompt_len must fit the page table.  bf16 pointers
- * 16-byte aligned.  Runs as the K/V write followed by bdlm_block_attention over B *
- * (prompt_len / L) block sequences that share their sequence's page-table row.
+ * 16-byte aligned.  Runs as the K/V write followed by the block attention over chunks of Lq
+ * prompt tokens (the largest multiple of L dividing prompt_len with Lq * Hq / Hkv <= 128 query
+ * rows, or L), each chunk reading the K/V before its end once with the block-causal mask
+ * applied inside it; the chunks share their sequence's page-table row.
  */
 int bdlm_prefill_attention(const bdlm_attn_desc* desc, int prompt_len, const bdlm_bf16* q,
                            const bdlm_bf16* k_new, const bdlm_bf16* v_new, bdlm_bf16* k_pages,
