@@ -126,3 +126,51 @@ def test_bad_page_ids_and_lengths_are_flagged_not_faulted(lib):
     assert lib.bdlm_device_error() & lib.BDLM_DEVERR_LENGTH
     # the library still works afterwards
     check(lib, a)
+
+
+@pytest.mark.parametrize("L", [32, 16])
+def test_rows_on_m_rescale_after_a_sharp_key(lib, L):
+    """More than 32 query rows per KV head (query rows on the UMMA M side).  One key in the
+    third 128-token tile is planted as 3x a query of its KV head, so that row's max rises
+    far above the first tiles' and the kernel must rescale the row's output before the next
+    PV product; every other row keeps the lazily kept max."""
+    rng = np.random.default_rng(515)
+    B, Hq, Hkv = 2, 32, 8
+    G = Hq // Hkv
+    a = W.make_attention(rng, B, L, Hq, Hkv, 128, prefix_range=(600, 900))
+    for b in range(B):
+        for g in (1, 6):
+            t = 300 + 7 * g                                  # a prefix token in the third tile
+            r = a.page_table_ref[b, t // 16]
+            qf = W.bf16_bits_to_f32(a.q[b, 3, g * G + 1])
+            a.k_ref[r, t % 16, g] = W.f32_to_bf16_bits(3.0 * qf)
+    check(lib, a)
+
+
+def test_prefill_chunk_across_a_split_boundary(lib):
+    """Block prefill whose cached prefix ends just before a 2048-token KV split boundary: in
+    the chunk that straddles it, the queries of the first blocks see no key of the second
+    split (their partial is empty: max -inf, sum 0) and the merge must ignore it."""
+    import torch
+    from gpu_util import host
+    rng = np.random.default_rng(2048)
+    B, L, Hq, Hkv, n = 2, 4, 32, 8, 64
+    lens = np.array([2040, 2028])
+    a = W.make_attention(rng, B, n, Hq, Hkv, 128, prefix_lens=lens, poison=False)
+    q = W._normal_bf16(rng, (B, n, Hq, 128), 0.5)
+    kn = W._normal_bf16(rng, (B, n, Hkv, 128), 0.5)
+    vn = W._normal_bf16(rng, (B, n, Hkv, 128), 0.5)
+    kp, vp = bf16_tensor(a.k_ref), bf16_tensor(a.v_ref)
+    out = torch.full((B, n, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    desc = lib.attn_desc(B, L, Hq, Hkv, 128, a.page_table_ref.shape[1], a.k_ref.shape[0])
+    lib.bdlm_prefill_attention(desc, n, bf16_tensor(q), bf16_tensor(kn), bf16_tensor(vn), kp, vp,
+                               dev(a.page_table_ref), dev(a.prefix_lens), out)
+    torch.cuda.synchronize()
+    ref, k_ref, _ = oracle.prefill_attention(q, kn, vn, a.k_ref, a.v_ref, a.page_table_ref,
+                                             a.prefix_lens, L, Hq, Hkv, 128)
+    assert np.array_equal(host(kp.view(torch.int16)).view(np.uint16), k_ref)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    excess = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
+    assert excess.max() <= 0, f"max excess {excess.max()}"
+    assert lib.bdlm_device_error() == 0
