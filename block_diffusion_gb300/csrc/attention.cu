@@ -137,11 +137,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = base;                          // 2 halves x N rows x 128 B
-  uint8_t* sKV = sQ + N * 256;                 // STAGES x 32 KB
+  // Q buffers: one for the transposed mode (4 KB at N = 16: two CTAs per SM leave no room for
+  // another); with rows on M two, so the next item's Q lands while this item finishes
+  constexpr int kQBufs = ROWS ? 2 : 1;
+  uint8_t* sQ = base;                          // kQBufs x 2 halves x N rows x 128 B
+  uint8_t* sKV = sQ + kQBufs * N * 256;        // STAGES x 32 KB
   uint8_t* sP = sKV + STAGES * kStageBytes;    // 1 or 2 buffers x (2 K-atoms x N rows x 128 B)
 
-  __shared__ uint64_t bar_qfull, bar_qempty, bar_full[STAGES], bar_empty[STAGES];
+  __shared__ uint64_t bar_qfull[kQBufs], bar_qempty[kQBufs], bar_full[STAGES], bar_empty[STAGES];
   __shared__ uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_pempty[2];
   __shared__ uint64_t bar_oready, bar_ofull[2], bar_done;  // bar_ofull: PV of chunk u, by parity
   __shared__ uint64_t bar_ifull[kItemRing], bar_iempty[kItemRing];
@@ -174,8 +177,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
   // ---- setup
   if (threadIdx.x == 0) {
-    mbar_init(&bar_qfull, 1);
-    mbar_init(&bar_qempty, 1);
+    for (int b = 0; b < kQBufs; ++b) {
+      mbar_init(&bar_qfull[b], 1);
+      mbar_init(&bar_qempty[b], 1);
+    }
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
@@ -217,8 +222,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int rows = p.rows_per_group;
     const int t = threadIdx.x - 64;
     for (int o = t * 16; o < (N - rows) * 128; o += kSoftmax * 16) {
-      *reinterpret_cast<uint4*>(sQ + rows * 128 + o) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sQ + N * 128 + rows * 128 + o) = make_uint4(0, 0, 0, 0);
+      for (int b = 0; b < kQBufs; ++b) {
+        *reinterpret_cast<uint4*>(sQ + b * N * 256 + rows * 128 + o) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sQ + b * N * 256 + N * 128 + rows * 128 + o) =
+            make_uint4(0, 0, 0, 0);
+      }
     }
     fence_proxy_async_smem();
   }
@@ -285,15 +293,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // K/V pages are read exactly once: first to leave L2, so that the split partials (and Q)
     // stay resident for the merge
     const uint64_t kv_policy = l2_policy_evict_first();
-    // Loads the Q tile of item `it` (sequence number s) into the single Q buffer once the
-    // previous item's S^T MMAs are done with it.  Lane 0.
+    // Loads the Q tile of item `it` (sequence number s) into Q buffer s % kQBufs once the S
+    // MMAs of the item that used it before are done with it.  Lane 0.
     int q_loads = 0;
     auto load_q = [&](const Item& it, int s) {
-      if (ok) ok = mbar_wait(&bar_qempty, (s & 1) ^ 1, &abort_flag);
+      const int b = s % kQBufs;
+      if (ok) ok = mbar_wait(&bar_qempty[b], ((s / kQBufs) & 1) ^ 1, &abort_flag);
       if (!ok) return;
-      mbar_arrive_expect_tx(&bar_qfull, 2u * 128u * static_cast<uint32_t>(p.G * p.lsub));
+      mbar_arrive_expect_tx(&bar_qfull[b], 2u * 128u * static_cast<uint32_t>(p.G * p.lsub));
       for (int h = 0; h < 2; ++h)
-        tma_load_3d(sQ + h * N * 128, &tm_q, &bar_qfull, h * 64, it.kvh * p.G,
+        tma_load_3d(sQ + b * N * 256 + h * N * 128, &tm_q, &bar_qfull[b], h * 64, it.kvh * p.G,
                     it.b * p.L + it.rg * p.lsub);
       ++q_loads;
     };
@@ -423,7 +432,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       if (!ok) {
         for (int s = 0; s < STAGES; ++s) mbar_wait_drain(&bar_full[s], ph ^ (s < st ? 0 : 1));
-        if (q_loads > 0) mbar_wait_drain(&bar_qfull, (q_loads - 1) & 1);
+        for (int s = max(0, q_loads - kQBufs); s < q_loads; ++s)
+          mbar_wait_drain(&bar_qfull[s % kQBufs], (s / kQBufs) & 1);
       }
     }
   } else if (ROWS && warp == kRowIssueWarp) {
@@ -467,7 +477,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       // S^T of chunk `c` of `it` (global chunk number u) into S buffer u & 1
       auto do_s = [&](const Item& it, int c, int u, int seq) {
         if (!(ok = ok && mbar_wait(&bar_sfree[u & 1], ((u >> 1) & 1) ^ 1, &abort_flag))) return;
-        if (c == 0 && !(ok = mbar_wait(&bar_qfull, seq & 1, &abort_flag))) return;
+        const int qb = seq % kQBufs;
+        if (c == 0 && !(ok = mbar_wait(&bar_qfull[qb], (seq / kQBufs) & 1, &abort_flag))) return;
         tc_fence_after();
         const uint32_t tS = tmem + static_cast<uint32_t>((u & 1) * p.chunk_tiles * N);
         const int j0 = c * p.chunk_tiles;
@@ -480,7 +491,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t ad = smem_desc(ka + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
             const uint64_t bd =
-                smem_desc(q_addr + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+                smem_desc(q_addr + qb * N * 256 + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
             if constexpr (ROWS)
               umma_bf16(tS + (j - j0) * N, bd, ad, kIdescS, kk > 0 ? 1u : 0u);
             else
@@ -493,7 +504,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
         }
         umma_commit(&bar_sfull[u & 1]);
-        if (c == it.n_chunks - 1) umma_commit(&bar_qempty);  // Q no longer needed
+        if (c == it.n_chunks - 1) umma_commit(&bar_qempty[qb]);  // Q no longer needed
       };
       // O^T += V^T P^T over the tiles of chunk `c`
       auto do_pv = [&](const Item& it, int c, int u) {
@@ -1144,8 +1155,8 @@ attn_merge_kernel(const AttnParams p, int N) {
 
 template <int N, int STAGES, bool ROWS>
 constexpr size_t smem_bytes() {
-  return 1024 + static_cast<size_t>(N) * 256 + static_cast<size_t>(STAGES) * kStageBytes +
-         static_cast<size_t>(ROWS ? 1 : 2) * N * 256;
+  return 1024 + static_cast<size_t>(ROWS ? 2 : 1) * N * 256 +
+         static_cast<size_t>(STAGES) * kStageBytes + static_cast<size_t>(ROWS ? 1 : 2) * N * 256;
 }
 
 template <int N, int STAGES, int CPS, bool MASKED, bool ROWS>
@@ -1289,8 +1300,8 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
       e = launch_t<32, 2, 2, false, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     case 128:
-      e = mask_block > 0 ? launch_t<128, 4, 1, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream)
-                         : launch_t<128, 4, 1, false, true>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      e = mask_block > 0 ? launch_t<128, 3, 1, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream)
+                         : launch_t<128, 3, 1, false, true>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     default: return cudaErrorInvalidValue;
   }
