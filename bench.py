@@ -640,10 +640,10 @@ def prefill_bench(bd, device, flush, reps: int, seed: int, B=128, n=512, L=4):
     assert bd.bdlm_device_error() == 0
     ms = float(np.mean([x.elapsed_time(y) for x, y in evs]))
     # the library cuts the prompt into chunks of Lq queries (the largest multiple of L dividing n
-    # with Lq * G <= 128 rows), block-causal inside a chunk; chunk c reads the K/V of the
+    # with Lq * G <= 256 rows), block-causal inside a chunk; chunk c reads the K/V of the
     # (c + 1) * Lq tokens up to its end once per KV head
     G = Hq // Hkv
-    Lq = max([c for c in range(L, n + 1, L) if n % c == 0 and c * G <= 128] or [L])
+    Lq = max([c for c in range(L, n + 1, L) if n % c == 0 and c * G <= 256] or [L])
     if Lq * G <= 32:
         Lq = L
     nq = n // Lq

@@ -265,12 +265,13 @@ int bdlm_prefill_attention(const bdlm_attn_desc* desc, int prompt_len, const bdl
       !aligned16(v_pages) || !aligned16(out))
     return BDLM_ERR_INVALID;
   // Queries go to the attention in chunks of Lq positions (a multiple of L dividing the prompt,
-  // Lq * G <= 128 query rows per KV head, the most that fit) with the block-causal mask inside
-  // a chunk, so each chunk reads the K/V before it once; chunks of one block (Lq = L) need no
-  // mask.  Narrow chunks (Lq * G <= 32 rows) stay one block per attention sequence.
+  // Lq * G <= 256 query rows per KV head, the most one attention item takes) with the
+  // block-causal mask inside a chunk, so each chunk reads the K/V before it once; chunks of
+  // one block (Lq = L) need no mask.  Narrow chunks (Lq * G <= 32 rows) stay one block per
+  // attention sequence.
   const int G = d.Hq / d.Hkv;
   int Lq = d.L;
-  for (int c = d.L; c * G <= 128 && c <= prompt_len; c += d.L)
+  for (int c = d.L; c * G <= 256 && c <= prompt_len; c += d.L)
     if (prompt_len % c == 0) Lq = c;
   if (Lq * G <= 32) Lq = d.L;
   const int nb = prompt_len / Lq;

@@ -129,7 +129,7 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   return true;
 }
 
-template <int N, int STAGES, int CTAS_PER_SM, bool MASKED, bool ROWS>
+template <int N, int STAGES, int CTAS_PER_SM, bool MASKED, bool ROWS, bool TWO>
 __global__ void __launch_bounds__(ROWS ? kRowThreads : kThreads, CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -137,11 +137,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  // With rows on M an item has one or two (TWO) sub-groups of 128 query rows; they share every
+  // K/V stage, each with its own S and O in tensor memory.
+  constexpr int kSub = TWO ? 2 : 1;
+  constexpr int kRowsItem = N * kSub;          // query rows of an item
   // Q buffers: one for the transposed mode (4 KB at N = 16: two CTAs per SM leave no room for
-  // another); with rows on M two, so the next item's Q lands while this item finishes
-  constexpr int kQBufs = ROWS ? 2 : 1;
-  uint8_t* sQ = base;                          // kQBufs x 2 halves x N rows x 128 B
-  uint8_t* sKV = sQ + kQBufs * N * 256;        // STAGES x 32 KB
+  // another) and for two sub-groups (64 KB); otherwise two, so the next item's Q lands while
+  // this item finishes
+  constexpr int kQBufs = ROWS && !TWO ? 2 : 1;
+  uint8_t* sQ = base;                          // kQBufs x 2 halves x kRowsItem rows x 128 B
+  uint8_t* sKV = sQ + kQBufs * kRowsItem * 256;   // STAGES x 32 KB
   uint8_t* sP = sKV + STAGES * kStageBytes;    // 1 or 2 buffers x (2 K-atoms x N rows x 128 B)
 
   __shared__ uint64_t bar_qfull[kQBufs], bar_qempty[kQBufs], bar_full[STAGES], bar_empty[STAGES];
@@ -158,7 +163,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ int s_pflag[2];  // P buffer: its tile starts a chunk whose PV waits for a rescale
   __shared__ float s_red[4][kCols];
   __shared__ float s_hmax[ROWS ? 2 : 1][2][ROWS ? N : 1];   // half-row maxima by tile parity
-  __shared__ float s_hsum[2][ROWS ? N : 1];                 // half-row sums at an item's end
+  __shared__ float s_hsum[2][2][ROWS ? N : 1];              // half-row sums, by exchange parity
   __shared__ uint64_t bar_pair[ROWS ? 4 : 1][2], bar_pair_end[ROWS ? 4 : 1];   // halves of a row
   // rows on M: the producer issues half 0 of each stage's page boxes and hands the stage to a
   // second issuer warp for half 1 (one warp's copies issue at about 1 us per 16 boxes)
@@ -170,6 +175,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   constexpr int kPBufs = ROWS ? 1 : 2;
   static_assert(!MASKED || ROWS, "the block-causal mask is applied by the row-per-thread softmax");
   static_assert(!ROWS || N == 128, "rows on M: one UMMA of 128 query rows");
+  static_assert(!TWO || ROWS, "two sub-groups only with rows on M");
   static_assert(ROWS || N <= 32, "keys on M: at most 32 query rows on N");
 
   const int warp = threadIdx.x >> 5;
@@ -221,10 +227,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // zero the padding rows of the Q operand (rows >= rows_per_group); TMA never writes them
     const int rows = p.rows_per_group;
     const int t = threadIdx.x - 64;
-    for (int o = t * 16; o < (N - rows) * 128; o += kSoftmax * 16) {
+    for (int o = t * 16; o < (kRowsItem - rows) * 128; o += kSoftmax * 16) {
       for (int b = 0; b < kQBufs; ++b) {
-        *reinterpret_cast<uint4*>(sQ + b * N * 256 + rows * 128 + o) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sQ + b * N * 256 + N * 128 + rows * 128 + o) =
+        *reinterpret_cast<uint4*>(sQ + b * kRowsItem * 256 + rows * 128 + o) =
+            make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sQ + b * kRowsItem * 256 + kRowsItem * 128 + rows * 128 + o) =
             make_uint4(0, 0, 0, 0);
       }
     }
@@ -302,8 +309,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       if (!ok) return;
       mbar_arrive_expect_tx(&bar_qfull[b], 2u * 128u * static_cast<uint32_t>(p.G * p.lsub));
       for (int h = 0; h < 2; ++h)
-        tma_load_3d(sQ + b * N * 256 + h * N * 128, &tm_q, &bar_qfull[b], h * 64, it.kvh * p.G,
-                    it.b * p.L + it.rg * p.lsub);
+        tma_load_3d(sQ + b * kRowsItem * 256 + h * kRowsItem * 128, &tm_q, &bar_qfull[b], h * 64,
+                    it.kvh * p.G, it.b * p.L + it.rg * p.lsub);
       ++q_loads;
     };
     // Streams the K (pass 0) or V (pass 1) tiles of chunk c of item `it` (page ids in
@@ -474,28 +481,39 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       int st = 0;
       uint32_t ph = 0;
       int pcount = 0, ocount = 0;
-      // S^T of chunk `c` of `it` (global chunk number u) into S buffer u & 1
+      // S of chunk `c` of `it` (global chunk number u): into S buffer u & 1, or with two
+      // sub-groups into sub-group x's buffer x (one tile per chunk)
       auto do_s = [&](const Item& it, int c, int u, int seq) {
-        if (!(ok = ok && mbar_wait(&bar_sfree[u & 1], ((u >> 1) & 1) ^ 1, &abort_flag))) return;
+        if constexpr (!TWO)
+          if (!(ok = ok && mbar_wait(&bar_sfree[u & 1], ((u >> 1) & 1) ^ 1, &abort_flag))) return;
         const int qb = seq % kQBufs;
         if (c == 0 && !(ok = mbar_wait(&bar_qfull[qb], (seq / kQBufs) & 1, &abort_flag))) return;
         tc_fence_after();
-        const uint32_t tS = tmem + static_cast<uint32_t>((u & 1) * p.chunk_tiles * N);
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
           if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
           tc_fence_after();
           const uint32_t ka = kv_addr + st * kStageBytes;
+          for (int x = 0; x < kSub; ++x) {
+            const int sb = kSub == 1 ? (u & 1) : x;
+            // a sub-group's S buffer is free once the softmax has read its previous tile
+            if constexpr (TWO)
+              if (!(ok = ok && mbar_wait(&bar_sfree[sb], (u & 1) ^ 1, &abort_flag))) return;
+            const uint32_t tS = tmem + static_cast<uint32_t>(sb * p.chunk_tiles * N);
+            const uint32_t qa = q_addr + qb * kRowsItem * 256 + x * N * 128;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = smem_desc(ka + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                smem_desc(q_addr + qb * N * 256 + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-            if constexpr (ROWS)
-              umma_bf16(tS + (j - j0) * N, bd, ad, kIdescS, kk > 0 ? 1u : 0u);
-            else
-              umma_bf16(tS + (j - j0) * N, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad =
+                  smem_desc(ka + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd =
+                  smem_desc(qa + (kk >> 2) * (kRowsItem * 128) + (kk & 3) * 32, 16, 1024);
+              if constexpr (ROWS)
+                umma_bf16(tS + (j - j0) * N, bd, ad, kIdescS, kk > 0 ? 1u : 0u);
+              else
+                umma_bf16(tS + (j - j0) * N, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            if constexpr (TWO) umma_commit(&bar_sfull[sb]);   // this sub-group's S is ready
           }
           umma_commit(&bar_empty[st]);
           if (++st == STAGES) {
@@ -503,22 +521,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             ph ^= 1;
           }
         }
-        umma_commit(&bar_sfull[u & 1]);
+        if constexpr (!TWO) umma_commit(&bar_sfull[u & 1]);
         if (c == it.n_chunks - 1) umma_commit(&bar_qempty[qb]);  // Q no longer needed
       };
-      // O^T += V^T P^T over the tiles of chunk `c`
+      // O^T += V^T P^T (O += P V) over the tiles of chunk `c`, for each sub-group
       auto do_pv = [&](const Item& it, int c, int u) {
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
-          const int pb = pcount % kPBufs;
           if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
-          if (!(ok = mbar_wait(&bar_pfull[pb], (pcount / kPBufs) & 1, &abort_flag))) return;
-          if (c > 0 && j == j0 && s_pflag[pb]) {  // the softmax rescales O^T first
-            if (!(ok = mbar_wait(&bar_oready, ocount & 1, &abort_flag))) return;
-            ++ocount;
-          }
-          tc_fence_after();
           const int tok0 = it.t_begin + j * kTile;
           const int valid = min(kTile, it.t_end - tok0);
           const int npg = (valid + kPage - 1) / kPage;
@@ -534,18 +545,29 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             fence_proxy_async_smem();
           }
           const uint32_t va = kv_addr + st * kStageBytes;
-          const uint32_t pa = p_addr + pb * (N * 256);
-          for (int q = 0; q < npg; ++q) {
-            const uint64_t ad = smem_desc(va + q * 2048, kHalfBytes, 1024);
-            const uint64_t bd = smem_desc(pa + (q >> 2) * (N * 128) + (q & 3) * 32, 16, 1024);
-            if constexpr (ROWS)
-              umma_bf16(tO, bd, ad, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
-            else
-              umma_bf16(tO, ad, bd, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
+          for (int x = 0; x < kSub; ++x) {
+            const int pb = pcount % kPBufs;
+            if (!(ok = mbar_wait(&bar_pfull[pb], (pcount / kPBufs) & 1, &abort_flag))) return;
+            if constexpr (!ROWS) {
+              if (c > 0 && j == j0 && s_pflag[pb]) {  // the softmax rescales O^T first
+                if (!(ok = mbar_wait(&bar_oready, ocount & 1, &abort_flag))) return;
+                ++ocount;
+              }
+            }
+            tc_fence_after();
+            const uint32_t pa = p_addr + pb * (N * 256);
+            for (int q = 0; q < npg; ++q) {
+              const uint64_t ad = smem_desc(va + q * 2048, kHalfBytes, 1024);
+              const uint64_t bd = smem_desc(pa + (q >> 2) * (N * 128) + (q & 3) * 32, 16, 1024);
+              if constexpr (ROWS)
+                umma_bf16(tO + x * N, bd, ad, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
+              else
+                umma_bf16(tO, ad, bd, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
+            }
+            umma_commit(&bar_pempty[pb]);
+            ++pcount;
           }
           umma_commit(&bar_empty[st]);
-          umma_commit(&bar_pempty[pb]);
-          ++pcount;
           if (++st == STAGES) {
             st = 0;
             ph ^= 1;
@@ -574,6 +596,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             nxt = s_item[rs];
             has_next = !nxt.end;
           }
+          // S(u + 1) ahead of PV(u), so the softmax can start the next tile while PV runs
           if (has_next) do_s(nxt, nc, u + 1, nseq);
           if (!ok) break;
           do_pv(cur, c, u);
@@ -590,11 +613,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     }
   } else if constexpr (ROWS) {
     // ====================================================== softmax/epilogue, a row per 2 threads
-    // Query row n of the item is tensor-memory lane n: row n of S(u) holds its 128 scores of
-    // tile u, row n of O its 128 head dims.  Two warps share each lane quadrant, so each row
-    // has two threads: half 0 takes columns 0-63, half 1 columns 64-127 (of S, then of O).
-    // They exchange the half-row maxima every tile and the half sums at the end; one tile per
-    // chunk (N = 128 leaves room for two S buffers and O).
+    // Query row x * 128 + n of the item (sub-group x) is tensor-memory lane n of sub-group x's
+    // S and O.  Two warps share each lane quadrant, so each row has two threads: half 0 takes
+    // columns 0-63, half 1 columns 64-127 (of S, then of O).  They exchange the half-row maxima
+    // every tile and the half sums at the end.  One tile per chunk; with two sub-groups the
+    // threads take sub-group 0, then 1, of every tile.
     const int q4 = warp & 3;
     const int half = (warp - 2) >> 2;
     const int n = (q4 << 5) | lane;
@@ -602,160 +625,180 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t col0 = static_cast<uint32_t>(half * 64);
     const float cs = p.scale_log2;
     bool ok = true;
-    int pcount = 0, u = 0, pair_ends = 0;
+    int pcount = 0, u = 0, pe = 0, pair_ends = 0;   // pe, pair_ends: exchanges so far
     for (int seq = 0; ok; ++seq) {
       const int rs = seq % kItemRing;
       if (!(ok = mbar_wait(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
       const Item it = s_item[rs];
       mbar_arrive(&bar_iempty[rs]);   // the descriptor is in registers: its slot may be reused
       if (it.end) break;
-      const int i_row = it.rg * p.lsub + n / p.G;   // block position of the row
-      int lim = 0x7FFFFFFF;                         // keys past q0 the row may see
-      if constexpr (MASKED) lim = (i_row / p.mask_block + 1) * p.mask_block;
-      float m_run = -CUDART_INF_F, l_run = 0.f;     // l_run: this half's sum
+      int i_row[kSub], lim[kSub];   // block position of the row; keys past q0 it may see
+      float m_run[kSub], l_run[kSub];   // l_run: this half's sum
+#pragma unroll
+      for (int x = 0; x < kSub; ++x) {
+        i_row[x] = it.rg * p.lsub + (x * N + n) / p.G;
+        lim[x] = 0x7FFFFFFF;
+        if constexpr (MASKED) lim[x] = (i_row[x] / p.mask_block + 1) * p.mask_block;
+        m_run[x] = -CUDART_INF_F;
+        l_run[x] = 0.f;
+      }
       for (int c = 0; c < it.n_chunks && ok; ++c, ++u) {
-        const uint32_t tS = tmem + lane_off + static_cast<uint32_t>((u & 1) * N) + col0;
-        if (!(ok = mbar_wait(&bar_sfull[u & 1], (u >> 1) & 1, &abort_flag))) break;
-        tc_fence_after();
-        uint32_t r[64];
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-          tmem_ld16(tS + g * 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * g));
-        tmem_wait_ld();
-#pragma unroll
-        for (int g = 0; g < 4; ++g) tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + 16 * g));
-        tc_fence_before();
-        mbar_arrive(&bar_sfree[u & 1]);   // S(u) is in registers: the buffer may take S(u + 2)
-        // keys of the tile the row sees: a prefix of it (sequence end, block-causal limit);
-        // the others read as -inf
         const int key0 = it.t_begin + c * kTile;
-        int nvalid = min(kTile, it.t_end - key0);
-        if constexpr (MASKED) nvalid = min(nvalid, lim - (key0 - it.q0));
-        nvalid -= half * 64;   // of this half's columns
-        if (nvalid < 64) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (k >= nvalid) r[k] = 0xFF800000u;
-        }
-        // half-row max (a tree, so the warp has work in flight), then the row max
-        float t[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          t[k] = fmaxf(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
-#pragma unroll
-        for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-          for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
-        s_hmax[u & 1][half][n] = t[0];
-        mbar_arrive(&bar_pair[q4][u & 1]);
-        if (!(ok = mbar_wait(&bar_pair[q4][u & 1], (u >> 1) & 1, &abort_flag))) break;
-        const float mx = fmaxf(s_hmax[u & 1][0][n], s_hmax[u & 1][1][n]);
-        // the running max moves only when the tile raises it by more than 2^kLazyRescale
-        // (both halves of a row take the same decision)
-        float alpha = 1.f;
-        bool resc = false;
-        if (m_run == -CUDART_INF_F) {
-          m_run = mx;
-        } else if ((mx - m_run) * cs > kLazyRescale) {
-          alpha = ex2((m_run - mx) * cs);
-          m_run = mx;
-          resc = true;
-        }
-        // p = 2^(s cs - m cs): scaling two scores per packed FMA, the exponentials independent,
-        // the sum a tree of packed adds (a row that has seen no key yet has m = -inf: p = 0)
-        const float mc = m_run == -CUDART_INF_F ? 0.f : m_run * cs;
-        const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-mc, -mc);
-        float2 e[32];
-        uint32_t pk[32];   // this half of the row's P as bf16 pairs
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float2 y = __ffma2_rn(
-              make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), cs2, nm2);
-          e[k] = make_float2(ex2(y.x), ex2(y.y));
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[k].x, e[k].y);
-          pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-#pragma unroll
-        for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-          for (int k = 0; k < w; ++k) e[k] = __fadd2_rn(e[k], e[k + w]);
-        l_run = l_run * alpha + (e[0].x + e[0].y);
-        if (__any_sync(0xffffffffu, resc)) {
-          // bring this warp's half of its rows of O to the new maxima once the previous
-          // tile's PV is done
-          if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+        for (int x = 0; x < kSub; ++x) {
+          const int sb = kSub == 1 ? (u & 1) : x;
+          const uint32_t sph = kSub == 1 ? ((u >> 1) & 1) : (u & 1);
+          const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(sb * N) + col0;
+          if (!(ok = mbar_wait(&bar_sfull[sb], sph, &abort_flag))) break;
           tc_fence_after();
+          uint32_t r[64];
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            tmem_ld16(tS + g * 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * g));
+          tmem_wait_ld();
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + 16 * g));
+          tc_fence_before();
+          mbar_arrive(&bar_sfree[sb]);   // S is in registers: the buffer may take the next S
+          // keys of the tile the row sees: a prefix of it (sequence end, block-causal limit);
+          // the others read as -inf
+          int nvalid = min(kTile, it.t_end - key0);
+          if constexpr (MASKED) nvalid = min(nvalid, lim[x] - (key0 - it.q0));
+          nvalid -= half * 64;   // of this half's columns
+          if (nvalid < 64) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (k >= nvalid) r[k] = 0xFF800000u;
+          }
+          // half-row max (a tree, so the warp has work in flight), then the row max
+          float t[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            t[k] = fmaxf(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+#pragma unroll
+          for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+          s_hmax[pe & 1][half][n] = t[0];
+          mbar_arrive(&bar_pair[q4][pe & 1]);
+          if (!(ok = mbar_wait(&bar_pair[q4][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
+          const float mx = fmaxf(s_hmax[pe & 1][0][n], s_hmax[pe & 1][1][n]);
+          ++pe;
+          // the running max moves only when the tile raises it by more than 2^kLazyRescale
+          // (both halves of a row take the same decision)
+          float alpha = 1.f;
+          bool resc = false;
+          if (m_run[x] == -CUDART_INF_F) {
+            m_run[x] = mx;
+          } else if ((mx - m_run[x]) * cs > kLazyRescale) {
+            alpha = ex2((m_run[x] - mx) * cs);
+            m_run[x] = mx;
+            resc = true;
+          }
+          // p = 2^(s cs - m cs): scaling two scores per packed FMA, the exponentials
+          // independent, the sum a tree of packed adds (a row that has seen no key yet has
+          // m = -inf: p = 0)
+          const float mc = m_run[x] == -CUDART_INF_F ? 0.f : m_run[x] * cs;
+          const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-mc, -mc);
+          float2 e[32];
+          uint32_t pk[32];   // this half of the row's P as bf16 pairs
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float2 y = __ffma2_rn(
+                make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), cs2, nm2);
+            e[k] = make_float2(ex2(y.x), ex2(y.y));
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[k].x, e[k].y);
+            pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+#pragma unroll
+          for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) e[k] = __fadd2_rn(e[k], e[k + w]);
+          l_run[x] = l_run[x] * alpha + (e[0].x + e[0].y);
+          if (__any_sync(0xffffffffu, resc)) {
+            // bring this warp's half of its rows of O to the new maxima once the previous
+            // tile's PV is done
+            if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint32_t o[16];
+              tmem_ld16(tO + lane_off + x * N + col0 + g * 16, o);
+              tmem_wait_ld();
+              tmem_regs_ready(o);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st16(tO + lane_off + x * N + col0 + g * 16, o);
+            }
+            tmem_wait_st();
+          }
+          // this half of P row n into the K-major, 128-byte-swizzled operand: keys 64h ..
+          // 64h+63 are its half h
+          const int pb = pcount % kPBufs;
+          if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount / kPBufs) & 1) ^ 1, &abort_flag))) break;
+          uint8_t* prow = sP + pb * (N * 256) + half * (N * 128) + n * 128;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (n & 7)) << 4)) =
+                make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(&bar_pfull[pb]);
+          ++pcount;
+        }
+        if (!ok || c != it.n_chunks - 1) continue;
+        // ---- epilogue of the item: this half of each row of O, divided by the row's sum or
+        // as a split partial
+        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        tc_fence_after();
+        const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
+        float* mine =
+            p.part + (grp * p.max_splits + it.split) * static_cast<size_t>(kRowsItem) * 130;
+#pragma unroll
+        for (int x = 0; x < kSub; ++x) {
+          s_hsum[pair_ends & 1][half][n] = l_run[x];
+          mbar_arrive(&bar_pair_end[q4]);
+          if (!(ok = mbar_wait(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
+          const float l_row = s_hsum[pair_ends & 1][0][n] + s_hsum[pair_ends & 1][1][n];
+          ++pair_ends;
+          const int r_item = x * N + n;   // row of the item
+          const bool live = r_item < p.rows_per_group && i_row[x] < p.L;
+          uint16_t* dst =
+              live ? p.out + ((static_cast<size_t>(it.b) * p.L + i_row[x]) * p.Hq +
+                              static_cast<size_t>(it.kvh) * p.G + r_item % p.G) * 128 + col0
+                   : p.out;
+          const float inv = 1.f / l_row;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint32_t o[16];
-            tmem_ld16(tO + lane_off + col0 + g * 16, o);
+            tmem_ld16(tO + lane_off + x * N + col0 + g * 16, o);
             tmem_wait_ld();
             tmem_regs_ready(o);
+            if (!live) continue;
+            if (it.n_splits == 1) {
+              uint32_t w[8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st16(tO + lane_off + col0 + g * 16, o);
-          }
-          tmem_wait_st();
-        }
-        // this half of P row n into the K-major, 128-byte-swizzled operand: keys 64h ..
-        // 64h+63 are its half h
-        const int pb = pcount % kPBufs;
-        if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount / kPBufs) & 1) ^ 1, &abort_flag))) break;
-        uint8_t* prow = sP + pb * (N * 256) + half * (N * 128) + n * 128;
+              for (int k = 0; k < 8; ++k) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                    __uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+                w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              uint4* d4 = reinterpret_cast<uint4*>(dst + g * 16);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              float4* d4 = reinterpret_cast<float4*>(mine + r_item * 128 + col0 + g * 16);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(prow + ((ch ^ (n & 7)) << 4)) =
-              make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bar_pfull[pb]);
-        ++pcount;
-        if (c != it.n_chunks - 1) continue;
-        // ---- epilogue of the item: this half of row n of O, divided by the row's sum or as a
-        // split partial
-        s_hsum[half][n] = l_run;
-        mbar_arrive(&bar_pair_end[q4]);
-        if (!(ok = mbar_wait(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
-        ++pair_ends;
-        const float l_row = s_hsum[0][n] + s_hsum[1][n];
-        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
-        tc_fence_after();
-        const bool live = n < p.rows_per_group && i_row < p.L;
-        const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
-        float* mine = p.part + (grp * p.max_splits + it.split) * static_cast<size_t>(N) * 130;
-        uint16_t* dst = live ? p.out + ((static_cast<size_t>(it.b) * p.L + i_row) * p.Hq +
-                                        static_cast<size_t>(it.kvh) * p.G + n % p.G) * 128 + col0
-                             : p.out;
-        const float inv = 1.f / l_row;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t o[16];
-          tmem_ld16(tO + lane_off + col0 + g * 16, o);
-          tmem_wait_ld();
-          tmem_regs_ready(o);
-          if (!live) continue;
-          if (it.n_splits == 1) {
-            uint32_t w[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[2 * k]) * inv,
-                                                              __uint_as_float(o[2 * k + 1]) * inv);
-              w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+              for (int k = 0; k < 4; ++k)
+                d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                    __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
             }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + g * 16);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else {
-            float4* d4 = reinterpret_cast<float4*>(mine + n * 128 + col0 + g * 16);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                  __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
           }
-        }
-        if (live && it.n_splits > 1 && half == 0) {
-          mine[N * 128 + n] = m_run;
-          mine[N * 128 + N + n] = l_row;
+          if (live && it.n_splits > 1 && half == 0) {
+            mine[kRowsItem * 128 + r_item] = m_run[x];
+            mine[kRowsItem * 128 + kRowsItem + r_item] = l_row;
+          }
         }
         tc_fence_before();   // O is read: the next item's first PV (after its P) may overwrite it
       }
@@ -1153,29 +1196,32 @@ attn_merge_kernel(const AttnParams p, int N) {
   }
 }
 
-template <int N, int STAGES, bool ROWS>
+template <int N, int STAGES, bool ROWS, bool TWO>
 constexpr size_t smem_bytes() {
-  return 1024 + static_cast<size_t>(ROWS ? 2 : 1) * N * 256 +
-         static_cast<size_t>(STAGES) * kStageBytes + static_cast<size_t>(ROWS ? 1 : 2) * N * 256;
+  // Q buffers (as the kernel: two with rows on M and one sub-group), K/V stages, P buffers
+  const size_t q = TWO ? static_cast<size_t>(2) * N * 256
+                       : static_cast<size_t>(ROWS ? 2 : 1) * N * 256;
+  return 1024 + q + static_cast<size_t>(STAGES) * kStageBytes +
+         static_cast<size_t>(ROWS ? 1 : 2) * N * 256;
 }
 
-template <int N, int STAGES, int CPS, bool MASKED, bool ROWS>
+template <int N, int STAGES, int CPS, bool MASKED, bool ROWS, bool TWO>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const AttnParams& prm, int num_sms, cudaStream_t stream) {
-  constexpr size_t smem = smem_bytes<N, STAGES, ROWS>();
+  constexpr size_t smem = smem_bytes<N, STAGES, ROWS, TWO>();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS>,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS>,
+    e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(attn_kernel<N, STAGES, CPS, MASKED, ROWS>, dim3(num_sms * CPS),
+  return launch_pdl(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>, dim3(num_sms * CPS),
                     dim3(ROWS ? kRowThreads : kThreads), smem,
                     stream, tq, tk, tv, prm);
 }
@@ -1212,20 +1258,24 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
   }
   pl.G = Hq / Hkv;
   pl.rows = pl.G * L;
-  if (pl.rows <= 128) {
+  // one item takes up to 256 query rows (two sub-groups of 128 sharing the K/V); more rows
+  // are cut into row groups of 256 that each read the K/V
+  if (pl.rows <= 256) {
     pl.lsub = L;
     pl.row_groups = 1;
   } else {
-    pl.lsub = 128 / pl.G;
+    pl.lsub = 256 / pl.G;
     pl.row_groups = (L + pl.lsub - 1) / pl.lsub;
   }
   const int rpg = pl.G * pl.lsub;
-  // up to 32 query rows: S^T = K Q^T with the rows on N; more: S = Q K^T, 128 rows on M
-  pl.n_mma = rpg <= 16 ? 16 : rpg <= 32 ? 32 : 128;
-  // tensor memory per CTA holds two S^T chunks and O^T
+  // up to 32 query rows: S^T = K Q^T with the rows on N; more: S = Q K^T, 128 rows on M per
+  // sub-group (n_mma = 256: two sub-groups)
+  pl.n_mma = rpg <= 16 ? 16 : rpg <= 32 ? 32 : rpg <= 128 ? 128 : 256;
+  // tensor memory per CTA holds two S^T chunks and O^T (rows on N), two S tiles and O (one
+  // sub-group), or S and O of each of two sub-groups
   const int ctas_per_sm = pl.n_mma <= 32 ? 2 : 1;
   pl.tmem_cols = 512 / ctas_per_sm;
-  pl.chunk_tiles = (pl.tmem_cols - pl.n_mma) / (2 * pl.n_mma);
+  pl.chunk_tiles = pl.n_mma >= 128 ? 1 : (pl.tmem_cols - pl.n_mma) / (2 * pl.n_mma);
   const int chunks_per_split = pl.n_mma == 16 ? 1 : pl.n_mma == 32 ? 3 : 16;
   pl.split_tokens = pl.chunk_tiles * kTile * chunks_per_split;
   if (pl.split_tokens > kMaxSplitTokens) pl.split_tokens = kMaxSplitTokens;
@@ -1293,15 +1343,21 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   switch (plan.n_mma) {
     case 16:
       if (mask_block > 0) return cudaErrorInvalidValue;   // the mask needs rows on M
-      e = launch_t<16, 3, 2, false, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      e = launch_t<16, 3, 2, false, false, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     case 32:
       if (mask_block > 0) return cudaErrorInvalidValue;
-      e = launch_t<32, 2, 2, false, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      e = launch_t<32, 2, 2, false, false, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     case 128:
-      e = mask_block > 0 ? launch_t<128, 3, 1, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream)
-                         : launch_t<128, 3, 1, false, true>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      e = mask_block > 0
+              ? launch_t<128, 3, 1, true, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream)
+              : launch_t<128, 3, 1, false, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+      break;
+    case 256:   // two sub-groups of 128 query rows sharing the K/V
+      e = mask_block > 0
+              ? launch_t<128, 3, 1, true, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream)
+              : launch_t<128, 3, 1, false, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     default: return cudaErrorInvalidValue;
   }

@@ -118,7 +118,7 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
  * the slots prefix_lens[b] .. + prompt_len - 1); pools, page_table, prefix_lens as
  * bdlm_block_attention; prefix_lens[b] + prompt_len must fit the page table.  bf16 pointers
  * 16-byte aligned.  Runs as the K/V write followed by the block attention over chunks of Lq
- * prompt tokens (the largest multiple of L dividing prompt_len with Lq * Hq / Hkv <= 128 query
+ * prompt tokens (the largest multiple of L dividing prompt_len with Lq * Hq / Hkv <= 256 query
  * rows, or L), each chunk reading the K/V before its end once with the block-causal mask
  * applied inside it; the chunks share their sequence's page-table row.
  */
