@@ -170,9 +170,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ StageInfo s_sinfo[ROWS ? STAGES : 1];
   __shared__ uint64_t bar_sready[ROWS ? STAGES : 1];
   constexpr int kSoftmax = ROWS ? kRowSoftmaxThreads : kSoftmaxThreads;
-  // P buffers: the transposed softmax double-buffers P^T; with rows on M one buffer suffices
-  // (a thread writes P(u + 1) only after its tile's math, long after PV(u) has read P(u))
-  constexpr int kPBufs = ROWS ? 1 : 2;
+  // P buffers: the transposed softmax double-buffers P^T in shared memory; with rows on M and
+  // one sub-group P lives in tensor memory (two buffers of 64 columns beside S and O, the PV
+  // MMA's A operand); with two sub-groups one shared-memory buffer (a thread writes its next P
+  // only after that tile's math, long after the PV that read the previous one)
+  constexpr bool kPTmem = ROWS && !TWO;
+  constexpr int kPBufs = kPTmem ? 2 : ROWS ? 1 : 2;
+  constexpr uint32_t kPCol = 384;   // first tensor-memory column of the P buffers (kPTmem)
   static_assert(!MASKED || ROWS, "the block-causal mask is applied by the row-per-thread softmax");
   static_assert(!ROWS || N == 128, "rows on M: one UMMA of 128 query rows");
   static_assert(!TWO || ROWS, "two sub-groups only with rows on M");
@@ -558,11 +562,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const uint32_t pa = p_addr + pb * (N * 256);
             for (int q = 0; q < npg; ++q) {
               const uint64_t ad = smem_desc(va + q * 2048, kHalfBytes, 1024);
-              const uint64_t bd = smem_desc(pa + (q >> 2) * (N * 128) + (q & 3) * 32, 16, 1024);
-              if constexpr (ROWS)
-                umma_bf16(tO + x * N, bd, ad, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
-              else
-                umma_bf16(tO, ad, bd, kIdescO, (c > 0 || j > j0 || q > 0) ? 1u : 0u);
+              const uint32_t acc = (c > 0 || j > j0 || q > 0) ? 1u : 0u;
+              if constexpr (kPTmem) {
+                // A = P in tensor memory: page q's 16 keys are 8 columns of buffer pb
+                umma_bf16_ts(tO, tmem + kPCol + static_cast<uint32_t>(pb * 64 + q * 8), ad,
+                             kIdescO, acc);
+              } else {
+                const uint64_t bd =
+                    smem_desc(pa + (q >> 2) * (N * 128) + (q & 3) * 32, 16, 1024);
+                if constexpr (ROWS)
+                  umma_bf16(tO + x * N, bd, ad, kIdescO, acc);
+                else
+                  umma_bf16(tO, ad, bd, kIdescO, acc);
+              }
             }
             umma_commit(&bar_pempty[pb]);
             ++pcount;
@@ -733,16 +745,25 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             tmem_wait_st();
           }
-          // this half of P row n into the K-major, 128-byte-swizzled operand: keys 64h ..
-          // 64h+63 are its half h
           const int pb = pcount % kPBufs;
           if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount / kPBufs) & 1) ^ 1, &abort_flag))) break;
-          uint8_t* prow = sP + pb * (N * 256) + half * (N * 128) + n * 128;
+          if constexpr (kPTmem) {
+            // this half of P row n into tensor memory: keys 64h + 2k, 64h + 2k + 1 in column
+            // 32h + k of buffer pb (the PV MMA's A operand)
+            const uint32_t tP = tmem + lane_off + kPCol + static_cast<uint32_t>(pb * 64) + col0 / 2;
+            tmem_st16(tP, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+            tmem_st16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+            tmem_wait_st();
+          } else {
+            // this half of P row n into the K-major, 128-byte-swizzled operand: keys 64h ..
+            // 64h+63 are its half h
+            uint8_t* prow = sP + pb * (N * 256) + half * (N * 128) + n * 128;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (n & 7)) << 4)) =
-                make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-          fence_proxy_async_smem();
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(prow + ((ch ^ (n & 7)) << 4)) =
+                  make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+            fence_proxy_async_smem();
+          }
           tc_fence_before();
           mbar_arrive(&bar_pfull[pb]);
           ++pcount;
@@ -1198,11 +1219,12 @@ attn_merge_kernel(const AttnParams p, int N) {
 
 template <int N, int STAGES, bool ROWS, bool TWO>
 constexpr size_t smem_bytes() {
-  // Q buffers (as the kernel: two with rows on M and one sub-group), K/V stages, P buffers
+  // Q buffers (as the kernel: two with rows on M and one sub-group), K/V stages, P buffers in
+  // shared memory (none with rows on M and one sub-group: P is in tensor memory)
   const size_t q = TWO ? static_cast<size_t>(2) * N * 256
                        : static_cast<size_t>(ROWS ? 2 : 1) * N * 256;
-  return 1024 + q + static_cast<size_t>(STAGES) * kStageBytes +
-         static_cast<size_t>(ROWS ? 1 : 2) * N * 256;
+  const size_t pbufs = ROWS ? (TWO ? 1 : 0) : 2;
+  return 1024 + q + static_cast<size_t>(STAGES) * kStageBytes + pbufs * N * 256;
 }
 
 template <int N, int STAGES, int CPS, bool MASKED, bool ROWS, bool TWO>
@@ -1351,8 +1373,8 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
       break;
     case 128:
       e = mask_block > 0
-              ? launch_t<128, 3, 1, true, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream)
-              : launch_t<128, 3, 1, false, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+              ? launch_t<128, 4, 1, true, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream)
+              : launch_t<128, 4, 1, false, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     case 256:   // two sub-groups of 128 query rows sharing the K/V
       e = mask_block > 0
