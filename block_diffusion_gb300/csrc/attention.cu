@@ -44,9 +44,14 @@ constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 // the rows-on-M kernel: two softmax warps per tensor-memory lane quadrant
 constexpr int kRowSoftmaxThreads = 256;
-// warps 0-1 producer and MMA, 2-9 softmax, 10 a second K/V copy issuer
-constexpr int kRowIssueWarp = 2 + kRowSoftmaxThreads / 32;
-constexpr int kRowThreads = 32 * (kRowIssueWarp + 1);
+// threads of a CTA: the transposed mode has warps 0-1 (producer, MMA) and 4 softmax warps; with
+// rows on M 8 softmax warps per sub-group (two per lane quadrant) and a second K/V copy issuer
+__host__ __device__ constexpr int attn_softmax_threads(bool rows, bool two) {
+  return rows ? kRowSoftmaxThreads * (two ? 2 : 1) : kSoftmaxThreads;
+}
+__host__ __device__ constexpr int attn_threads(bool rows, bool two) {
+  return 64 + attn_softmax_threads(rows, two) + (rows ? 32 : 0);
+}
 constexpr int kMaxSplitTokens = 2048;
 // Page ids staged per item: a split of up to kMaxSplitTokens, or a whole sequence of up to
 // kMaxItemPages pages when sequences are processed whole (two CTAs per SM at N = 16 leave
@@ -130,7 +135,7 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
 }
 
 template <int N, int STAGES, int CTAS_PER_SM, bool MASKED, bool ROWS, bool TWO>
-__global__ void __launch_bounds__(ROWS ? kRowThreads : kThreads, CTAS_PER_SM)
+__global__ void __launch_bounds__(attn_threads(ROWS, TWO), CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   constexpr uint32_t kTmemCols = 512 / CTAS_PER_SM;
@@ -162,20 +167,23 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ int s_need[2];   // chunk u (parity): some column's max rose enough to rescale O^T
   __shared__ int s_pflag[2];  // P buffer: its tile starts a chunk whose PV waits for a rescale
   __shared__ float s_red[4][kCols];
-  __shared__ float s_hmax[ROWS ? 2 : 1][2][ROWS ? N : 1];   // half-row maxima by tile parity
-  __shared__ float s_hsum[2][2][ROWS ? N : 1];              // half-row sums, by exchange parity
-  __shared__ uint64_t bar_pair[ROWS ? 4 : 1][2], bar_pair_end[ROWS ? 4 : 1];   // halves of a row
+  // the two halves of a row exchange maxima and sums, by exchange parity and sub-group; their
+  // mbarriers are per (sub-group, lane quadrant)
+  __shared__ float s_hmax[ROWS ? 2 : 1][TWO ? 2 : 1][2][ROWS ? N : 1];
+  __shared__ float s_hsum[ROWS ? 2 : 1][TWO ? 2 : 1][2][ROWS ? N : 1];
+  __shared__ uint64_t bar_pair[ROWS ? (TWO ? 8 : 4) : 1][2], bar_pair_end[ROWS ? (TWO ? 8 : 4) : 1];
   // rows on M: the producer issues half 0 of each stage's page boxes and hands the stage to a
   // second issuer warp for half 1 (one warp's copies issue at about 1 us per 16 boxes)
   __shared__ StageInfo s_sinfo[ROWS ? STAGES : 1];
   __shared__ uint64_t bar_sready[ROWS ? STAGES : 1];
-  constexpr int kSoftmax = ROWS ? kRowSoftmaxThreads : kSoftmaxThreads;
+  constexpr int kSoftmax = attn_softmax_threads(ROWS, TWO);
+  constexpr int kIssueWarp = 2 + kSoftmax / 32;   // rows on M: the second K/V copy issuer
   // P buffers: the transposed softmax double-buffers P^T in shared memory; with rows on M and
   // one sub-group P lives in tensor memory (two buffers of 64 columns beside S and O, the PV
-  // MMA's A operand); with two sub-groups one shared-memory buffer (a thread writes its next P
-  // only after that tile's math, long after the PV that read the previous one)
+  // MMA's A operand); with two sub-groups each sub-group's P overwrites its own S columns
+  // (tensor memory holds S_0, S_1, O_0, O_1: all 512 columns)
   constexpr bool kPTmem = ROWS && !TWO;
-  constexpr int kPBufs = kPTmem ? 2 : ROWS ? 1 : 2;
+  constexpr int kPBufs = 2;
   constexpr uint32_t kPCol = 384;   // first tensor-memory column of the P buffers (kPTmem)
   static_assert(!MASKED || ROWS, "the block-causal mask is applied by the row-per-thread softmax");
   static_assert(!ROWS || N == 128, "rows on M: one UMMA of 128 query rows");
@@ -198,7 +206,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_sfull[i], 1);
       mbar_init(&bar_sfree[i], kSoftmax);
-      mbar_init(&bar_pfull[i], kSoftmax);
+      mbar_init(&bar_pfull[i], TWO ? kSoftmax / 2 : kSoftmax);   // TWO: one per sub-group
       mbar_init(&bar_pempty[i], 1);
     }
     mbar_init(&bar_oready, kSoftmaxThreads);
@@ -208,11 +216,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(&bar_ifull[i], 1);
       // the MMA warp, and one softmax thread (every softmax thread with rows on M)
-      mbar_init(&bar_iempty[i], ROWS ? 1 + kRowSoftmaxThreads : 2);
+      mbar_init(&bar_iempty[i], ROWS ? 1 + kSoftmax : 2);
     }
     if constexpr (ROWS) {
       for (int s = 0; s < STAGES; ++s) mbar_init(&bar_sready[s], 1);
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < (TWO ? 8 : 4); ++q) {
         mbar_init(&bar_pair[q][0], 64);
         mbar_init(&bar_pair[q][1], 64);
         mbar_init(&bar_pair_end[q], 64);
@@ -402,17 +410,23 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const bool has_next = same || have_pend;
       bool have_pend2 = false;
       int pend2_seq = 0;
-      if (same) {
-        emit(cur, c + 1, cur_seq % 3, 0);
-      } else if (have_pend) {
-        if (lane == 0) load_q(pend, pend_seq);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        emit(pend, 0, pend_seq % 3, 0);
-      }
+      // K of the next chunk, then V of this one, in the order the MMA issuer consumes them
+      // (S(u + 1) before PV(u); with two sub-groups PV(u) before S(u + 1))
+      auto emit_next_k = [&]() {
+        if (same) {
+          emit(cur, c + 1, cur_seq % 3, 0);
+        } else if (have_pend) {
+          if (lane == 0) load_q(pend, pend_seq);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          emit(pend, 0, pend_seq % 3, 0);
+        }
+      };
+      if constexpr (!TWO) emit_next_k();
       if (!same && have_pend)
         emit(cur, c, cur_seq % 3, 1, &pend2, &have_pend2, &pend2_seq);
       else
         emit(cur, c, cur_seq % 3, 1);
+      if constexpr (TWO) emit_next_k();
       if (!has_next) break;
       if (same) {
         ++c;
@@ -447,7 +461,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           mbar_wait_drain(&bar_qfull[s % kQBufs], (s / kQBufs) & 1);
       }
     }
-  } else if (ROWS && warp == kRowIssueWarp) {
+  } else if (ROWS && warp == kIssueWarp) {
     // ================================================= second K/V copy issuer (rows on M)
     // Follows the ring stage by stage: once the producer has armed a stage and described it,
     // lanes 0-7 copy half 1 (head dims 64-127) of its pages.
@@ -501,9 +515,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           const uint32_t ka = kv_addr + st * kStageBytes;
           for (int x = 0; x < kSub; ++x) {
             const int sb = kSub == 1 ? (u & 1) : x;
-            // a sub-group's S buffer is free once the softmax has read its previous tile
-            if constexpr (TWO)
-              if (!(ok = ok && mbar_wait(&bar_sfree[sb], (u & 1) ^ 1, &abort_flag))) return;
+            // (two sub-groups: S(u) holds P(u) once the softmax is done with it, and PV(u) was
+            // issued before this S(u + 1), so the in-order tensor pipe reads P first)
             const uint32_t tS = tmem + static_cast<uint32_t>(sb * p.chunk_tiles * N);
             const uint32_t qa = q_addr + qb * kRowsItem * 256 + x * N * 128;
 #pragma unroll
@@ -550,8 +563,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
           const uint32_t va = kv_addr + st * kStageBytes;
           for (int x = 0; x < kSub; ++x) {
-            const int pb = pcount % kPBufs;
-            if (!(ok = mbar_wait(&bar_pfull[pb], (pcount / kPBufs) & 1, &abort_flag))) return;
+            const int pb = TWO ? x : pcount % kPBufs;
+            const uint32_t pph = TWO ? (u & 1) : ((pcount / kPBufs) & 1);
+            if (!(ok = mbar_wait(&bar_pfull[pb], pph, &abort_flag))) return;
             if constexpr (!ROWS) {
               if (c > 0 && j == j0 && s_pflag[pb]) {  // the softmax rescales O^T first
                 if (!(ok = mbar_wait(&bar_oready, ocount & 1, &abort_flag))) return;
@@ -567,6 +581,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // A = P in tensor memory: page q's 16 keys are 8 columns of buffer pb
                 umma_bf16_ts(tO, tmem + kPCol + static_cast<uint32_t>(pb * 64 + q * 8), ad,
                              kIdescO, acc);
+              } else if constexpr (TWO) {
+                // A = P in sub-group x's S columns: keys 64h .. 64h+63 as columns 64h .. 64h+31
+                const uint32_t pc = static_cast<uint32_t>(x * N + (q >> 2) * 64 + (q & 3) * 8);
+                umma_bf16_ts(tO + x * N, tmem + pc, ad, kIdescO, acc);
               } else {
                 const uint64_t bd =
                     smem_desc(pa + (q >> 2) * (N * 128) + (q & 3) * 32, 16, 1024);
@@ -576,7 +594,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                   umma_bf16(tO, ad, bd, kIdescO, acc);
               }
             }
-            umma_commit(&bar_pempty[pb]);
+            if constexpr (!TWO) umma_commit(&bar_pempty[pb]);
             ++pcount;
           }
           umma_commit(&bar_empty[st]);
@@ -586,6 +604,88 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
         }
         umma_commit(&bar_ofull[u & 1]);
+      };
+      // Two sub-groups: PV(u) and S(u + 1) interleaved by sub-group (PV_0, S_0, PV_1, S_1) with
+      // V(u) and K(u + 1) both staged, so sub-group 0's softmax of u + 1 runs while sub-group
+      // 1's PV(u) and S(u + 1) execute.  S_x(u + 1) overwrites the P_x(u) that PV_x(u) reads;
+      // the tensor pipe executes one thread's MMAs in issue order.
+      // S_x = Q_x K^T from the K stage at ka, into sub-group x's S columns
+      auto issue_s = [&](uint32_t ka, int qb, int x) {
+        const uint32_t tS = tmem + static_cast<uint32_t>(x * N);
+        const uint32_t qa = q_addr + qb * kRowsItem * 256 + x * N * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = smem_desc(ka + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd =
+              smem_desc(qa + (kk >> 2) * (kRowsItem * 128) + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tS, bd, ad, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar_sfull[x]);
+      };
+      auto do_pv_s = [&](const Item& it, int c, int u, const Item& nx, int nc, int nseq,
+                         bool has_next) {
+        const int stv = st;
+        if (!(ok = mbar_wait(&bar_full[stv], ph, &abort_flag))) return;
+        if (++st == STAGES) {
+          st = 0;
+          ph ^= 1;
+        }
+        const int tok0 = it.t_begin + c * kTile;
+        const int valid = min(kTile, it.t_end - tok0);
+        const int npg = (valid + kPage - 1) / kPage;
+        const int tail = valid - (npg - 1) * kPage;
+        if (tail < kPage) {
+          // slots past the sequence end may hold anything (NaN): 0 * NaN would poison O
+          uint8_t* stage = sKV + stv * kStageBytes;
+          for (int h = 0; h < 2; ++h) {
+            uint4* z = reinterpret_cast<uint4*>(stage + h * kHalfBytes + (npg - 1) * 2048 +
+                                                tail * 128);
+            for (int o = 0; o < (kPage - tail) * 8; ++o) z[o] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        const int stk = st;
+        const uint32_t phk = ph;
+        const int qb = nseq % kQBufs;
+        if (has_next && ++st == STAGES) {
+          st = 0;
+          ph ^= 1;
+        }
+        const uint32_t va = kv_addr + stv * kStageBytes;
+        const uint32_t ka = kv_addr + stk * kStageBytes;
+        // at an item boundary S(u + 1) waits for the next item's Q: both PVs first
+        const bool inter = has_next && nc > 0;
+        for (int x = 0; x < 2; ++x) {
+          if (!(ok = mbar_wait(&bar_pfull[x], u & 1, &abort_flag))) return;
+          tc_fence_after();
+          for (int q = 0; q < npg; ++q) {
+            // A = P in sub-group x's S columns: keys 64h .. 64h+63 as columns 64h .. 64h+31
+            const uint64_t ad = smem_desc(va + q * 2048, kHalfBytes, 1024);
+            const uint32_t pc = static_cast<uint32_t>(x * N + (q >> 2) * 64 + (q & 3) * 8);
+            umma_bf16_ts(tO + x * N, tmem + pc, ad, kIdescO, (c > 0 || q > 0) ? 1u : 0u);
+          }
+          if (x == 1) {
+            umma_commit(&bar_empty[stv]);
+            umma_commit(&bar_ofull[u & 1]);
+          }
+          if (!inter) continue;
+          if (x == 0) {   // K(u + 1) only now: PV_0(u) does not need it
+            if (!(ok = mbar_wait(&bar_full[stk], phk, &abort_flag))) return;
+            tc_fence_after();
+          }
+          issue_s(ka, qb, x);
+        }
+        if (has_next && !inter) {
+          if (!(ok = mbar_wait(&bar_full[stk], phk, &abort_flag))) return;
+          if (!(ok = mbar_wait(&bar_qfull[qb], (nseq / kQBufs) & 1, &abort_flag))) return;
+          tc_fence_after();
+          issue_s(ka, qb, 0);
+          issue_s(ka, qb, 1);
+        }
+        if (has_next) {
+          umma_commit(&bar_empty[stk]);
+          if (nc == nx.n_chunks - 1) umma_commit(&bar_qempty[qb]);  // Q no longer needed
+        }
       };
       int seq = 0;
       Item cur, nxt;
@@ -609,9 +709,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             has_next = !nxt.end;
           }
           // S(u + 1) ahead of PV(u), so the softmax can start the next tile while PV runs
-          if (has_next) do_s(nxt, nc, u + 1, nseq);
-          if (!ok) break;
-          do_pv(cur, c, u);
+          if constexpr (!TWO) {
+            if (has_next) do_s(nxt, nc, u + 1, nseq);
+            if (!ok) break;
+          }
+          if constexpr (TWO)
+            do_pv_s(cur, c, u, nxt, nc, nseq, has_next);
+          else
+            do_pv(cur, c, u);
           if (!ok) break;
           if (c == cur.n_chunks - 1) mbar_arrive(&bar_iempty[seq % kItemRing]);
           if (!has_next) break;
@@ -622,6 +727,183 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
       }
       umma_commit(&bar_done);
+    }
+  } else if constexpr (ROWS && TWO) {
+    // ======================== softmax/epilogue, two sub-groups in parallel, a row per 2 threads
+    // Warps 2-9 take sub-group 0, warps 10-17 sub-group 1: query row x * 128 + n of the item is
+    // lane n of sub-group x's S and O; half 0 takes columns 0-63, half 1 columns 64-127.  A
+    // half reads its 64 scores 32 at a time (a max pass, then an exponent pass) and writes its
+    // P over the first 32 of its own S columns, the PV MMA's A operand.
+    const int x = (warp - 2) >> 3;
+    const int half = ((warp - 2) >> 2) & 1;
+    const int q4 = warp & 3;
+    const int n = (q4 << 5) | lane;
+    const int pq = x * 4 + q4;   // the two halves' exchange barriers
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half * 64);
+    const uint32_t tSx = tmem + lane_off + static_cast<uint32_t>(x * N) + col0;
+    const uint32_t tOx = tO + lane_off + static_cast<uint32_t>(x * N) + col0;
+    const float cs = p.scale_log2;
+    bool ok = true;
+    int u = 0, pe = 0, pair_ends = 0;
+    for (int seq = 0; ok; ++seq) {
+      const int rs = seq % kItemRing;
+      if (!(ok = mbar_wait(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      const Item it = s_item[rs];
+      mbar_arrive(&bar_iempty[rs]);   // the descriptor is in registers: its slot may be reused
+      if (it.end) break;
+      const int r_item = x * N + n;                  // row of the item
+      const int i_row = it.rg * p.lsub + r_item / p.G;
+      int lim = 0x7FFFFFFF;                           // keys past q0 the row may see
+      if constexpr (MASKED) lim = (i_row / p.mask_block + 1) * p.mask_block;
+      float m_run = -CUDART_INF_F, l_run = 0.f;       // l_run: this half's sum
+      for (int c = 0; c < it.n_chunks && ok; ++c, ++u) {
+        if (!(ok = mbar_wait(&bar_sfull[x], u & 1, &abort_flag))) break;
+        tc_fence_after();
+        const int key0 = it.t_begin + c * kTile;
+        int nvalid = min(kTile, it.t_end - key0);
+        if constexpr (MASKED) nvalid = min(nvalid, lim - (key0 - it.q0));
+        nvalid -= half * 64;   // of this half's columns
+        // pass 1: the half-row max, 32 scores at a time; then the row max
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          uint32_t r[32];
+          tmem_ld16(tSx + g2 * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
+          tmem_ld16(tSx + g2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+          tmem_wait_ld();
+          tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r));
+          tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
+          float t[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float a = g2 * 32 + 2 * k < nvalid ? __uint_as_float(r[2 * k]) : -CUDART_INF_F;
+            const float b =
+                g2 * 32 + 2 * k + 1 < nvalid ? __uint_as_float(r[2 * k + 1]) : -CUDART_INF_F;
+            t[k] = fmaxf(a, b);
+          }
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+          mx = fmaxf(mx, t[0]);
+        }
+        s_hmax[pe & 1][x][half][n] = mx;
+        mbar_arrive(&bar_pair[pq][pe & 1]);
+        if (!(ok = mbar_wait(&bar_pair[pq][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
+        mx = fmaxf(s_hmax[pe & 1][x][0][n], s_hmax[pe & 1][x][1][n]);
+        ++pe;
+        // the running max moves only when the tile raises it by more than 2^kLazyRescale
+        float alpha = 1.f;
+        bool resc = false;
+        if (m_run == -CUDART_INF_F) {
+          m_run = mx;
+        } else if ((mx - m_run) * cs > kLazyRescale) {
+          alpha = ex2((m_run - mx) * cs);
+          m_run = mx;
+          resc = true;
+        }
+        const float mc = m_run == -CUDART_INF_F ? 0.f : m_run * cs;
+        const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-mc, -mc);
+        // pass 2: p = 2^(s cs - m cs), 32 at a time; P (bf16 pairs) over columns already read
+        float sum = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          uint32_t r[32];
+          tmem_ld16(tSx + g2 * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
+          tmem_ld16(tSx + g2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+          tmem_wait_ld();
+          tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r));
+          tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
+          float2 e[16];
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float a = g2 * 32 + 2 * k < nvalid ? __uint_as_float(r[2 * k]) : -CUDART_INF_F;
+            const float b =
+                g2 * 32 + 2 * k + 1 < nvalid ? __uint_as_float(r[2 * k + 1]) : -CUDART_INF_F;
+            const float2 y = __ffma2_rn(make_float2(a, b), cs2, nm2);
+            e[k] = make_float2(ex2(y.x), ex2(y.y));
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[k].x, e[k].y);
+            pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          tmem_st16(tSx + g2 * 16, pk);   // keys 64h + 32 g2 .. + 31 as 16 columns
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) e[k] = __fadd2_rn(e[k], e[k + w]);
+          sum += e[0].x + e[0].y;
+        }
+        l_run = l_run * alpha + sum;
+        if (__any_sync(0xffffffffu, resc)) {
+          // bring this warp's half of its rows of O to the new maxima once the previous
+          // tile's PV is done
+          if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t o[16];
+            tmem_ld16(tOx + g * 16, o);
+            tmem_wait_ld();
+            tmem_regs_ready(o);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st16(tOx + g * 16, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_pfull[x]);
+        if (c != it.n_chunks - 1) continue;
+        // ---- epilogue of the item: this half of the row of O, divided by the row's sum or as
+        // a split partial
+        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        tc_fence_after();
+        s_hsum[pair_ends & 1][x][half][n] = l_run;
+        mbar_arrive(&bar_pair_end[pq]);
+        if (!(ok = mbar_wait(&bar_pair_end[pq], pair_ends & 1, &abort_flag))) break;
+        const float l_row = s_hsum[pair_ends & 1][x][0][n] + s_hsum[pair_ends & 1][x][1][n];
+        ++pair_ends;
+        const bool live = r_item < p.rows_per_group && i_row < p.L;
+        const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
+        float* mine =
+            p.part + (grp * p.max_splits + it.split) * static_cast<size_t>(kRowsItem) * 130;
+        uint16_t* dst = live ? p.out + ((static_cast<size_t>(it.b) * p.L + i_row) * p.Hq +
+                                        static_cast<size_t>(it.kvh) * p.G + r_item % p.G) * 128 + col0
+                             : p.out;
+        const float inv = 1.f / l_row;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t o[16];
+          tmem_ld16(tOx + g * 16, o);
+          tmem_wait_ld();
+          tmem_regs_ready(o);
+          if (!live) continue;
+          if (it.n_splits == 1) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[2 * k]) * inv,
+                                                              __uint_as_float(o[2 * k + 1]) * inv);
+              w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + g * 16);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            float4* d4 = reinterpret_cast<float4*>(mine + r_item * 128 + col0 + g * 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                  __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+          }
+        }
+        if (live && it.n_splits > 1 && half == 0) {
+          mine[kRowsItem * 128 + r_item] = m_run;
+          mine[kRowsItem * 128 + kRowsItem + r_item] = l_row;
+        }
+        tc_fence_before();   // O is read: the next item's first PV (after its P) may overwrite it
+      }
     }
   } else if constexpr (ROWS) {
     // ====================================================== softmax/epilogue, a row per 2 threads
@@ -692,10 +974,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           for (int w = 16; w > 0; w >>= 1)
 #pragma unroll
             for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
-          s_hmax[pe & 1][half][n] = t[0];
+          s_hmax[pe & 1][0][half][n] = t[0];
           mbar_arrive(&bar_pair[q4][pe & 1]);
           if (!(ok = mbar_wait(&bar_pair[q4][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
-          const float mx = fmaxf(s_hmax[pe & 1][0][n], s_hmax[pe & 1][1][n]);
+          const float mx = fmaxf(s_hmax[pe & 1][0][0][n], s_hmax[pe & 1][0][1][n]);
           ++pe;
           // the running max moves only when the tile raises it by more than 2^kLazyRescale
           // (both halves of a row take the same decision)
@@ -778,10 +1060,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             p.part + (grp * p.max_splits + it.split) * static_cast<size_t>(kRowsItem) * 130;
 #pragma unroll
         for (int x = 0; x < kSub; ++x) {
-          s_hsum[pair_ends & 1][half][n] = l_run[x];
+          s_hsum[pair_ends & 1][0][half][n] = l_run[x];
           mbar_arrive(&bar_pair_end[q4]);
           if (!(ok = mbar_wait(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
-          const float l_row = s_hsum[pair_ends & 1][0][n] + s_hsum[pair_ends & 1][1][n];
+          const float l_row = s_hsum[pair_ends & 1][0][0][n] + s_hsum[pair_ends & 1][0][1][n];
           ++pair_ends;
           const int r_item = x * N + n;   // row of the item
           const bool live = r_item < p.rows_per_group && i_row[x] < p.L;
@@ -1220,10 +1502,10 @@ attn_merge_kernel(const AttnParams p, int N) {
 template <int N, int STAGES, bool ROWS, bool TWO>
 constexpr size_t smem_bytes() {
   // Q buffers (as the kernel: two with rows on M and one sub-group), K/V stages, P buffers in
-  // shared memory (none with rows on M and one sub-group: P is in tensor memory)
+  // shared memory (none with rows on M: P is in tensor memory)
   const size_t q = TWO ? static_cast<size_t>(2) * N * 256
                        : static_cast<size_t>(ROWS ? 2 : 1) * N * 256;
-  const size_t pbufs = ROWS ? (TWO ? 1 : 0) : 2;
+  const size_t pbufs = ROWS ? 0 : 2;
   return 1024 + q + static_cast<size_t>(STAGES) * kStageBytes + pbufs * N * 256;
 }
 
@@ -1244,7 +1526,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     attr_set = true;
   }
   return launch_pdl(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>, dim3(num_sms * CPS),
-                    dim3(ROWS ? kRowThreads : kThreads), smem,
+                    dim3(attn_threads(ROWS, TWO)), smem,
                     stream, tq, tk, tv, prm);
 }
 
@@ -1378,8 +1660,8 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
       break;
     case 256:   // two sub-groups of 128 query rows sharing the K/V
       e = mask_block > 0
-              ? launch_t<128, 3, 1, true, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream)
-              : launch_t<128, 3, 1, false, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+              ? launch_t<128, 4, 1, true, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream)
+              : launch_t<128, 4, 1, false, true, true>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     default: return cudaErrorInvalidValue;
   }
