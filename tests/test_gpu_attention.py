@@ -128,22 +128,26 @@ def test_bad_page_ids_and_lengths_are_flagged_not_faulted(lib):
     check(lib, a)
 
 
-@pytest.mark.parametrize("L", [32, 16])
+@pytest.mark.parametrize("L", [32, 16, 64])
 def test_rows_on_m_rescale_after_a_sharp_key(lib, L):
     """More than 32 query rows per KV head (query rows on the UMMA M side).  One key in the
     third 128-token tile is planted as 3x a query of its KV head, so that row's max rises
     far above the first tiles' and the kernel must rescale the row's output before the next
-    PV product; every other row keeps the lazily kept max."""
+    PV product; every other row keeps the lazily kept max.  At L = 64 (256 rows per KV head:
+    two 128-row sub-groups) a second key in the fourth tile does the same for a row of the
+    second sub-group."""
     rng = np.random.default_rng(515)
     B, Hq, Hkv = 2, 32, 8
     G = Hq // Hkv
     a = W.make_attention(rng, B, L, Hq, Hkv, 128, prefix_range=(600, 900))
+    plants = [(3, 300)] + ([(50, 420)] if L == 64 else [])   # (query position, first token)
     for b in range(B):
-        for g in (1, 6):
-            t = 300 + 7 * g                                  # a prefix token in the third tile
-            r = a.page_table_ref[b, t // 16]
-            qf = W.bf16_bits_to_f32(a.q[b, 3, g * G + 1])
-            a.k_ref[r, t % 16, g] = W.f32_to_bf16_bits(3.0 * qf)
+        for i, t0 in plants:
+            for g in (1, 6):
+                t = t0 + 7 * g                               # a prefix token in tile t0 // 128
+                r = a.page_table_ref[b, t // 16]
+                qf = W.bf16_bits_to_f32(a.q[b, i, g * G + 1])
+                a.k_ref[r, t % 16, g] = W.f32_to_bf16_bits(3.0 * qf)
     check(lib, a)
 
 
