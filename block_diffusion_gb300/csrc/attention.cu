@@ -146,13 +146,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   // K/V stage, each with its own S and O in tensor memory.
   constexpr int kSub = TWO ? 2 : 1;
   constexpr int kRowsItem = N * kSub;          // query rows of an item
-  // Q buffers: one for the transposed mode (4 KB at N = 16: two CTAs per SM leave no room for
-  // another) and for two sub-groups (64 KB); otherwise two, so the next item's Q lands while
-  // this item finishes
-  constexpr int kQBufs = ROWS && !TWO ? 2 : 1;
-  uint8_t* sQ = base;                          // kQBufs x 2 halves x kRowsItem rows x 128 B
+  // One Q buffer: 4 KB at N = 16 in the transposed mode, 64 KB for two sub-groups; with rows on
+  // M and one sub-group it only stages Q, which the MMA issuer copies into tensor memory (the S
+  // MMA's A operand) as the item starts, so the next item's Q can land during this item
+  constexpr int kQBufs = 1;
+  constexpr bool kQTmem = ROWS && !TWO;
+  uint8_t* sQ = base;                          // 2 halves x kRowsItem rows x 128 B
   uint8_t* sKV = sQ + kQBufs * kRowsItem * 256;   // STAGES x 32 KB
-  uint8_t* sP = sKV + STAGES * kStageBytes;    // 1 or 2 buffers x (2 K-atoms x N rows x 128 B)
+  uint8_t* sP = sKV + STAGES * kStageBytes;    // transposed mode: 2 buffers x (2 K-atoms x N rows x 128 B)
 
   __shared__ uint64_t bar_qfull[kQBufs], bar_qempty[kQBufs], bar_full[STAGES], bar_empty[STAGES];
   __shared__ uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_pempty[2];
@@ -178,13 +179,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ uint64_t bar_sready[ROWS ? STAGES : 1];
   constexpr int kSoftmax = attn_softmax_threads(ROWS, TWO);
   constexpr int kIssueWarp = 2 + kSoftmax / 32;   // rows on M: the second K/V copy issuer
-  // P buffers: the transposed softmax double-buffers P^T in shared memory; with rows on M and
-  // one sub-group P lives in tensor memory (two buffers of 64 columns beside S and O, the PV
-  // MMA's A operand); with two sub-groups each sub-group's P overwrites its own S columns
-  // (tensor memory holds S_0, S_1, O_0, O_1: all 512 columns)
+  // P buffers: the transposed softmax double-buffers P^T in shared memory; with rows on M, P is
+  // written over the S columns it came from (the PV MMA's A operand; the tensor pipe executes
+  // one thread's MMAs in issue order, so the next S into those columns, issued after that PV,
+  // cannot overwrite P before the PV has read it).  Tensor memory with rows on M: S buffers
+  // 0-255, O 256-383 and Q 384-447 (one sub-group); S_0, S_1, O_0, O_1 (two sub-groups).
   constexpr bool kPTmem = ROWS && !TWO;
   constexpr int kPBufs = 2;
-  constexpr uint32_t kPCol = 384;   // first tensor-memory column of the P buffers (kPTmem)
+  constexpr uint32_t kQCol = 384;   // first tensor-memory column of Q (kQTmem)
   static_assert(!MASKED || ROWS, "the block-causal mask is applied by the row-per-thread softmax");
   static_assert(!ROWS || N == 128, "rows on M: one UMMA of 128 query rows");
   static_assert(!TWO || ROWS, "two sub-groups only with rows on M");
@@ -507,6 +509,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int qb = seq % kQBufs;
         if (c == 0 && !(ok = mbar_wait(&bar_qfull[qb], (seq / kQBufs) & 1, &abort_flag))) return;
         tc_fence_after();
+        if (kQTmem && c == 0) {
+          // the item's Q into tensor memory, 16 head dims (8 columns) per copy, behind the last
+          // S of the previous item; the staging buffer is free once the copies are done
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tmem_cp_128x256b(tmem + kQCol + static_cast<uint32_t>(kk * 8),
+                             smem_desc(q_addr + (kk >> 2) * (kRowsItem * 128) + (kk & 3) * 32, 16,
+                                       1024));
+          umma_commit(&bar_qempty[qb]);
+        }
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
@@ -525,7 +537,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                   smem_desc(ka + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
               const uint64_t bd =
                   smem_desc(qa + (kk >> 2) * (kRowsItem * 128) + (kk & 3) * 32, 16, 1024);
-              if constexpr (ROWS)
+              if constexpr (kQTmem)
+                umma_bf16_ts(tS + (j - j0) * N, tmem + kQCol + static_cast<uint32_t>(kk * 8), ad,
+                             kIdescS, kk > 0 ? 1u : 0u);
+              else if constexpr (ROWS)
                 umma_bf16(tS + (j - j0) * N, bd, ad, kIdescS, kk > 0 ? 1u : 0u);
               else
                 umma_bf16(tS + (j - j0) * N, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
@@ -539,7 +554,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
         }
         if constexpr (!TWO) umma_commit(&bar_sfull[u & 1]);
-        if (c == it.n_chunks - 1) umma_commit(&bar_qempty[qb]);  // Q no longer needed
+        if (!kQTmem && c == it.n_chunks - 1) umma_commit(&bar_qempty[qb]);  // Q no longer needed
       };
       // O^T += V^T P^T (O += P V) over the tiles of chunk `c`, for each sub-group
       auto do_pv = [&](const Item& it, int c, int u) {
@@ -578,9 +593,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
               const uint64_t ad = smem_desc(va + q * 2048, kHalfBytes, 1024);
               const uint32_t acc = (c > 0 || j > j0 || q > 0) ? 1u : 0u;
               if constexpr (kPTmem) {
-                // A = P in tensor memory: page q's 16 keys are 8 columns of buffer pb
-                umma_bf16_ts(tO, tmem + kPCol + static_cast<uint32_t>(pb * 64 + q * 8), ad,
-                             kIdescO, acc);
+                // A = P over S buffer u & 1: keys 64h .. 64h+63 as columns 64h .. 64h+31
+                const uint32_t pc =
+                    static_cast<uint32_t>((u & 1) * N + (q >> 2) * 64 + (q & 3) * 8);
+                umma_bf16_ts(tO, tmem + pc, ad, kIdescO, acc);
               } else if constexpr (TWO) {
                 // A = P in sub-group x's S columns: keys 64h .. 64h+63 as columns 64h .. 64h+31
                 const uint32_t pc = static_cast<uint32_t>(x * N + (q >> 2) * 64 + (q & 3) * 8);
@@ -594,7 +610,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                   umma_bf16(tO, ad, bd, kIdescO, acc);
               }
             }
-            if constexpr (!TWO) umma_commit(&bar_pempty[pb]);
+            if constexpr (!ROWS) umma_commit(&bar_pempty[pb]);
             ++pcount;
           }
           umma_commit(&bar_empty[st]);
@@ -1027,25 +1043,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             tmem_wait_st();
           }
-          const int pb = pcount % kPBufs;
-          if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount / kPBufs) & 1) ^ 1, &abort_flag))) break;
-          if constexpr (kPTmem) {
-            // this half of P row n into tensor memory: keys 64h + 2k, 64h + 2k + 1 in column
-            // 32h + k of buffer pb (the PV MMA's A operand)
-            const uint32_t tP = tmem + lane_off + kPCol + static_cast<uint32_t>(pb * 64) + col0 / 2;
-            tmem_st16(tP, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-            tmem_st16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
-            tmem_wait_st();
-          } else {
-            // this half of P row n into the K-major, 128-byte-swizzled operand: keys 64h ..
-            // 64h+63 are its half h
-            uint8_t* prow = sP + pb * (N * 256) + half * (N * 128) + n * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4*>(prow + ((ch ^ (n & 7)) << 4)) =
-                  make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-            fence_proxy_async_smem();
-          }
+          const int pb = pcount % kPBufs;   // = u & 1, the S buffer
+          // this half of P row n over the first 32 of this half's S columns (already in
+          // registers): keys 64h + 2k, 64h + 2k + 1 in column 64h + k, the PV MMA's A operand
+          tmem_st16(tS, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+          tmem_st16(tS + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+          tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bar_pfull[pb]);
           ++pcount;
@@ -1501,10 +1504,9 @@ attn_merge_kernel(const AttnParams p, int N) {
 
 template <int N, int STAGES, bool ROWS, bool TWO>
 constexpr size_t smem_bytes() {
-  // Q buffers (as the kernel: two with rows on M and one sub-group), K/V stages, P buffers in
-  // shared memory (none with rows on M: P is in tensor memory)
-  const size_t q = TWO ? static_cast<size_t>(2) * N * 256
-                       : static_cast<size_t>(ROWS ? 2 : 1) * N * 256;
+  // the Q buffer (as the kernel: one of the item's rows), K/V stages, P buffers in shared memory
+  // (none with rows on M: P is in tensor memory)
+  const size_t q = static_cast<size_t>(TWO ? 2 : 1) * N * 256;
   const size_t pbufs = ROWS ? 0 : 2;
   return 1024 + q + static_cast<size_t>(STAGES) * kStageBytes + pbufs * N * 256;
 }
@@ -1655,8 +1657,8 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
       break;
     case 128:
       e = mask_block > 0
-              ? launch_t<128, 4, 1, true, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream)
-              : launch_t<128, 4, 1, false, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
+              ? launch_t<128, 5, 1, true, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream)
+              : launch_t<128, 5, 1, false, true, false>(tm_q, tm_k, tm_v, prm, num_sms, stream);
       break;
     case 256:   // two sub-groups of 128 query rows sharing the K/V
       e = mask_block > 0

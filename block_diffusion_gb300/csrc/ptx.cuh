@@ -155,6 +155,13 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Shared memory -> tensor memory: 128 rows of 32 bytes (the matrix the descriptor describes, in
+// its canonical layout) into lanes 0-127, 8 columns from `taddr`.  Asynchronous and ordered with
+// the issuing thread's tcgen05.mma; tcgen05.commit tracks its completion.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Non-tensor bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
