@@ -25,6 +25,12 @@
 //  * Either whole sequences, longest first (when there are enough items), or splits of a
 //    long sequence that write (O, m, l) partials merged by a small second kernel; no CTA
 //    ever waits on another one, and every wait inside a CTA is bounded.
+//  * More than 32 query rows per KV head (ROWS): S = Q K^T with 128 query rows on M, a row per
+//    tensor-memory lane, two softmax threads per row (half a row each); P is written over the
+//    S columns it came from and is the PV MMA's A operand in tensor memory.  With one 128-row
+//    sub-group Q is copied into tensor memory too (tcgen05.cp) and the ring has five stages;
+//    with two sub-groups (TWO, up to 256 rows) both share every K/V stage and sixteen softmax
+//    warps work on both at once.  The block-causal prefill mask (MASKED) applies per row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -314,8 +320,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // K/V pages are read exactly once: first to leave L2, so that the split partials (and Q)
     // stay resident for the merge
     const uint64_t kv_policy = l2_policy_evict_first();
-    // Loads the Q tile of item `it` (sequence number s) into Q buffer s % kQBufs once the S
-    // MMAs of the item that used it before are done with it.  Lane 0.
+    // Loads the Q tile of item `it` (sequence number s) into Q buffer s % kQBufs once the item
+    // that used it before is done with it (its last S MMA, or with Q in tensor memory the copy
+    // out of the buffer).  Lane 0.
     int q_loads = 0;
     auto load_q = [&](const Item& it, int s) {
       const int b = s % kQBufs;
