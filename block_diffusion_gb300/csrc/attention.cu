@@ -140,6 +140,47 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   return true;
 }
 
+// Rows on M, two sub-groups: 32 scores of a half-row (keys base .. base + 31 of its 64).
+// FULL: all of them are keys the row sees; otherwise keys at or past nvalid read as -inf.
+template <bool FULL>
+__device__ __forceinline__ float max32(const uint32_t (&r)[32], int base, int nvalid) {
+  float t[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float a = FULL || base + 2 * k < nvalid ? __uint_as_float(r[2 * k]) : -CUDART_INF_F;
+    const float b =
+        FULL || base + 2 * k + 1 < nvalid ? __uint_as_float(r[2 * k + 1]) : -CUDART_INF_F;
+    t[k] = fmaxf(a, b);
+  }
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+  return t[0];
+}
+
+// p = 2^(s cs - m cs) of the same 32 scores, packed as bf16 pairs into pk; returns their sum.
+template <bool FULL>
+__device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int base, int nvalid,
+                                            float2 cs2, float2 nm2, uint32_t (&pk)[16]) {
+  float2 e[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float a = FULL || base + 2 * k < nvalid ? __uint_as_float(r[2 * k]) : -CUDART_INF_F;
+    const float b =
+        FULL || base + 2 * k + 1 < nvalid ? __uint_as_float(r[2 * k + 1]) : -CUDART_INF_F;
+    const float2 y = __ffma2_rn(make_float2(a, b), cs2, nm2);
+    e[k] = make_float2(ex2(y.x), ex2(y.y));
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[k].x, e[k].y);
+    pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) e[k] = __fadd2_rn(e[k], e[k + w]);
+  return e[0].x + e[0].y;
+}
+
 template <int N, int STAGES, int CTAS_PER_SM, bool MASKED, bool ROWS, bool TWO>
 __global__ void __launch_bounds__(attn_threads(ROWS, TWO), CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -787,6 +828,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         int nvalid = min(kTile, it.t_end - key0);
         if constexpr (MASKED) nvalid = min(nvalid, lim - (key0 - it.q0));
         nvalid -= half * 64;   // of this half's columns
+        const bool full = nvalid >= 64;   // every score of this half-row is a key the row sees
         // pass 1: the half-row max, 32 scores at a time; then the row max
         float mx = -CUDART_INF_F;
 #pragma unroll
@@ -797,19 +839,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           tmem_wait_ld();
           tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r));
           tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
-          float t[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float a = g2 * 32 + 2 * k < nvalid ? __uint_as_float(r[2 * k]) : -CUDART_INF_F;
-            const float b =
-                g2 * 32 + 2 * k + 1 < nvalid ? __uint_as_float(r[2 * k + 1]) : -CUDART_INF_F;
-            t[k] = fmaxf(a, b);
-          }
-#pragma unroll
-          for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
-          mx = fmaxf(mx, t[0]);
+          mx = fmaxf(mx, full ? max32<true>(r, 0, 0) : max32<false>(r, g2 * 32, nvalid));
         }
         s_hmax[pe & 1][x][half][n] = mx;
         mbar_arrive(&bar_pair[pq][pe & 1]);
@@ -838,24 +868,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           tmem_wait_ld();
           tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r));
           tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
-          float2 e[16];
           uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float a = g2 * 32 + 2 * k < nvalid ? __uint_as_float(r[2 * k]) : -CUDART_INF_F;
-            const float b =
-                g2 * 32 + 2 * k + 1 < nvalid ? __uint_as_float(r[2 * k + 1]) : -CUDART_INF_F;
-            const float2 y = __ffma2_rn(make_float2(a, b), cs2, nm2);
-            e[k] = make_float2(ex2(y.x), ex2(y.y));
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[k].x, e[k].y);
-            pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
+          sum += full ? exp_pack32<true>(r, 0, 0, cs2, nm2, pk)
+                      : exp_pack32<false>(r, g2 * 32, nvalid, cs2, nm2, pk);
           tmem_st16(tSx + g2 * 16, pk);   // keys 64h + 32 g2 .. + 31 as 16 columns
-#pragma unroll
-          for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) e[k] = __fadd2_rn(e[k], e[k + w]);
-          sum += e[0].x + e[0].y;
         }
         l_run = l_run * alpha + sum;
         if (__any_sync(0xffffffffu, resc)) {
