@@ -144,19 +144,18 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
 // FULL: all of them are keys the row sees; otherwise keys at or past nvalid read as -inf.
 template <bool FULL>
 __device__ __forceinline__ float max32(const uint32_t (&r)[32], int base, int nvalid) {
-  float t[16];
+  float v[32];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const float a = FULL || base + 2 * k < nvalid ? __uint_as_float(r[2 * k]) : -CUDART_INF_F;
-    const float b =
-        FULL || base + 2 * k + 1 < nvalid ? __uint_as_float(r[2 * k + 1]) : -CUDART_INF_F;
-    t[k] = fmaxf(a, b);
-  }
+  for (int k = 0; k < 32; ++k)
+    v[k] = FULL || base + k < nvalid ? __uint_as_float(r[k]) : -CUDART_INF_F;
+  // a tree of three-input maxima: 32 -> 11 -> 4 -> 1 (17 instructions)
+  float t[11];
 #pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-    for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
-  return t[0];
+  for (int k = 0; k < 10; ++k) t[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  t[10] = fmaxf(v[30], v[31]);
+  const float u0 = fmax3(t[0], t[1], t[2]), u1 = fmax3(t[3], t[4], t[5]);
+  const float u2 = fmax3(t[6], t[7], t[8]), u3 = fmaxf(t[9], t[10]);
+  return fmaxf(fmax3(u0, u1, u2), u3);
 }
 
 // p = 2^(s cs - m cs) of the same 32 scores, packed as bf16 pairs into pk; returns their sum.
@@ -1004,16 +1003,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             for (int k = 0; k < 64; ++k)
               if (k >= nvalid) r[k] = 0xFF800000u;
           }
-          // half-row max (a tree, so the warp has work in flight), then the row max
-          float t[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            t[k] = fmaxf(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
-#pragma unroll
-          for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
-          s_hmax[pe & 1][0][half][n] = t[0];
+          // half-row max (trees of three-input maxima over the masked scores), then the row max
+          const float hmax =
+              fmaxf(max32<true>(*reinterpret_cast<const uint32_t(*)[32]>(r), 0, 0),
+                    max32<true>(*reinterpret_cast<const uint32_t(*)[32]>(r + 32), 0, 0));
+          s_hmax[pe & 1][0][half][n] = hmax;
           mbar_arrive(&bar_pair[q4][pe & 1]);
           if (!(ok = mbar_wait(&bar_pair[q4][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
           const float mx = fmaxf(s_hmax[pe & 1][0][0][n], s_hmax[pe & 1][0][1][n]);
