@@ -46,8 +46,7 @@ constexpr int kTile = 128;          // KV tokens per tile (UMMA M)
 constexpr int kPage = 16;           // tokens per page
 constexpr int kStageBytes = 32768;  // one K or V tile: 2 halves x 8 pages x 16 slots x 128 B
 constexpr int kHalfBytes = 16384;
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxThreads = 128;   // transposed mode: warps 2-5, after producer and MMA
 // the rows-on-M kernel: two softmax warps per tensor-memory lane quadrant
 constexpr int kRowSoftmaxThreads = 256;
 // threads of a CTA: the transposed mode has warps 0-1 (producer, MMA) and 4 softmax warps; with
