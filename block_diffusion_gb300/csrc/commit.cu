@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRing = 3;              // shared-memory stages per warp
+constexpr int kRing = 2;              // shared-memory stages per warp
 constexpr int kChunkBytes = 4096;     // bytes per stage
 constexpr int kChunk = kChunkBytes / 2;
 constexpr int kUnroll = 4;            // 16-byte vectors per lane per group of 32 logits
