@@ -56,7 +56,8 @@ class RoundLoopDesc(ctypes.Structure):
                 ("q_steps", _P), ("k_new_steps", _P), ("v_new_steps", _P), ("hidden_steps", _P),
                 ("k_pages", _P), ("v_pages", _P), ("page_table", _P), ("prefix_lens", _P),
                 ("w", _P), ("mask", _P), ("denoising", _P), ("tok_steps", _P),
-                ("conf_steps", _P), ("commit_steps", _P), ("steps_done", _P)]
+                ("conf_steps", _P), ("commit_steps", _P), ("steps_done", _P),
+                ("attn_out_steps", _P)]
 
 
 class BdlmError(RuntimeError):

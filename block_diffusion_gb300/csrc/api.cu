@@ -149,16 +149,25 @@ const char* bdlm_status_string(int status) {
 
 int bdlm_device_error(int* bits_out) {
   if (!bits_out) return BDLM_ERR_INVALID;
-  std::lock_guard<std::mutex> lk(g_mu);
-  DeviceState* st = nullptr;
-  int rc = current_device(&st);
-  if (rc) return rc;
-  int v = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BDLM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return BDLM_ERR_UNSUPPORTED;
   if (cudaDeviceSynchronize() != cudaSuccess) return BDLM_ERR_CUDA;
-  if (cudaMemcpy(&v, st->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return BDLM_ERR_CUDA;
-  if (cudaMemset(st->err, 0, sizeof(int)) != cudaSuccess) return BDLM_ERR_CUDA;
-  *bits_out = v;
+  int v = 0;
+  {
+    // the workspace's word exists once an allocating call has run on this device
+    std::lock_guard<std::mutex> lk(g_mu);
+    const DeviceState& s = g_dev[dev];
+    if (s.err) {
+      if (cudaMemcpy(&v, s.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return BDLM_ERR_CUDA;
+      if (cudaMemset(s.err, 0, sizeof(int)) != cudaSuccess) return BDLM_ERR_CUDA;
+    }
+  }
+  int w = 0;
+  const int rc = bdlm::noalloc_take_error(dev, &w);  // bdlm_confidence_commit_noalloc's word
+  if (rc) return rc;
+  *bits_out = v | w;
   return BDLM_OK;
 }
 
@@ -621,6 +630,9 @@ int capture_round_loop(bdlm_round_loop* lp) {
                                     nullptr, s);
   if (!r2 && bdlm::launch_record_step(lp->step, d.steps, R, lp->tok, lp->conf, lp->com,
                                       d.tok_steps, d.conf_steps, d.commit_steps,
+                                      reinterpret_cast<const uint4*>(lp->attn_out),
+                                      reinterpret_cast<uint4*>(d.attn_out_steps),
+                                      static_cast<long long>(R) * a.Hq * a.D * 2 / 16,
                                       lp->cap) != cudaSuccess)
     r2 = BDLM_ERR_CUDA;
   if (!r2) r2 = bdlm_apply_commit(d.mask, lp->com, R, s);
@@ -655,6 +667,7 @@ int bdlm_round_loop_create(const bdlm_round_loop_desc* desc, bdlm_round_loop** o
       !d.v_pages || !d.page_table || !d.prefix_lens || !d.w || !d.mask || !d.tok_steps ||
       !d.conf_steps || !d.commit_steps || !d.steps_done)
     return BDLM_ERR_INVALID;
+  if (d.attn_out_steps && !aligned16(d.attn_out_steps)) return BDLM_ERR_INVALID;
   const long long R = static_cast<long long>(a.B) * a.L;
   if (R * a.Hq > 0x7FFFFFFFll || R * d.V > (1ll << 40)) return BDLM_ERR_INVALID;
   auto* lp = new bdlm_round_loop();

@@ -516,7 +516,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint64_t kv_policy = l2_policy_evict_first();
     int st = 0;
     uint32_t ph = 0;
-    while (mbar_wait(&bar_sready[st], ph, &abort_flag)) {
+    while (mbar_wait_warp(&bar_sready[st], ph, &abort_flag)) {
       const StageInfo& si = s_sinfo[st];
       if (si.end) break;
       if (lane < kTile / kPage) {
@@ -810,7 +810,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int u = 0, pe = 0, pair_ends = 0;
     for (int seq = 0; ok; ++seq) {
       const int rs = seq % kItemRing;
-      if (!(ok = mbar_wait(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      if (!(ok = mbar_wait_warp(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
       const Item it = s_item[rs];
       mbar_arrive(&bar_iempty[rs]);   // the descriptor is in registers: its slot may be reused
       if (it.end) break;
@@ -820,7 +820,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       if constexpr (MASKED) lim = (i_row / p.mask_block + 1) * p.mask_block;
       float m_run = -CUDART_INF_F, l_run = 0.f;       // l_run: this half's sum
       for (int c = 0; c < it.n_chunks && ok; ++c, ++u) {
-        if (!(ok = mbar_wait(&bar_sfull[x], u & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp(&bar_sfull[x], u & 1, &abort_flag))) break;
         tc_fence_after();
         const int key0 = it.t_begin + c * kTile;
         int nvalid = min(kTile, it.t_end - key0);
@@ -841,7 +841,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         s_hmax[pe & 1][x][half][n] = mx;
         mbar_arrive(&bar_pair[pq][pe & 1]);
-        if (!(ok = mbar_wait(&bar_pair[pq][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp(&bar_pair[pq][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
         mx = fmaxf(s_hmax[pe & 1][x][0][n], s_hmax[pe & 1][x][1][n]);
         ++pe;
         // the running max moves only when the tile raises it by more than 2^kLazyRescale
@@ -875,7 +875,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (__any_sync(0xffffffffu, resc)) {
           // bring this warp's half of its rows of O to the new maxima once the previous
           // tile's PV is done
-          if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
           tc_fence_after();
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -894,11 +894,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (c != it.n_chunks - 1) continue;
         // ---- epilogue of the item: this half of the row of O, divided by the row's sum or as
         // a split partial
-        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
         s_hsum[pair_ends & 1][x][half][n] = l_run;
         mbar_arrive(&bar_pair_end[pq]);
-        if (!(ok = mbar_wait(&bar_pair_end[pq], pair_ends & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp(&bar_pair_end[pq], pair_ends & 1, &abort_flag))) break;
         const float l_row = s_hsum[pair_ends & 1][x][0][n] + s_hsum[pair_ends & 1][x][1][n];
         ++pair_ends;
         const bool live = r_item < p.rows_per_group && i_row < p.L;
@@ -959,7 +959,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int pcount = 0, u = 0, pe = 0, pair_ends = 0;   // pe, pair_ends: exchanges so far
     for (int seq = 0; ok; ++seq) {
       const int rs = seq % kItemRing;
-      if (!(ok = mbar_wait(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      if (!(ok = mbar_wait_warp(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
       const Item it = s_item[rs];
       mbar_arrive(&bar_iempty[rs]);   // the descriptor is in registers: its slot may be reused
       if (it.end) break;
@@ -980,7 +980,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           const int sb = kSub == 1 ? (u & 1) : x;
           const uint32_t sph = kSub == 1 ? ((u >> 1) & 1) : (u & 1);
           const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(sb * N) + col0;
-          if (!(ok = mbar_wait(&bar_sfull[sb], sph, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp(&bar_sfull[sb], sph, &abort_flag))) break;
           tc_fence_after();
           uint32_t r[64];
 #pragma unroll
@@ -1008,7 +1008,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     max32<true>(*reinterpret_cast<const uint32_t(*)[32]>(r + 32), 0, 0));
           s_hmax[pe & 1][0][half][n] = hmax;
           mbar_arrive(&bar_pair[q4][pe & 1]);
-          if (!(ok = mbar_wait(&bar_pair[q4][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp(&bar_pair[q4][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
           const float mx = fmaxf(s_hmax[pe & 1][0][0][n], s_hmax[pe & 1][0][1][n]);
           ++pe;
           // the running max moves only when the tile raises it by more than 2^kLazyRescale
@@ -1045,7 +1045,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           if (__any_sync(0xffffffffu, resc)) {
             // bring this warp's half of its rows of O to the new maxima once the previous
             // tile's PV is done
-            if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+            if (!(ok = mbar_wait_warp(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
             tc_fence_after();
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -1072,7 +1072,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (!ok || c != it.n_chunks - 1) continue;
         // ---- epilogue of the item: this half of each row of O, divided by the row's sum or
         // as a split partial
-        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
         const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
         float* mine =
@@ -1081,7 +1081,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         for (int x = 0; x < kSub; ++x) {
           s_hsum[pair_ends & 1][0][half][n] = l_run[x];
           mbar_arrive(&bar_pair_end[q4]);
-          if (!(ok = mbar_wait(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
           const float l_row = s_hsum[pair_ends & 1][0][0][n] + s_hsum[pair_ends & 1][0][1][n];
           ++pair_ends;
           const int r_item = x * N + n;   // row of the item
@@ -1137,7 +1137,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int pcount = 0, u = 0;
     for (int seq = 0; ok; ++seq) {
       const int rs = seq % kItemRing;
-      if (!(ok = mbar_wait(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      if (!(ok = mbar_wait_warp(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
       const Item it = s_item[rs];
       if (it.end) break;
 #pragma unroll
@@ -1147,7 +1147,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         const uint32_t tS = tmem + lane_off + static_cast<uint32_t>((u & 1) * p.chunk_tiles * N);
-        if (!(ok = mbar_wait(&bar_sfull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp(&bar_sfull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
         // phase A: exact column maxima over the chunk
 #pragma unroll
@@ -1201,7 +1201,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const bool need = s_need[u & 1] != 0;
         if (c > 0 && need) {
           // rescale the running O^T columns (and l) to the new maxima
-          if (!(ok = mbar_wait(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
           tc_fence_after();
 #pragma unroll
           for (int cg = 0; cg < N / 16; ++cg) {
@@ -1251,7 +1251,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
               }
             }
             const int pb = pcount & 1;
-            if (!(ok = mbar_wait(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1, &abort_flag))) break;
+            if (!(ok = mbar_wait_warp(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1, &abort_flag))) break;
             uint8_t* pbuf = sP + pb * (N * 256) + (x >> 6) * (N * 128);
             const uint32_t xc = (x & 63) >> 3;
             const uint32_t xb = (x & 7) * 2;
@@ -1274,7 +1274,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_arrive(&bar_sfree[u & 1]);
         if (c != it.n_chunks - 1) continue;
         // ---- epilogue of the item
-        if (!(ok = mbar_wait(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int n = 0; n < N; ++n) {
@@ -1531,18 +1531,17 @@ template <int N, int STAGES, int CPS, bool MASKED, bool ROWS, bool TWO>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const AttnParams& prm, int num_sms, cudaStream_t stream) {
   constexpr size_t smem = smem_bytes<N, STAGES, ROWS, TWO>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>,
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [] {
+    cudaError_t r = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>,
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(attn_kernel<N, STAGES, CPS, MASKED, ROWS, TWO>, dim3(num_sms * CPS),
                     dim3(attn_threads(ROWS, TWO)), smem,
                     stream, tq, tk, tv, prm);

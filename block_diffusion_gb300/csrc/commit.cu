@@ -9,7 +9,7 @@
 // Layout of the work: the masked rows, laid end to end, form one sequence of T = n_masked * V
 // logits that is cut evenly across every warp of a persistent grid (each CTA first counts the
 // mask to learn n_masked and where each masked row sits).  A warp streams its range through a
-// private ring of three 4 KB shared-memory stages filled by bulk copies (one instruction per
+// private ring of two 4 KB shared-memory stages filled by bulk copies (one instruction per
 // stage), keeping a running (max, sum of exp, first argmax) per lane, and at the end of each
 // row segment merges its lanes with shuffles into one partial: that is all it writes.  A second
 // kernel, one CTA per block, then merges each masked row's partials in warp order, writes
@@ -208,7 +208,10 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
   lane_reset(acc);
   for (int u = 0; u < issued; ++u) {
     const int slot = u % kRing;
-    if (!mbar_wait(&bars[slot], (u / kRing) & 1, &abort_flag)) {
+    // every lane waits on its own clock; the warp then agrees on the outcome, so no lane
+    // leaves for the drain while the others go on to the full-warp shuffles below
+    const bool landed = mbar_wait(&bars[slot], (u / kRing) & 1, &abort_flag);
+    if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0 && a.err) atomicOr(a.err, BDLM_DEVERR_TIMEOUT);
       break;
     }
@@ -441,13 +444,13 @@ cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, in
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
                           uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
                           int* err, cudaStream_t stream, bool programmatic, int rule, int k) {
-  static size_t attr = 0;
-  if (plan.smem_bytes > attr) {
-    cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(plan.smem_bytes));
-    if (e != cudaSuccess) return e;
-    attr = plan.smem_bytes;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const int smem_bytes = static_cast<int>(plan.smem_bytes);  // the same for every plan
+  cudaError_t ea = once_per_device(attr_done, [smem_bytes] {
+    return cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes);
+  });
+  if (ea != cudaSuccess) return ea;
   CommitArgs args;
   args.logits = logits;
   args.mask = mask;

@@ -16,8 +16,11 @@
 //  * The first call on a device looks the array's device address up (cudaGetSymbolAddress)
 //    with that device current; make that first call before any stream capture.
 //  * Every call shares the one array: calls that overlap on the GPU (different streams, or
-//    different host threads without ordering) race and give wrong results.  Each call clears
-//    the array's device error word with cudaMemsetAsync on its own stream before the kernels.
+//    different host threads without ordering) race and give wrong results.
+//  * A device error of these kernels (a bounded wait that gave up) is recorded in the error
+//    word at the head of the array.  bdlm_device_error() reads and clears it together with the
+//    workspace's word, and allocates nothing either; the calls never clear it themselves, so a
+//    recorded error stays until it is read.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -71,6 +74,24 @@ int scratch_address(void** out, int* num_sms) {
 
 }  // namespace
 
+namespace bdlm {
+// Reads and clears the fixed array's device error word on device `dev` into *bits (0 when no
+// call has set the array up on that device).  Allocates nothing.
+int noalloc_take_error(int dev, int* bits) {
+  *bits = 0;
+  if (dev < 0 || dev >= kMaxDevices) return BDLM_OK;
+  void* p = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    p = g_noalloc_ptr[dev];
+  }
+  if (p == nullptr) return BDLM_OK;
+  if (cudaMemcpy(bits, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return BDLM_ERR_CUDA;
+  if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return BDLM_ERR_CUDA;
+  return BDLM_OK;
+}
+}  // namespace bdlm
+
 extern "C" int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uint8_t* mask, int B,
                                               int L, int V, float threshold, float temperature,
                                               int32_t* tok_out, float* conf_out,
@@ -90,11 +111,9 @@ extern "C" int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uin
   if (plan.part_bytes > kPartialBytes) return BDLM_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(base);
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return BDLM_ERR_CUDA;
   auto* part = reinterpret_cast<bdlm::CommitPartial*>(static_cast<unsigned char*>(base) +
                                                       kCounterBytes);
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
-                                      conf_out, commit_out, plan, part, err, s,
-                                      /*programmatic=*/false);  // ordered after the memset
+                                      conf_out, commit_out, plan, part, err, s);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/bdlm.h"
 
 namespace bdlm {
@@ -27,6 +29,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Runs `set` (a kernel-attribute setter) once per device: function attributes belong to a
+// device's context, so a flag per process would leave a second device without them.  Two
+// threads may both run `set` the first time; it is idempotent.  Devices past 63 run it on
+// every call.
+template <typename F>
+cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 // ------------------------------------------------------------------ commit
@@ -52,6 +70,9 @@ cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, in
                           int* err, cudaStream_t stream, bool programmatic = true,
                           int rule = BDLM_COMMIT_THRESHOLD, int k = 1);
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
+// The error word of bdlm_confidence_commit_noalloc's fixed array on device `dev`, read and
+// cleared (0 if the array was never set up there); allocates nothing.
+int noalloc_take_error(int dev, int* bits);
 
 // ------------------------------------------------------------------ attention
 struct AttnPlan {
@@ -149,9 +170,11 @@ struct StepCopy {  // per-step inputs: slice s of src[j] (n_vec[j] 16-byte vecto
 };
 cudaError_t launch_select_step(const StepCopy& c, const int* step, int n_steps,
                                cudaStream_t stream);
+// out_s (may be null): per-step copies of out (out_vec 16-byte vectors per step).
 cudaError_t launch_record_step(const int* step, int n_steps, int R, const int32_t* tok,
                                const float* conf, const uint8_t* commit, int32_t* tok_s,
-                               float* conf_s, uint8_t* commit_s, cudaStream_t stream);
+                               float* conf_s, uint8_t* commit_s, const uint4* out, uint4* out_s,
+                               long long out_vec, cudaStream_t stream);
 cudaError_t launch_loop_condition(cudaGraphConditionalHandle handle, const uint8_t* mask, int R,
                                   int* step, int n_steps, int* steps_done, cudaStream_t stream);
 cudaError_t launch_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,

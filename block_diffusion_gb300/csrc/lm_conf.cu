@@ -218,7 +218,7 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     }
     bool ok = true;
     for (int j = 0; j < n_jobs; ++j) {
-      if (!ok || !(ok = mbar_wait(&acc_full, j & 1, &abort_flag))) break;
+      if (!ok || !(ok = mbar_wait_warp(&acc_full, j & 1, &abort_flag))) break;
       tc_fence_after();
       const int vbase = (m_first + j * per_tile) * kConfN + col0;
       // Sub-tile by sub-tile (the registers hold one row's 64 logits at a time): read the
@@ -522,7 +522,7 @@ lm_conf_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
     bool ok = true;
     for (int j = 0; j < n_jobs; ++j) {
       const int buf = j & 1;
-      if (!ok || !(ok = mbar_wait(&acc_full[buf], (j >> 1) & 1, &abort_flag))) break;
+      if (!ok || !(ok = mbar_wait_warp(&acc_full[buf], (j >> 1) & 1, &abort_flag))) break;
       tc_fence_after();
       const int vbase = jobs.col0(j) + col0;
       const int vend = min(jobs.col0(j) + jobs.width(j), p.V);   // the tile's last column + 1
@@ -826,13 +826,12 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            int n_rows, int H, int V, float temperature, uint16_t* logits,
                            CommitPartial* part, const LmConfPlan& plan, int* err,
                            cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lm_conf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(lm_conf_smem()));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(lm_conf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(lm_conf_smem()));
+  });
+  if (ea != cudaSuccess) return ea;
   LmConfParams prm;
   prm.active_idx = active_idx;
   prm.n_active_dev = n_active_dev;

@@ -241,7 +241,7 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         s_rows[j] = (row >= 0 && row < p.n_rows) ? row : -1;
       }
       named_barrier(1, kEpiThreads);
-      if (!ok || !(ok = mbar_wait(&acc_full[acc], (i / kBufs) & 1, &abort_flag))) continue;
+      if (!ok || !(ok = mbar_wait_warp(&acc_full[acc], (i / kBufs) & 1, &abort_flag))) continue;
       tc_fence_after();
       const int v0 = m * (kSub * kBM) + x;       // sub-tile 0; sub-tile 1 is kBM further
       const bool ok0 = v0 < p.V, ok1 = v0 + kBM < p.V;
@@ -292,15 +292,14 @@ size_t lm_smem() {
 template <int BN_MAX>
 cudaError_t launch_bn(const CUtensorMap& tw, const CUtensorMap& th, const LmParams& prm, int grid,
                       cudaStream_t stream) {
-  static bool attr_set = false;
+  static std::atomic<unsigned long long> attr_done{0};
   const size_t smem = lm_smem<BN_MAX>();
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lm_head_kernel<BN_MAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = once_per_device(attr_done, [smem] {
+    return cudaFuncSetAttribute(lm_head_kernel<BN_MAX>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(lm_head_kernel<BN_MAX>, dim3(grid), dim3(kThreads), smem, stream, tw, th,
                     prm);
 }

@@ -80,6 +80,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait called by all 32 lanes of a warp: the lanes agree on the outcome, so no lane goes
+// on to warp-collective instructions (tcgen05.ld, shuffles, __syncwarp) while another has
+// given up.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
 // ------------------------------------------------------------------ proxies / barriers
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

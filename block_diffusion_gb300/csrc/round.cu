@@ -105,11 +105,14 @@ __global__ void select_step_kernel(StepCopy c, const int* __restrict__ step, int
   }
 }
 
-// Stores this step's tok/conf/commit into slice *step of the per-step outputs.
+// Stores this step's tok/conf/commit (and, when out_s is given, the attention output: out_vec
+// 16-byte vectors) into slice *step of the per-step outputs.
 __global__ void record_step_kernel(const int* __restrict__ step, int n_steps, int R,
                                    const int32_t* __restrict__ tok, const float* __restrict__ conf,
                                    const uint8_t* __restrict__ commit, int32_t* __restrict__ tok_s,
-                                   float* __restrict__ conf_s, uint8_t* __restrict__ commit_s) {
+                                   float* __restrict__ conf_s, uint8_t* __restrict__ commit_s,
+                                   const uint4* __restrict__ out, uint4* __restrict__ out_s,
+                                   long long out_vec) {
   griddep_wait();
   griddep_launch_dependents();
   const int s = *step;
@@ -120,6 +123,12 @@ __global__ void record_step_kernel(const int* __restrict__ step, int n_steps, in
     conf_s[o] = conf[r];
     commit_s[o] = commit[r];
   }
+  if (out_s == nullptr) return;
+  uint4* dst = out_s + s * out_vec;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < out_vec;
+       v += stride)
+    dst[v] = out[v];
 }
 
 // End of a round: counts it, and repeats the loop while some position is still masked and
@@ -153,10 +162,16 @@ cudaError_t launch_select_step(const StepCopy& c, const int* step, int n_steps,
 
 cudaError_t launch_record_step(const int* step, int n_steps, int R, const int32_t* tok,
                                const float* conf, const uint8_t* commit, int32_t* tok_s,
-                               float* conf_s, uint8_t* commit_s, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>((R + 255) / 256);
+                               float* conf_s, uint8_t* commit_s, const uint4* out, uint4* out_s,
+                               long long out_vec, cudaStream_t stream) {
+  long long blocks = (R + 255) / 256;
+  if (out_s != nullptr) {
+    const long long ob = (out_vec + 255) / 256;
+    if (ob > blocks) blocks = ob > 1216 ? 1216 : ob;
+  }
+  const unsigned grid = static_cast<unsigned>(blocks < 1 ? 1 : blocks);
   return launch_pdl(record_step_kernel, dim3(grid), dim3(256), 0, stream, step, n_steps, R, tok,
-                    conf, commit, tok_s, conf_s, commit_s);
+                    conf, commit, tok_s, conf_s, commit_s, out, out_s, out_vec);
 }
 
 cudaError_t launch_loop_condition(cudaGraphConditionalHandle handle, const uint8_t* mask, int R,

@@ -249,8 +249,11 @@ int bdlm_confidence_commit_rule(const bdlm_bf16* logits, const uint8_t* mask, in
  *    before any launch.
  *  - The first call on a device looks up the array's address with that device current;
  *    make that first call before any stream capture.
- *  - All calls share the array, which keeps the last call's contents: each call clears its
- *    error word on `stream` first, and calls that overlap on the GPU race.
+ *  - All calls share the array, which keeps the last call's contents; calls that overlap on
+ *    the GPU race.
+ *  - A device error of this call (a bounded wait inside a kernel that gave up) is recorded
+ *    in an error word at the head of the array; bdlm_device_error() reads and clears it
+ *    (it allocates nothing either).  The calls themselves never clear it.
  */
 int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uint8_t* mask, int B, int L,
                                    int V, float threshold, float temperature, int32_t* tok_out,
@@ -310,7 +313,8 @@ int bdlm_apply_commit(uint8_t* mask, const uint8_t* commit, int n, bdlm_stream s
  *   conf_steps, commit_steps [S, B, L] -> bdlm_apply_commit on mask.
  * After the last round *steps_done holds the number of rounds run, and slices at or past it
  * are untouched.  The attention output is kept in the loop's own scratch (a model would feed
- * it to its next layer).
+ * it to its next layer); when attn_out_steps [S, B, L, Hq, D] bf16 is given, each round also
+ * copies it into slice s.
  *
  * All pointers are device pointers owned by the caller and must stay valid while the loop
  * exists.  bdlm_round_loop_create allocates the loop's scratch (one step's inputs, the
@@ -341,6 +345,7 @@ typedef struct {
   float* conf_steps;
   uint8_t* commit_steps;
   int32_t* steps_done;        /* one int32 */
+  bdlm_bf16* attn_out_steps;  /* [S, B, L, Hq, D] or NULL */
 } bdlm_round_loop_desc;
 
 int bdlm_round_loop_create(const bdlm_round_loop_desc* desc, bdlm_round_loop** loop_out);
@@ -353,8 +358,11 @@ int bdlm_round_loop_destroy(bdlm_round_loop* loop);
 const char* bdlm_status_string(int status);
 
 /*
- * Reads and clears the device error word of the current device (BDLM_DEVERR_* bits) into
- * *bits_out (a HOST pointer).  Synchronises the device.  Returns BDLM_OK or an error.
+ * Reads and clears the device error words of the current device (BDLM_DEVERR_* bits) into
+ * *bits_out (a HOST pointer): the workspace's word, written by every call except
+ * bdlm_confidence_commit_noalloc, ORed with the word of that call's fixed array.  Allocates
+ * nothing (a word that no call has set up yet reads as 0).  Synchronises the device.
+ * Returns BDLM_OK or an error.
  */
 int bdlm_device_error(int* bits_out);
 

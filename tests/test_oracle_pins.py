@@ -365,6 +365,48 @@ def test_written_block_kv_is_what_attention_reads():
     assert np.array_equal(k[untouched], a.k_ref[untouched])
 
 
+def test_block_kv_write_by_hand_across_a_page_boundary():
+    """Prefix 14, L = 4, pages of 16, page-table row [5, 2, 7]: block tokens 0 and 1 land in
+    page 5, slots 14 and 15; tokens 2 and 3 in page 2, slots 0 and 1 (coordinates worked out by
+    hand).  Every other slot of the pool keeps its value."""
+    Hkv, D = 2, 3
+    k0 = np.arange(8 * 16 * Hkv * D, dtype=np.uint16).reshape(8, 16, Hkv, D)
+    v0 = k0 + 7000
+    kn = (50000 + np.arange(4 * Hkv * D, dtype=np.uint16)).reshape(1, 4, Hkv, D)
+    vn = kn + 5000
+    pt = np.array([[5, 2, 7]], np.int32)
+    k, v = oracle.write_block_kv(k0, v0, pt, np.array([14], np.int32), kn, vn, P=16)
+    want_k, want_v = k0.copy(), v0.copy()
+    for tok, (page, slot) in enumerate([(5, 14), (5, 15), (2, 0), (2, 1)]):
+        want_k[page, slot] = kn[0, tok]
+        want_v[page, slot] = vn[0, tok]
+    assert np.array_equal(k, want_k) and np.array_equal(v, want_v)
+
+
+def test_block_kv_write_against_gathered_sequences():
+    """The written cache read back a second way: each sequence's pages gathered whole and laid
+    end to end give its tokens in order; the block's L tokens follow the untouched prefix, and
+    pages no sequence uses keep their contents."""
+    rng = np.random.default_rng(29)
+    B, L, Hkv, D = 5, 7, 2, 128
+    a = make_attention(rng, B, L, 4, Hkv, D, prefix_range=(0, 60), poison=False)
+    kn = f32_to_bf16_bits(rng.normal(0, 0.5, (B, L, Hkv, D)).astype(np.float32))
+    vn = f32_to_bf16_bits(rng.normal(0, 0.5, (B, L, Hkv, D)).astype(np.float32))
+    k, v = oracle.write_block_kv(a.k_ref, a.v_ref, a.page_table_ref, a.prefix_lens, kn, vn)
+    used = np.zeros(a.k_ref.shape[0], bool)
+    for b in range(B):
+        pages = a.page_table_ref[b][a.page_table_ref[b] >= 0]
+        used[pages] = True
+        n = int(a.prefix_lens[b])
+        for pool0, pool1, new in ((a.k_ref, k, kn), (a.v_ref, v, vn)):
+            before = pool0[pages].reshape(-1, Hkv, D)
+            after = pool1[pages].reshape(-1, Hkv, D)
+            assert np.array_equal(after[:n], before[:n])
+            assert np.array_equal(after[n:n + L], new[b])
+            assert np.array_equal(after[n + L:], before[n + L:])
+    assert np.array_equal(k[~used], a.k_ref[~used]) and np.array_equal(v[~used], a.v_ref[~used])
+
+
 def test_prefill_oracle_against_dense_block_causal_attention():
     """A fresh prompt of three blocks: the block-by-block paged prefill equals dense attention
     with the block-causal mask over the whole prompt."""

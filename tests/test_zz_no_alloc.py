@@ -4,15 +4,18 @@ The no-allocation entry point serves callers that cannot let the library call cu
 (an engine that owns all of the GPU's memory, a loop that cannot absorb an allocation's
 implicit synchronisation).  It must give the same tokens, confidences (within the 1e-5
 relative tolerance used elsewhere) and commit masks as the allocating entry point, on two
-calls in a row that reuse its fixed scratch array.  This file is collected last so that a
-run that stops at the first failure has already run every other test.
+calls in a row that reuse its fixed scratch array, and agree with the fp64 oracle; its device
+error word (read through bdlm_device_error) stays clear.  This file is collected last so that
+a run that stops at the first failure has already run every other test.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import workloads as W
+from gpu_util import compare_commit
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +64,10 @@ def test_noalloc_matches_allocating_entry_point_twice(lib):
         assert rel.max() <= 1e-5
         assert np.all(np.isneginf(c1[~m]))
         assert np.array_equal(m0, m1)
+        # and the oracle, on the same bf16 logits
+        ref = oracle.confidence_commit(logits, mask, 0.5, 1.0)
+        compare_commit(ref, t1, c1, m1, mask)
+    # no bounded wait gave up in either entry point (bdlm_device_error reads both words)
     assert lib.bdlm_device_error() == 0
 
 
