@@ -230,9 +230,9 @@ class Round:
     STAGES = {"fused": ("attention", "lm_head_commit", "mask_update"),
               "unfused": ("attention", "lm_head", "commit", "mask_update"),
               "supplied": ("attention", "commit", "mask_update")}
-    # attention + split merge; [scored rows + row gather + fused GEMM + finalize |
-    # row gather + LM head]; commit streaming + finalize; mask update
-    LAUNCHES = {"fused": 2 + 4 + 1, "unfused": 2 + 2 + 2 + 1, "supplied": 2 + 2 + 1}
+    # attention + split merge; [scored rows + fused GEMM + finalize | row gather + LM head];
+    # commit (one launch); mask update
+    LAUNCHES = {"fused": 2 + 3 + 1, "unfused": 2 + 2 + 1 + 1, "supplied": 2 + 1 + 1}
 
     def __init__(self, lib, a, ci, lm, device, mode="fused"):
         import torch

@@ -31,6 +31,7 @@ BDLM_COMMIT_THRESHOLD = 0
 BDLM_COMMIT_TOPK = 1
 BDLM_COMMIT_SEQUENTIAL = 2
 BDLM_COMMIT_ANTI_SEQUENTIAL = 3
+BDLM_COMMIT_ENTROPY_BOUNDED = 4
 
 EXPORTS = ("bdlm_block_attention", "bdlm_prefill_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
            "bdlm_lm_head_commit", "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
@@ -84,11 +85,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bdlm_lm_head.restype = I
     lib.bdlm_confidence_commit.argtypes = [P, P, I, I, I, F, F, P, P, P, P]
     lib.bdlm_confidence_commit.restype = I
-    lib.bdlm_confidence_commit_rule.argtypes = [P, P, I, I, I, I, I, F, F, P, P, P, P]
+    lib.bdlm_confidence_commit_rule.argtypes = [P, P, I, I, I, I, I, F, F, P, P, P, P, P]
     lib.bdlm_confidence_commit_rule.restype = I
     lib.bdlm_lm_head_device_count.argtypes = [P, P, P, P, I, I, I, I, P, P]
     lib.bdlm_lm_head_device_count.restype = I
-    lib.bdlm_lm_head_commit.argtypes = [P, P, P, P, I, I, I, I, I, I, F, F, P, P, P, P, P]
+    lib.bdlm_lm_head_commit.argtypes = [P, P, P, P, I, I, I, I, I, I, F, F, P, P, P, P, P, P]
     lib.bdlm_lm_head_commit.restype = I
     lib.bdlm_active_rows.argtypes = [P, P, I, I, P, P, P]
     lib.bdlm_active_rows.restype = I
@@ -183,12 +184,13 @@ def bdlm_confidence_commit(logits, mask, B: int, L: int, V: int, threshold: floa
 
 def bdlm_confidence_commit_rule(logits, mask, B: int, L: int, V: int, rule: int, k: int,
                                 threshold: float, temperature: float, tok_out, conf_out,
-                                commit_out, stream=None) -> None:
+                                commit_out, stream=None, entropy_out=None) -> None:
+    """entropy_out (keyword; the C call takes it between conf_out and commit_out) may be None."""
     lib = load_library()
     rc = lib.bdlm_confidence_commit_rule(_ptr(logits), _ptr(mask), int(B), int(L), int(V),
                                          int(rule), int(k), float(threshold), float(temperature),
-                                         _ptr(tok_out), _ptr(conf_out), _ptr(commit_out),
-                                         _stream(stream))
+                                         _ptr(tok_out), _ptr(conf_out), _ptr(entropy_out),
+                                         _ptr(commit_out), _stream(stream))
     _check("bdlm_confidence_commit_rule", rc)
 
 
@@ -203,12 +205,14 @@ def bdlm_lm_head_device_count(hidden, w, active_idx, n_active_dev, max_active: i
 
 def bdlm_lm_head_commit(hidden, w, mask, denoising, B: int, L: int, H: int, V: int, rule: int,
                         k: int, threshold: float, temperature: float, tok_out, conf_out,
-                        commit_out, logits=None, stream=None) -> None:
+                        commit_out, logits=None, stream=None, entropy_out=None) -> None:
+    """entropy_out (keyword; the C call takes it between conf_out and commit_out) may be None."""
     lib = load_library()
     rc = lib.bdlm_lm_head_commit(_ptr(hidden), _ptr(w), _ptr(mask), _ptr(denoising), int(B),
                                  int(L), int(H), int(V), int(rule), int(k), float(threshold),
                                  float(temperature), _ptr(tok_out), _ptr(conf_out),
-                                 _ptr(commit_out), _ptr(logits), _stream(stream))
+                                 _ptr(entropy_out), _ptr(commit_out), _ptr(logits),
+                                 _stream(stream))
     _check("bdlm_lm_head_commit", rc)
 
 

@@ -112,6 +112,19 @@ int encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Arguments of a commit rule: the threshold rule wants 0 <= threshold <= 1, the entropy rule a
+// finite budget >= 0 (in `threshold`), the others k >= 1.
+bool rule_ok(int rule, int k, float threshold) {
+  switch (rule) {
+    case BDLM_COMMIT_THRESHOLD: return threshold >= 0.f && threshold <= 1.f;
+    case BDLM_COMMIT_ENTROPY_BOUNDED: return threshold >= 0.f && isfinite(threshold);
+    case BDLM_COMMIT_TOPK:
+    case BDLM_COMMIT_SEQUENTIAL:
+    case BDLM_COMMIT_ANTI_SEQUENTIAL: return k >= 1;
+    default: return false;
+  }
+}
+
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
 // Workspace of the fused LM head + commit: gathered rows | partials | scored-row list | count.
@@ -192,19 +205,16 @@ int bdlm_confidence_commit(const bdlm_bf16* logits, const uint8_t* mask, int B, 
                            float threshold, float temperature, int32_t* tok_out,
                            float* conf_out, uint8_t* commit_out, bdlm_stream stream) {
   return bdlm_confidence_commit_rule(logits, mask, B, L, V, BDLM_COMMIT_THRESHOLD, 1, threshold,
-                                     temperature, tok_out, conf_out, commit_out, stream);
+                                     temperature, tok_out, conf_out, nullptr, commit_out, stream);
 }
 
 int bdlm_confidence_commit_rule(const bdlm_bf16* logits, const uint8_t* mask, int B, int L, int V,
                                 int rule, int k, float threshold, float temperature,
-                                int32_t* tok_out, float* conf_out, uint8_t* commit_out,
-                                bdlm_stream stream) {
+                                int32_t* tok_out, float* conf_out, float* entropy_out,
+                                uint8_t* commit_out, bdlm_stream stream) {
   if (B < 0 || L < 1 || L > 64 || V < 1) return BDLM_ERR_INVALID;
   if (!(temperature > 0.f) || !isfinite(temperature)) return BDLM_ERR_INVALID;
-  if (rule < BDLM_COMMIT_THRESHOLD || rule > BDLM_COMMIT_ANTI_SEQUENTIAL) return BDLM_ERR_INVALID;
-  if (rule == BDLM_COMMIT_THRESHOLD && !(threshold >= 0.f && threshold <= 1.f))
-    return BDLM_ERR_INVALID;
-  if (rule != BDLM_COMMIT_THRESHOLD && k < 1) return BDLM_ERR_INVALID;
+  if (!rule_ok(rule, k, threshold)) return BDLM_ERR_INVALID;
   if (B == 0) return BDLM_OK;
   if (!logits || !mask || !tok_out || !conf_out || !commit_out) return BDLM_ERR_INVALID;
   if (static_cast<long long>(B) * L > 0x7FFFFFFFll) return BDLM_ERR_INVALID;
@@ -217,9 +227,9 @@ int bdlm_confidence_commit_rule(const bdlm_bf16* logits, const uint8_t* mask, in
   rc = ensure(&st->data, &st->data_cap, plan.part_bytes, false);
   if (rc) return rc;
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
-                                      conf_out, commit_out, plan,
+                                      conf_out, entropy_out, commit_out, plan,
                                       static_cast<bdlm::CommitPartial*>(st->data), st->err,
-                                      static_cast<cudaStream_t>(stream), true, rule, k);
+                                      static_cast<cudaStream_t>(stream), rule, k);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 
@@ -462,14 +472,12 @@ int bdlm_write_block_kv(const bdlm_attn_desc* desc, const bdlm_bf16* k_new,
 int bdlm_lm_head_commit(const bdlm_bf16* hidden, const bdlm_bf16* w, const uint8_t* mask,
                         const uint8_t* denoising, int B, int L, int H, int V, int rule, int k,
                         float threshold, float temperature, int32_t* tok_out, float* conf_out,
-                        uint8_t* commit_out, bdlm_bf16* logits, bdlm_stream stream) {
+                        float* entropy_out, uint8_t* commit_out, bdlm_bf16* logits,
+                        bdlm_stream stream) {
   if (B < 0 || L < 1 || L > 64 || H < 8 || V < 8 || H % 8 != 0 || V % 8 != 0)
     return BDLM_ERR_INVALID;
   if (!(temperature > 0.f) || !isfinite(temperature)) return BDLM_ERR_INVALID;
-  if (rule < BDLM_COMMIT_THRESHOLD || rule > BDLM_COMMIT_ANTI_SEQUENTIAL) return BDLM_ERR_INVALID;
-  if (rule == BDLM_COMMIT_THRESHOLD && !(threshold >= 0.f && threshold <= 1.f))
-    return BDLM_ERR_INVALID;
-  if (rule != BDLM_COMMIT_THRESHOLD && k < 1) return BDLM_ERR_INVALID;
+  if (!rule_ok(rule, k, threshold)) return BDLM_ERR_INVALID;
   if (B == 0) return BDLM_OK;
   if (!hidden || !w || !mask || !tok_out || !conf_out || !commit_out) return BDLM_ERR_INVALID;
   if (!aligned16(hidden) || !aligned16(w) || (logits && !aligned16(logits)))
@@ -510,10 +518,11 @@ int bdlm_lm_head_commit(const bdlm_bf16* hidden, const bdlm_bf16* w, const uint8
                                              n_act, s);
   if (e == cudaSuccess)
     e = bdlm::launch_lm_conf(tm_w, tm_h, act, n_act, rows, rows, H, V, temperature, logits, part,
-                             plan, st->err, s);
+                             plan, st->err, s,
+                             entropy_out != nullptr || rule == BDLM_COMMIT_ENTROPY_BOUNDED);
   if (e == cudaSuccess)
     e = bdlm::launch_lm_commit_finalize(mask, denoising, B, L, part, plan, temperature, rule, k,
-                                        threshold, tok_out, conf_out, commit_out, s);
+                                        threshold, tok_out, conf_out, entropy_out, commit_out, s);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 
@@ -626,8 +635,8 @@ int capture_round_loop(bdlm_round_loop* lp) {
   if (!r2) r2 = bdlm_block_attention(&a, lp->q_w, d.k_pages, d.v_pages, d.page_table,
                                      d.prefix_lens, a.L, lp->attn_out, s);
   if (!r2) r2 = bdlm_lm_head_commit(lp->h_w, d.w, d.mask, d.denoising, a.B, a.L, d.H, d.V, d.rule,
-                                    d.k, d.threshold, d.temperature, lp->tok, lp->conf, lp->com,
-                                    nullptr, s);
+                                    d.k, d.threshold, d.temperature, lp->tok, lp->conf, nullptr,
+                                    lp->com, nullptr, s);
   if (!r2 && bdlm::launch_record_step(lp->step, d.steps, R, lp->tok, lp->conf, lp->com,
                                       d.tok_steps, d.conf_steps, d.commit_steps,
                                       reinterpret_cast<const uint4*>(lp->attn_out),
@@ -660,9 +669,8 @@ int bdlm_round_loop_create(const bdlm_round_loop_desc* desc, bdlm_round_loop** o
       a.D != 128 || a.page_size != 16 || a.max_pages_per_seq < 1 || a.num_pages < 1)
     return BDLM_ERR_INVALID;
   if (d.steps < 1 || d.H < 8 || d.H % 8 != 0 || d.V < 8 || d.V % 8 != 0) return BDLM_ERR_INVALID;
-  if (d.rule < BDLM_COMMIT_THRESHOLD || d.rule > BDLM_COMMIT_ANTI_SEQUENTIAL) return BDLM_ERR_INVALID;
-  if (d.rule != BDLM_COMMIT_THRESHOLD && d.k < 1) return BDLM_ERR_INVALID;
-  if (!(d.temperature > 0.f) || !(d.threshold >= 0.f && d.threshold <= 1.f)) return BDLM_ERR_INVALID;
+  if (!rule_ok(d.rule, d.k, d.threshold)) return BDLM_ERR_INVALID;
+  if (!(d.temperature > 0.f) || !isfinite(d.temperature)) return BDLM_ERR_INVALID;
   if (!d.q_steps || !d.k_new_steps || !d.v_new_steps || !d.hidden_steps || !d.k_pages ||
       !d.v_pages || !d.page_table || !d.prefix_lens || !d.w || !d.mask || !d.tok_steps ||
       !d.conf_steps || !d.commit_steps || !d.steps_done)

@@ -1,20 +1,23 @@
-// Confidence + commit of one denoising step: one pass over the vocabulary.
+// Confidence + commit of one denoising step: one pass over the vocabulary, in one launch.
 //
-// Source: JetEngine notes (CLAUDE.md), "Remasking Strategies" (low_confidence_dynamic) and
-// "Remaining Optimization Avenues" (a fused postprocess kernel); dInfer blog, "Algorithmic
-// Innovations" (threshold decoding).  Per masked row: argmax token (lowest index on ties),
-// max softmax probability at temperature T; per block: commit every masked position at or
-// above the threshold, else the single most confident one.
+// Source: JetEngine notes (CLAUDE.md), "Remasking Strategies" (low_confidence_dynamic, top-k,
+// sequential orders, entropy_bounded) and "Remaining Optimization Avenues" (a fused
+// postprocess kernel); dInfer blog, "Algorithmic Innovations" (threshold decoding).  Per
+// masked row: argmax token (lowest index on ties), max softmax probability and entropy at
+// temperature T; per block: the commit rule over the block's masked positions.
 //
 // Layout of the work: the masked rows, laid end to end, form one sequence of T = n_masked * V
 // logits that is cut evenly across every warp of a persistent grid (each CTA first counts the
 // mask to learn n_masked and where each masked row sits).  A warp streams its range through a
 // private ring of two 4 KB shared-memory stages filled by bulk copies (one instruction per
-// stage), keeping a running (max, sum of exp, first argmax) per lane, and at the end of each
-// row segment merges its lanes with shuffles into one partial: that is all it writes.  A second
-// kernel, one CTA per block, then merges each masked row's partials in warp order, writes
-// tok/conf and decides the block's commit after a single round of loads: no counters, fences
-// or atomics sit on the streaming warps' path.
+// stage), keeping a running (max, sum of exponentials, first argmax, and for the entropy the
+// exponent-weighted sum) per lane, and at the end of each row segment merges its lanes with
+// shuffles into one partial: that is all it writes.  A second kernel, one CTA per block and
+// launched dependent on the first, merges each masked row's partials (one lane per row), writes
+// tok/conf/entropy and decides the block's commit with one warp: no counters, fences or atomics
+// sit on the streaming warps' path.  (A single-kernel variant in which the warp completing a
+// row or block finalizes it through acquire-release counters was measured slower: the counter
+// round trips lengthened the tail, and same-address arrivals serialised.)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -42,56 +45,74 @@ constexpr int kMaskSmem = 8192;       // masks of up to this many rows are copie
 struct LaneAcc {
   float m;            // running max (raw logit)
   float s;            // sum of 2^((x - m) c)
+  float a;            // sum of 2^((x - m) c) * (x - m) c
   int idx;            // first index of the max, or -1 while it lies in the saved group
   int gbase;          // saved group: vector q covers logits gbase + 256 q .. + 7
   uint32_t gw[16];    // saved group's packed bf16 pairs
 };
 
-__device__ __forceinline__ void lane_reset(LaneAcc& a) {
-  a.m = -CUDART_INF_F;
-  a.s = 0.f;
-  a.idx = 0x7FFFFFFF;
+__device__ __forceinline__ void lane_reset(LaneAcc& x) {
+  x.m = -CUDART_INF_F;
+  x.s = 0.f;
+  x.a = 0.f;
+  x.idx = 0x7FFFFFFF;
 }
 
 // Adds the 32 logits of one group (vector q = words 4q .. 4q+3, starting at logit
 // gbase + 256 q).  A lane sees its logits in increasing index order, so a strictly larger
-// max keeps the first occurrence.
-__device__ __forceinline__ void absorb32(LaneAcc& a, const uint32_t (&w)[16], int gbase, float c) {
+// max keeps the first occurrence.  ENT: also the exponent-weighted sum (for the entropy).
+template <bool ENT>
+__device__ __forceinline__ void absorb32(LaneAcc& x, const uint32_t (&w)[16], int gbase, float c) {
   const float gm = group_max(w);
-  if (gm > a.m) {
-    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - gm) * c);
-    a.m = gm;
-    a.idx = -1;
-    a.gbase = gbase;
+  if (gm > x.m) {
+    if (x.m == -CUDART_INF_F) {
+      x.s = 0.f;
+      x.a = 0.f;
+    } else {
+      acc_rebase(x.s, x.a, x.m, gm, c);
+    }
+    x.m = gm;
+    x.idx = -1;
+    x.gbase = gbase;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) a.gw[i] = w[i];
+    for (int i = 0; i < 16; ++i) x.gw[i] = w[i];
   }
-  if (a.m == -CUDART_INF_F) return;  // nothing but padding so far
-  a.s += exp_sum32(w, c, a.m * c);
+  if (x.m == -CUDART_INF_F) return;  // nothing but padding so far
+  exp_sum32<ENT>(w, c, x.m * c, x.s, x.a);
 }
 
-// Adds one logit x with index i.
-__device__ __forceinline__ void absorb1(LaneAcc& a, float x, int i, float c) {
-  if (x > a.m) {
-    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - x) * c);
-    a.m = x;
-    a.idx = i;
+// Adds one logit v with index i.
+template <bool ENT>
+__device__ __forceinline__ void absorb1(LaneAcc& x, float v, int i, float c) {
+  if (v > x.m) {
+    if (x.m == -CUDART_INF_F) {
+      x.s = 0.f;
+      x.a = 0.f;
+    } else {
+      acc_rebase(x.s, x.a, x.m, v, c);
+    }
+    x.m = v;
+    x.idx = i;
   }
-  a.s += ex2(fmaf(x, c, -a.m * c));
+  if (x.m == -CUDART_INF_F) return;
+  const float y = fmaf(v, c, -x.m * c);
+  const float e = ex2(y);
+  x.s += e;
+  if constexpr (ENT) x.a = fmaf(e, y, x.a);
 }
 
-// The lane's (max, sum, first index of the max) with the saved group's position resolved.
-__device__ __forceinline__ Acc lane_result(const LaneAcc& a) {
-  int idx = a.idx;
+// The lane's state with the saved group's position resolved.
+__device__ __forceinline__ Acc lane_result(const LaneAcc& x) {
+  int idx = x.idx;
   if (idx < 0) {
     idx = 0x7FFFFFFF;
 #pragma unroll
     for (int e = 31; e >= 0; --e) {
-      const float x = (e & 1) ? bf16_hi(a.gw[e >> 1]) : bf16_lo(a.gw[e >> 1]);
-      if (x == a.m) idx = a.gbase + (e >> 3) * 256 + (e & 7);
+      const float v = (e & 1) ? bf16_hi(x.gw[e >> 1]) : bf16_lo(x.gw[e >> 1]);
+      if (v == x.m) idx = x.gbase + (e >> 3) * 256 + (e & 7);
     }
   }
-  return Acc{a.m, a.s, idx};
+  return Acc{x.m, x.s, x.a, idx};
 }
 
 struct ChunkMeta {
@@ -110,10 +131,11 @@ struct CommitArgs {
   float threshold, c;
   int32_t* tok_out;
   float* conf_out;
+  float* ent_out;      // may be null
   uint8_t* commit_out;
-  CommitPartial* part;
-  int* err;  // device error word (may be null)
-  int rule, k;  // block decision: BDLM_COMMIT_* and positions per block
+  CommitPartial* part; // one per (warp, masked row segment): slot w + k
+  int* err;            // device error word (may be null)
+  int rule, k;         // block decision: BDLM_COMMIT_* and positions per block
 };
 
 // First logit (in the masked concatenation) of warp w out of W; a multiple of 8.
@@ -131,8 +153,27 @@ __device__ __forceinline__ int warp_of(long long e, long long T, int W) {
   return w;
 }
 
+__device__ __forceinline__ uint8_t mask_at(const CommitArgs& a, const uint8_t* s_mask, int r) {
+  return s_mask ? s_mask[r] : a.mask[r];
+}
+
+// Outputs of the positions of block b that are not candidates, and its commit mask.
+__device__ __forceinline__ void write_block(const CommitArgs& a, int b, uint64_t cand,
+                                            uint64_t sel, int lane) {
+  for (int i = lane; i < a.L; i += 32) {
+    const size_t r = static_cast<size_t>(b) * a.L + i;
+    a.commit_out[r] = static_cast<uint8_t>((sel >> i) & 1);
+    if (!((cand >> i) & 1)) {
+      a.tok_out[r] = -1;
+      a.conf_out[r] = -CUDART_INF_F;
+      if (a.ent_out) a.ent_out[r] = CUDART_INF_F;
+    }
+  }
+}
+
 // Streams warp w's range [e0, e1) of the masked concatenation (T logits, W warps) through
-// the warp's ring and finalizes the rows whose element count it completes.
+// the warp's ring; at the end of each row segment it stores the warp's partial.
+template <bool ENT>
 __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, int W, int w,
                                           long long e0, long long e1, int per,
                                           const int* s_pref, const uint8_t* s_mask,
@@ -148,7 +189,7 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
     int left = static_cast<int>(k - s_pref[lo]);
     int r = min(a.R, lo * per);
     for (;; ++r)
-      if ((s_mask ? s_mask[r] : a.mask[r]) && left-- == 0) break;
+      if (mask_at(a, s_mask, r) && left-- == 0) break;
     return r;
   };
 
@@ -221,7 +262,7 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
     const int nvec = (m.i1 - m.i0) >> 3;
     // logits before the aligned interior (at most 7) come first: each lane then sees its
     // logits in increasing index order
-    if (m.g0 + lane < m.i0) absorb1(acc, bf16f(row[m.g0 + lane]), m.g0 + lane, a.c);
+    if (m.g0 + lane < m.i0) absorb1<ENT>(acc, bf16f(row[m.g0 + lane]), m.g0 + lane, a.c);
     if (nvec == kChunk / 8) {
       // a full stage: no bounds checks
 #pragma unroll
@@ -235,7 +276,7 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
           wv[4 * q + 2] = t.z;
           wv[4 * q + 3] = t.w;
         }
-        absorb32(acc, wv, m.i0 + (v0 + lane) * 8, a.c);
+        absorb32<ENT>(acc, wv, m.i0 + (v0 + lane) * 8, a.c);
       }
     } else {
       for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
@@ -251,11 +292,11 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
           wv[4 * q + 2] = t.z;
           wv[4 * q + 3] = t.w;
         }
-        absorb32(acc, wv, m.i0 + (v0 + lane) * 8, a.c);
+        absorb32<ENT>(acc, wv, m.i0 + (v0 + lane) * 8, a.c);
       }
     }
     // logits after the aligned interior (at most 7)
-    if (m.i1 + lane < m.g1) absorb1(acc, bf16f(row[m.i1 + lane]), m.i1 + lane, a.c);
+    if (m.i1 + lane < m.g1) absorb1<ENT>(acc, bf16f(row[m.i1 + lane]), m.i1 + lane, a.c);
     __syncwarp();
     if (lane == 0 && issue(slot)) ++issued;  // refill the stage just read
     issued = __shfl_sync(0xffffffffu, issued, 0);
@@ -264,7 +305,7 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
     // ordered and contiguous, so the slots are distinct)
     Acc t = warp_merge(lane_result(acc), a.c);
     lane_reset(acc);
-    if (lane == 0) a.part[w + m.k] = CommitPartial{t.m, t.s, t.idx, 0};
+    if (lane == 0) a.part[w + m.k] = CommitPartial{t.m, t.s, t.idx, t.a};
   }
   // drain: nothing may still be landing in this warp's stages when it exits
   if (lane == 0) {
@@ -275,6 +316,8 @@ __device__ __forceinline__ void stream_range(const CommitArgs& a, long long T, i
   }
 }
 
+// ENT: the entropies are wanted (an entropy output or the entropy rule).
+template <bool ENT>
 __global__ void __launch_bounds__(kThreads, 1)
 commit_kernel(const CommitArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -315,6 +358,7 @@ commit_kernel(const CommitArgs a) {
   if (tid == kThreads - 1) s_pref[kThreads] = wbase + incl;
   __syncthreads();
   const long long n_masked = s_pref[kThreads];
+  const uint8_t* smask = mask_in_smem ? s_mask : nullptr;
 
   // ---- this warp's range of the masked concatenation
   const long long T = n_masked * a.V;
@@ -324,24 +368,25 @@ commit_kernel(const CommitArgs a) {
   const long long e0 = range_start(T, W, w);
   const long long e1 = range_start(T, W, w + 1);
   if (w < W && T > 0 && e0 < e1)
-    stream_range(a, T, W, w, e0, e1, per, s_pref, mask_in_smem ? s_mask : nullptr,
+    stream_range<ENT>(a, T, W, w, e0, e1, per, s_pref, smask,
                  ring_base + warp * (kRing * kChunkBytes), s_bar[warp], s_meta[warp], lane);
-
 }
 
-// One CTA per block b, min(L, 32) warps: the masked index of each row (from the mask, an input
-// that is complete before the streaming kernel lets this one start), then, once the streaming
-// kernel has finished, one warp per row merges the row's partials in warp order; thread 0
-// decides the block: every masked position with conf >= threshold, else the single most
-// confident one (lowest position on ties).  Unmasked rows get tok = -1, conf = -inf.
+// One CTA of min(L, 32) warps per block b.  Before the streaming kernel is done: the masked
+// rows before block b and in all (from the mask, which is complete before the streaming kernel
+// starts), hence every warp's range.  Then warp x merges the partials of the block's masked rows
+// x, x + warps, ...: lane j loads partial j (the row's warps in order), a shuffle tree merges
+// them (lowest index on max ties), and lane 0 writes tok / conf / entropy; warp 0 then decides
+// the block's commit.  Positions that are not masked get tok = -1, conf = -inf, entropy = +inf,
+// commit = 0.
 __global__ void __launch_bounds__(1024)
 commit_finalize_kernel(const CommitArgs a, int stream_grid) {
-  __shared__ int s_wsum[32];
-  __shared__ int s_blk_before, s_total;
-  __shared__ float s_conf[64];
+  __shared__ int s_wsum[2][32];
+  __shared__ int s_before, s_total;
+  __shared__ float s_stat[64];
+  __shared__ int s_order[64];
   const int b = blockIdx.x, L = a.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-  // masked rows before this block, and in all
   int before = 0, total = 0;
   for (int r = tid; r < a.R; r += blockDim.x) {
     const int mk = a.mask[r] != 0;
@@ -353,67 +398,62 @@ commit_finalize_kernel(const CommitArgs a, int stream_grid) {
     before += __shfl_xor_sync(0xffffffffu, before, off);
     total += __shfl_xor_sync(0xffffffffu, total, off);
   }
-  if (lane == 0) s_wsum[warp] = before;
-  __syncthreads();
-  if (tid == 0) {
-    int sb = 0;
-    for (int i = 0; i < nw; ++i) sb += s_wsum[i];
-    s_blk_before = sb;
+  if (lane == 0) {
+    s_wsum[0][warp] = before;
+    s_wsum[1][warp] = total;
   }
   __syncthreads();
-  if (lane == 0) s_wsum[warp] = total;
-  __syncthreads();
   if (tid == 0) {
-    int st = 0;
-    for (int i = 0; i < nw; ++i) st += s_wsum[i];
+    int sb = 0, st = 0;
+    for (int i = 0; i < nw; ++i) {
+      sb += s_wsum[0][i];
+      st += s_wsum[1][i];
+    }
+    s_before = sb;
     s_total = st;
   }
   __syncthreads();
   const long long T = static_cast<long long>(s_total) * a.V;
   const long long Wcap = static_cast<long long>(stream_grid) * kWarps;
   const int W = static_cast<int>(max(1ll, min(Wcap, T / kChunk)));
+  const uint8_t* mk = a.mask + static_cast<size_t>(b) * L;
+  const uint64_t cand =
+      (static_cast<uint64_t>(__ballot_sync(0xffffffffu, lane + 32 < L && mk[lane + 32] != 0))
+       << 32) |
+      __ballot_sync(0xffffffffu, lane < L && mk[lane] != 0);
   griddep_wait();  // the streaming kernel's partials are complete and visible
   griddep_launch_dependents();
-  const uint8_t* mk = a.mask + static_cast<size_t>(b) * L;
+  const bool ent_rule = a.rule == BDLM_COMMIT_ENTROPY_BOUNDED;
   for (int i = warp; i < L; i += nw) {
-    const int r = b * L + i;
-    if (!mk[i]) {
-      if (lane == 0) {
-        a.tok_out[r] = -1;
-        a.conf_out[r] = -CUDART_INF_F;
-        s_conf[i] = -CUDART_INF_F;
-      }
-      continue;
-    }
-    int k = s_blk_before;
-    for (int j = 0; j < i; ++j) k += mk[j] != 0;
+    if (!((cand >> i) & 1)) continue;
+    const int k = s_before + __popcll(cand & ((1ull << i) - 1ull));
     const long long kv = static_cast<long long>(k) * a.V;
     const int first_w = warp_of(kv, T, W);
     const int n_w = warp_of(min(kv + a.V, T) - 1, T, W) - first_w + 1;
     const CommitPartial* pr = a.part + first_w + k;
-    Acc f{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    Acc f = acc_init();
     for (int j0 = 0; j0 < n_w; j0 += 32) {
-      Acc q{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+      Acc q = acc_init();
       if (j0 + lane < n_w) {
-        const CommitPartial c = pr[j0 + lane];
-        q = Acc{c.m, c.s, c.idx};
+        const CommitPartial t = pr[j0 + lane];
+        q = Acc{t.m, t.s, t.a, t.idx};
       }
       f = merge(f, warp_merge(q, a.c), a.c);
     }
     if (lane == 0) {
-      const float conf = 1.0f / f.s;
+      const size_t r = static_cast<size_t>(b) * L + i;
+      const float conf = acc_conf(f), ent = acc_entropy(f);
       a.tok_out[r] = f.idx;
       a.conf_out[r] = conf;
-      s_conf[i] = conf;
+      if (a.ent_out) a.ent_out[r] = ent;
+      s_stat[i] = ent_rule ? ent : conf;
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    uint64_t cand = 0;
-    for (int i = 0; i < L; ++i) cand |= static_cast<uint64_t>(mk[i] != 0) << i;
-    const uint64_t sel = decide_block(a.rule, a.k, a.threshold, L, cand, s_conf);
-    uint8_t* co = a.commit_out + static_cast<size_t>(b) * L;
-    for (int i = 0; i < L; ++i) co[i] = static_cast<uint8_t>((sel >> i) & 1);
+  if (warp == 0) {
+    const uint64_t sel = decide_block_warp(a.rule, a.k, a.threshold, L, cand, s_stat, s_order,
+                                           lane);
+    write_block(a, b, cand, sel, lane);
   }
 }
 
@@ -435,19 +475,22 @@ CommitPlan plan_commit(int B, int L, int V, int num_sms) {
   p.smem_bytes = static_cast<size_t>(kWarps) * kRing * kChunkBytes + 128;
   // one partial per (warp, masked row segment): slots w + k < warps + rows
   p.part_bytes = static_cast<size_t>(p.grid * kWarps + rows) * sizeof(CommitPartial);
-  p.fin_threads = (L < 32 ? L : 32) * 32;
+  (void)B;
   (void)V;
   return p;
 }
 
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
-                          uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* err, cudaStream_t stream, bool programmatic, int rule, int k) {
+                          float* ent_out, uint8_t* commit_out, const CommitPlan& plan,
+                          CommitPartial* part, int* err, cudaStream_t stream, int rule, int k) {
   static std::atomic<unsigned long long> attr_done{0};
   const int smem_bytes = static_cast<int>(plan.smem_bytes);  // the same for every plan
   cudaError_t ea = once_per_device(attr_done, [smem_bytes] {
-    return cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t r = cudaFuncSetAttribute(commit_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(commit_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem_bytes);
   });
   if (ea != cudaSuccess) return ea;
@@ -461,21 +504,20 @@ cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, in
   args.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   args.tok_out = tok_out;
   args.conf_out = conf_out;
+  args.ent_out = ent_out;
   args.commit_out = commit_out;
   args.part = part;
   args.err = err;
   args.rule = rule;
   args.k = k;
-  cudaError_t e;
-  if (!programmatic) {
-    commit_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(args);
-    e = cudaGetLastError();
-  } else {
-    e = launch_pdl(commit_kernel, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream, args);
-  }
+  const bool ent = ent_out != nullptr || rule == BDLM_COMMIT_ENTROPY_BOUNDED;
+  cudaError_t e = ent ? launch_pdl(commit_kernel<true>, dim3(plan.grid), dim3(kThreads),
+                                   plan.smem_bytes, stream, args)
+                      : launch_pdl(commit_kernel<false>, dim3(plan.grid), dim3(kThreads),
+                                   plan.smem_bytes, stream, args);
   if (e != cudaSuccess) return e;
-  return launch_pdl(commit_finalize_kernel, dim3(B), dim3(plan.fin_threads), 0, stream, args,
-                    plan.grid);
+  return launch_pdl(commit_finalize_kernel, dim3(B), dim3((L < 32 ? L : 32) * 32), 0, stream,
+                    args, plan.grid);
 }
 
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream) {

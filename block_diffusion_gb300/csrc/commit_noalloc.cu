@@ -4,8 +4,8 @@
 // GPU's memory up front for its own pools (model weights, the paged KV cache) and hands
 // out nothing else, or a latency-critical decode loop where an allocation's implicit device
 // synchronisation is not acceptable.  This entry point runs the same kernel as
-// bdlm_confidence_commit, but its scratch (per-warp partial results and an error word) lives in a
-// fixed file-scope device array that is part of the loaded module, so no call allocates or
+// bdlm_confidence_commit, but its scratch (per-warp partial results and an error word) lives
+// in a fixed file-scope device array that is part of the loaded module, so no call allocates or
 // frees anything.
 //
 // Limits and behaviour (also stated in include/bdlm.h):
@@ -17,8 +17,8 @@
 //    with that device current; make that first call before any stream capture.
 //  * Every call shares the one array: calls that overlap on the GPU (different streams, or
 //    different host threads without ordering) race and give wrong results.
-//  * A device error of these kernels (a bounded wait that gave up) is recorded in the error
-//    word at the head of the array.  bdlm_device_error() reads and clears it together with the
+//  * A device error of the kernel (a bounded wait that gave up) is recorded in the error word
+//    at the head of the array.  bdlm_device_error() reads and clears it together with the
 //    workspace's word, and allocates nothing either; the calls never clear it themselves, so a
 //    recorded error stays until it is read.
 #include <cuda_runtime.h>
@@ -110,10 +110,10 @@ extern "C" int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uin
   const bdlm::CommitPlan plan = bdlm::plan_commit(B, L, V, sms);
   if (plan.part_bytes > kPartialBytes) return BDLM_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int* err = static_cast<int*>(base);
-  auto* part = reinterpret_cast<bdlm::CommitPartial*>(static_cast<unsigned char*>(base) +
-                                                      kCounterBytes);
+  unsigned char* p = static_cast<unsigned char*>(base);
+  int* err = reinterpret_cast<int*>(p);
+  auto* part = reinterpret_cast<bdlm::CommitPartial*>(p + kCounterBytes);
   cudaError_t e = bdlm::launch_commit(logits, mask, B, L, V, threshold, temperature, tok_out,
-                                      conf_out, commit_out, plan, part, err, s);
+                                      conf_out, nullptr, commit_out, plan, part, err, s);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }

@@ -48,26 +48,28 @@ cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& set) {
 }
 
 // ------------------------------------------------------------------ commit
+// A partial row state: (max, sum of exponentials, first argmax, exponent-weighted sum); see
+// confidence.cuh.
 struct CommitPartial {
   float m;
   float s;
   int idx;
-  int pad;
+  float a;
 };
 
 struct CommitPlan {
   long long total_items = 0;  // rows
-  int grid = 1;               // streaming CTAs (one per SM, persistent)
-  int fin_threads = 32;       // threads of a finalizing CTA (one CTA per block)
+  int grid = 1;               // CTAs (one per SM, persistent)
   size_t smem_bytes = 0;
-  size_t part_bytes = 0;      // one partial per (streaming warp, masked row segment)
+  size_t part_bytes = 0;      // one partial per (warp, masked row segment)
 };
 
 CommitPlan plan_commit(int B, int L, int V, int num_sms);
+// The streaming kernel and the per-block finalize kernel; ent_out may be null.
 cudaError_t launch_commit(const uint16_t* logits, const uint8_t* mask, int B, int L, int V,
                           float threshold, float temperature, int32_t* tok_out, float* conf_out,
-                          uint8_t* commit_out, const CommitPlan& plan, CommitPartial* part,
-                          int* err, cudaStream_t stream, bool programmatic = true,
+                          float* ent_out, uint8_t* commit_out, const CommitPlan& plan,
+                          CommitPartial* part, int* err, cudaStream_t stream,
                           int rule = BDLM_COMMIT_THRESHOLD, int k = 1);
 cudaError_t launch_apply_commit(uint8_t* mask, const uint8_t* commit, int n, cudaStream_t stream);
 // The error word of bdlm_confidence_commit_noalloc's fixed array on device `dev`, read and
@@ -124,7 +126,8 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            cudaStream_t stream);
 
 // LM head fused with the confidence step: partials of (max, sum of exponentials, first
-// argmax) per (active row, slot); a per-block kernel merges them and decides the commit.
+// argmax, and with `ent` the exponent-weighted sum the entropy needs) per (active row, slot); a
+// per-block kernel merges them and decides the commit.
 struct LmConfPlan {
   int grid = 0;            // persistent CTAs (one per SM)
   int units = 0;           // workers: CTA pairs of the pair kernel, else CTAs
@@ -142,7 +145,7 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            const int32_t* active_idx, const int32_t* n_active_dev, int max_rows,
                            int n_rows, int H, int V, float temperature, uint16_t* logits,
                            CommitPartial* part, const LmConfPlan& plan, int* err,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool ent = false);
 // The scored rows (masked, in a denoising sequence) listed in act / *n_act and their hidden
 // rows gathered, in one launch of B * L CTAs.
 cudaError_t launch_scored_gather(const uint16_t* hidden, const uint8_t* mask,
@@ -154,8 +157,8 @@ cudaError_t launch_scored_gather(const uint16_t* hidden, const uint8_t* mask,
 cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denoising, int B, int L,
                                       const CommitPartial* part, const LmConfPlan& plan,
                                       float temperature, int rule, int k, float threshold,
-                                      int32_t* tok_out, float* conf_out, uint8_t* commit_out,
-                                      cudaStream_t stream);
+                                      int32_t* tok_out, float* conf_out, float* ent_out,
+                                      uint8_t* commit_out, cudaStream_t stream);
 
 // Prompt chunk j of sequence b -> attention sequence b * nb + j with prefix prefix[b] + j * L.
 cudaError_t launch_prompt_prefix(const int32_t* prefix_lens, int B, int nb, int L, int32_t* out,

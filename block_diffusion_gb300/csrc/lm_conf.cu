@@ -84,11 +84,18 @@ __device__ bool produce_jobs(const CUtensorMap* tm, uint8_t* ring, uint64_t* ful
 }
 
 // Folds 32 logits (16 packed bf16 pairs, indices base .. base + 31 in order) into a row's
-// running state; a strictly larger group max moves the max and its first index.
+// running state; a strictly larger group max moves the max and its first index.  ENT: also the
+// exponent-weighted sum (for the entropy).
+template <bool ENT>
 __device__ __forceinline__ void fold32(Acc& a, const uint32_t (&w)[16], int base, float c) {
   const float gm = group_max(w);
   if (gm > a.m) {
-    a.s = (a.m == -CUDART_INF_F) ? 0.f : a.s * ex2((a.m - gm) * c);
+    if (a.m == -CUDART_INF_F) {
+      a.s = 0.f;
+      a.a = 0.f;
+    } else {
+      acc_rebase(a.s, a.a, a.m, gm, c);
+    }
     a.m = gm;
     int first = 0x7FFFFFFF;
 #pragma unroll
@@ -99,9 +106,10 @@ __device__ __forceinline__ void fold32(Acc& a, const uint32_t (&w)[16], int base
     a.idx = first;
   }
   if (a.m == -CUDART_INF_F) return;  // nothing but padding so far
-  a.s += exp_sum32(w, c, a.m * c);
+  exp_sum32<ENT>(w, c, a.m * c, a.s, a.a);
 }
 
+template <bool ENT>
 __global__ void __launch_bounds__(kThreads, 1)
 lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
                const LmConfParams p) {
@@ -214,7 +222,7 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         lrow[s] = (r >= 0 && r < p.n_rows) ? r : -1;   // a bad id is flagged by the gather
       }
       if (!valid) arow[s] = -1;
-      acc[s] = Acc{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+      acc[s] = acc_init();
     }
     bool ok = true;
     for (int j = 0; j < n_jobs; ++j) {
@@ -265,8 +273,8 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
               dst[q] = make_uint4(wv[q >> 2][(q & 3) * 4], wv[q >> 2][(q & 3) * 4 + 1],
                                   wv[q >> 2][(q & 3) * 4 + 2], wv[q >> 2][(q & 3) * 4 + 3]);
         }
-        fold32(acc[s], wv[0], vbase, p.c);
-        fold32(acc[s], wv[1], vbase + 32, p.c);
+        fold32<ENT>(acc[s], wv[0], vbase, p.c);
+        fold32<ENT>(acc[s], wv[1], vbase + 32, p.c);
       }
       tc_fence_before();
       mbar_arrive(&acc_empty);   // tensor memory is free for the next tile's MMAs
@@ -274,12 +282,14 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     // the four shares of each row, merged in the (now idle) W ring: [share][sub-tile][row]
     float* sh_m = reinterpret_cast<float*>(wring);
     float* sh_s = sh_m + kConfShares * kSub * kBM;
-    int* sh_i = reinterpret_cast<int*>(sh_s + kConfShares * kSub * kBM);
+    float* sh_a = sh_s + kConfShares * kSub * kBM;
+    int* sh_i = reinterpret_cast<int*>(sh_a + kConfShares * kSub * kBM);
 #pragma unroll
     for (int s = 0; s < kSub; ++s) {
       const int at = (share * kSub + s) * kBM + x;
       sh_m[at] = acc[s].m;
       sh_s[at] = acc[s].s;
+      sh_a[at] = acc[s].a;
       sh_i[at] = acc[s].idx;
     }
     named_barrier(1, kEpiThreads);
@@ -291,9 +301,9 @@ lm_conf_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         Acc t = acc[s];
         for (int o = 1; o < kConfShares; ++o) {
           const int at = (o * kSub + s) * kBM + x;
-          t = merge(t, Acc{sh_m[at], sh_s[at], sh_i[at]}, p.c);
+          t = merge(t, Acc{sh_m[at], sh_s[at], sh_a[at], sh_i[at]}, p.c);
         }
-        p.part[static_cast<size_t>(arow[s]) * p.slots + slot] = CommitPartial{t.m, t.s, t.idx, 0};
+        p.part[static_cast<size_t>(arow[s]) * p.slots + slot] = CommitPartial{t.m, t.s, t.idx, t.a};
       }
     }
   }
@@ -395,6 +405,7 @@ __device__ void produce_pair(const CUtensorMap* tm, uint8_t* ring, uint64_t* ful
   }
 }
 
+template <bool ENT>
 __global__ void __launch_bounds__(kThreads, 1)
 lm_conf_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_h, const LmConfParams p) {
@@ -518,7 +529,7 @@ lm_conf_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
       lrow = (r >= 0 && r < p.n_rows) ? r : -1;   // a bad id is flagged by the gather
     }
     if (!valid) arow = -1;
-    Acc acc{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    Acc acc = acc_init();
     bool ok = true;
     for (int j = 0; j < n_jobs; ++j) {
       const int buf = j & 1;
@@ -568,23 +579,26 @@ lm_conf_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
             dst[q] = make_uint4(wv[q >> 2][(q & 3) * 4], wv[q >> 2][(q & 3) * 4 + 1],
                                 wv[q >> 2][(q & 3) * 4 + 2], wv[q >> 2][(q & 3) * 4 + 3]);
       }
-      fold32(acc, wv[0], vbase, p.c);
-      fold32(acc, wv[1], vbase + 32, p.c);
+      fold32<ENT>(acc, wv[0], vbase, p.c);
+      fold32<ENT>(acc, wv[1], vbase + 32, p.c);
     }
     // the four shares of each row, merged in the (now idle) W ring: [share][row]
     float* sh_m = reinterpret_cast<float*>(wring);
     float* sh_s = sh_m + kConfShares * kBM;
-    int* sh_i = reinterpret_cast<int*>(sh_s + kConfShares * kBM);
+    float* sh_a = sh_s + kConfShares * kBM;
+    int* sh_i = reinterpret_cast<int*>(sh_a + kConfShares * kBM);
     sh_m[share * kBM + x] = acc.m;
     sh_s[share * kBM + x] = acc.s;
+    sh_a[share * kBM + x] = acc.a;
     sh_i[share * kBM + x] = acc.idx;
     named_barrier(1, kEpiThreads);
     if (share == 0 && arow >= 0) {
       Acc t = acc;
       for (int o = 1; o < kConfShares; ++o)
-        t = merge(t, Acc{sh_m[o * kBM + x], sh_s[o * kBM + x], sh_i[o * kBM + x]}, p.c);
+        t = merge(t, Acc{sh_m[o * kBM + x], sh_s[o * kBM + x], sh_a[o * kBM + x],
+                         sh_i[o * kBM + x]}, p.c);
       p.part[static_cast<size_t>(arow) * p.slots + slot] =
-          CommitPartial{t.m, t.s, t.idx, 0};
+          CommitPartial{t.m, t.s, t.idx, t.a};
     }
   }
 
@@ -665,6 +679,7 @@ struct LmCommitArgs {
   int rule, k;
   int32_t* tok_out;
   float* conf_out;
+  float* ent_out;            // may be null
   uint8_t* commit_out;
 };
 
@@ -678,14 +693,15 @@ __device__ __forceinline__ int scored(const LmCommitArgs& a, int r) {
 // order, as the active-row list of the LM head numbers them; with rt = ceil(scored / 256) row
 // tiles, the LM head ran lm_grid / rt workers (CTAs, or CTA pairs) per row tile and each wrote
 // `shares` partials per row.
-// Up to 32 rows at a time, 32 / rows warps per row merge a row's partials; then thread 0
+// Up to 32 rows at a time, 32 / rows warps per row merge a row's partials; then warp 0
 // decides the block over its scored positions.
 __global__ void __launch_bounds__(kFinThreads)
 lm_commit_finalize_kernel(const LmCommitArgs a) {
   __shared__ int s_wsum[2][kFinThreads / 32];
   __shared__ int s_before, s_total;
   __shared__ Acc s_acc[kFinThreads / 32];
-  __shared__ float s_conf[64];
+  __shared__ float s_stat[64];
+  __shared__ int s_order[64];
   const int b = blockIdx.x, L = a.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int before = 0, total = 0;
@@ -724,13 +740,13 @@ lm_commit_finalize_kernel(const LmCommitArgs a) {
     const int nr = min(32, L - i0);
     const int wpr = 32 / nr;   // warps per row
     const int i = i0 + warp / wpr;
-    Acc q{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+    Acc q = acc_init();
     if (warp < nr * wpr && ((cand >> i) & 1)) {
       const int ai = s_before + __popcll(cand & ((1ull << i) - 1ull));
       const CommitPartial* pr = a.part + static_cast<size_t>(ai) * a.slots;
       for (int j = (warp % wpr) * 32 + lane; j < n_slots; j += wpr * 32) {
         const CommitPartial t = pr[j];
-        q = merge(q, Acc{t.m, t.s, t.idx}, a.c);
+        q = merge(q, Acc{t.m, t.s, t.a, t.idx}, a.c);
       }
       q = warp_merge(q, a.c);
     }
@@ -739,24 +755,27 @@ lm_commit_finalize_kernel(const LmCommitArgs a) {
     if (tid < nr) {
       const int ii = i0 + tid;
       const int r = b * L + ii;
-      float conf = -CUDART_INF_F;
+      float conf = -CUDART_INF_F, ent = CUDART_INF_F;
       int tok = -1;
       if ((cand >> ii) & 1) {
-        Acc f{-CUDART_INF_F, 0.f, 0x7FFFFFFF};
+        Acc f = acc_init();
         for (int w = tid * wpr; w < (tid + 1) * wpr; ++w) f = merge(f, s_acc[w], a.c);
-        conf = 1.0f / f.s;
+        conf = acc_conf(f);
+        ent = acc_entropy(f);
         tok = f.idx;
       }
       a.tok_out[r] = tok;
       a.conf_out[r] = conf;
-      s_conf[ii] = conf;
+      if (a.ent_out) a.ent_out[r] = ent;
+      s_stat[ii] = a.rule == BDLM_COMMIT_ENTROPY_BOUNDED ? ent : conf;
     }
     __syncthreads();
   }
-  if (tid == 0) {
-    const uint64_t sel = decide_block(a.rule, a.k, a.threshold, L, cand, s_conf);
+  if (warp == 0) {
+    const uint64_t sel = decide_block_warp(a.rule, a.k, a.threshold, L, cand, s_stat, s_order,
+                                           lane);
     uint8_t* co = a.commit_out + static_cast<size_t>(b) * L;
-    for (int i = 0; i < L; ++i) co[i] = static_cast<uint8_t>((sel >> i) & 1);
+    for (int i = lane; i < L; i += 32) co[i] = static_cast<uint8_t>((sel >> i) & 1);
   }
 }
 
@@ -775,7 +794,11 @@ int pair_capacity() {
   if (!known[dev]) {
     int n = 0;
     const size_t smem = lm_conf_pair_smem();
-    if (cudaFuncSetAttribute(lm_conf_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(lm_conf_pair_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) == cudaSuccess &&
+        cudaFuncSetAttribute(lm_conf_pair_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2);
@@ -788,7 +811,8 @@ int pair_capacity() {
       at[0].val.clusterDim.z = 1;
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, lm_conf_pair_kernel, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, lm_conf_pair_kernel<false>, &cfg) != cudaSuccess)
+        n = 0;
     }
     cudaGetLastError();   // a failed query leaves no sticky error: the single-CTA kernel runs
     cap[dev] = n;
@@ -825,10 +849,14 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
                            const int32_t* active_idx, const int32_t* n_active_dev, int max_rows,
                            int n_rows, int H, int V, float temperature, uint16_t* logits,
                            CommitPartial* part, const LmConfPlan& plan, int* err,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool ent) {
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t ea = once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(lm_conf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t r = cudaFuncSetAttribute(lm_conf_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(lm_conf_smem()));
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(lm_conf_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(lm_conf_smem()));
   });
   if (ea != cudaSuccess) return ea;
@@ -861,10 +889,13 @@ cudaError_t launch_lm_conf(const CUtensorMap& tm_w, const CUtensorMap& tm_h,
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, lm_conf_pair_kernel, tm_w, tm_h, prm);
+    return ent ? cudaLaunchKernelEx(&cfg, lm_conf_pair_kernel<true>, tm_w, tm_h, prm)
+               : cudaLaunchKernelEx(&cfg, lm_conf_pair_kernel<false>, tm_w, tm_h, prm);
   }
-  return launch_pdl(lm_conf_kernel, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream,
-                    tm_w, tm_h, prm);
+  return ent ? launch_pdl(lm_conf_kernel<true>, dim3(plan.grid), dim3(kThreads), plan.smem_bytes,
+                          stream, tm_w, tm_h, prm)
+             : launch_pdl(lm_conf_kernel<false>, dim3(plan.grid), dim3(kThreads),
+                          plan.smem_bytes, stream, tm_w, tm_h, prm);
 }
 
 cudaError_t launch_scored_gather(const uint16_t* hidden, const uint8_t* mask,
@@ -878,8 +909,8 @@ cudaError_t launch_scored_gather(const uint16_t* hidden, const uint8_t* mask,
 cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denoising, int B, int L,
                                       const CommitPartial* part, const LmConfPlan& plan,
                                       float temperature, int rule, int k, float threshold,
-                                      int32_t* tok_out, float* conf_out, uint8_t* commit_out,
-                                      cudaStream_t stream) {
+                                      int32_t* tok_out, float* conf_out, float* ent_out,
+                                      uint8_t* commit_out, cudaStream_t stream) {
   LmCommitArgs a;
   a.mask = mask;
   a.den = denoising;
@@ -895,6 +926,7 @@ cudaError_t launch_lm_commit_finalize(const uint8_t* mask, const uint8_t* denois
   a.k = k;
   a.tok_out = tok_out;
   a.conf_out = conf_out;
+  a.ent_out = ent_out;
   a.commit_out = commit_out;
   return launch_pdl(lm_commit_finalize_kernel, dim3(B), dim3(kFinThreads), 0, stream, a);
 }

@@ -212,29 +212,40 @@ enum {
   BDLM_COMMIT_THRESHOLD = 0,       /* low_confidence_dynamic: as bdlm_confidence_commit */
   BDLM_COMMIT_TOPK = 1,            /* low_confidence_static: the k most confident */
   BDLM_COMMIT_SEQUENTIAL = 2,      /* the k leftmost masked positions */
-  BDLM_COMMIT_ANTI_SEQUENTIAL = 3  /* the k rightmost masked positions */
+  BDLM_COMMIT_ANTI_SEQUENTIAL = 3, /* the k rightmost masked positions */
+  BDLM_COMMIT_ENTROPY_BOUNDED = 4  /* lowest entropies first, within an entropy budget */
 };
 
 /*
- * Confidence and commit with a selectable rule.
+ * Confidence, entropy and commit with a selectable rule.
  * Source: JetEngine notes, "Remasking Strategies" (sequential: unmask left to right;
  * low_confidence_static: unmask the top-k by confidence; low_confidence_dynamic: unmask above
- * a threshold; anti_sequential is named beside sequential in the notes' scheduler tree).
+ * a threshold; entropy_bounded: unmask by a cumulative entropy budget; anti_sequential is named
+ * beside sequential in the notes' scheduler tree) and "Key Config Parameters" (eb_threshold).
  *
- * tok_out and conf_out are those of bdlm_confidence_commit for every rule.  Per block:
+ * tok_out and conf_out are those of bdlm_confidence_commit for every rule.  entropy_out [B, L]
+ * float (device, or NULL when not wanted) receives, for every masked position, the entropy in
+ * nats of its softmax at temperature T,
+ *     H = -sum_v p_v ln p_v,   p_v = exp((l_v - max) / T) / sum_u exp((l_u - max) / T),
+ * computed in the same pass; unmasked positions get +inf.  Per block:
  *   BDLM_COMMIT_THRESHOLD        exactly bdlm_confidence_commit (k ignored);
  *   BDLM_COMMIT_TOPK             the min(k, masked) masked positions of highest confidence
  *                                (compared as float32; lower position first among equals);
  *   BDLM_COMMIT_SEQUENTIAL       the min(k, masked) leftmost masked positions;
- *   BDLM_COMMIT_ANTI_SEQUENTIAL  the min(k, masked) rightmost masked positions.
- * k >= 1 for the last three (e.g. L / denoising steps); threshold is checked only for the
- * threshold rule.  Layouts, limits and errors as bdlm_confidence_commit; an unknown rule or
- * k < 1 returns BDLM_ERR_INVALID.
+ *   BDLM_COMMIT_ANTI_SEQUENTIAL  the min(k, masked) rightmost masked positions;
+ *   BDLM_COMMIT_ENTROPY_BOUNDED  the masked positions in increasing order of entropy (lower
+ *                                position first among equals), as long as the running float32
+ *                                sum of their entropies, added in that order, stays <= threshold
+ *                                (the entropy budget, eb_threshold, in nats); at least one.
+ * k >= 1 for the top-k and sequential rules (e.g. L / denoising steps); 0 <= threshold <= 1 for
+ * the threshold rule; a finite threshold >= 0 for the entropy rule.  Layouts, limits and errors
+ * as bdlm_confidence_commit; an unknown rule or an argument out of its range returns
+ * BDLM_ERR_INVALID.  Scratch (the partial results) comes from the library workspace.
  */
 int bdlm_confidence_commit_rule(const bdlm_bf16* logits, const uint8_t* mask, int B, int L, int V,
                                 int rule, int k, float threshold, float temperature,
-                                int32_t* tok_out, float* conf_out, uint8_t* commit_out,
-                                bdlm_stream stream);
+                                int32_t* tok_out, float* conf_out, float* entropy_out,
+                                uint8_t* commit_out, bdlm_stream stream);
 
 /*
  * bdlm_confidence_commit without any device allocation (the pages have no counterpart of
@@ -275,20 +286,22 @@ int bdlm_confidence_commit_noalloc(const bdlm_bf16* logits, const uint8_t* mask,
  * logits (lowest index on ties), conf_out its max probability (the same value up to float32
  * summation order), and each block commits among its scored positions by the rule.  Positions
  * that are not scored (unmasked, or in a SAVING sequence) get tok_out = -1, conf_out = -inf,
- * commit_out = 0.
+ * entropy_out = +inf, commit_out = 0.  entropy_out (NULL when not wanted) receives the scored
+ * positions' entropies as bdlm_confidence_commit_rule defines them, from the same bf16 logits.
  *
  * Layouts: hidden [B*L, H] bf16 (row b*L+i); w [V, H] bf16; mask [B, L] uint8; denoising [B]
- * uint8 or NULL; tok_out [B, L] int32; conf_out [B, L] float; commit_out [B, L] uint8; logits
+ * uint8 or NULL; tok_out [B, L] int32; conf_out, entropy_out [B, L] float; commit_out [B, L]
+ * uint8; logits
  * [B*L, V] bf16 or NULL: when given, the scored rows' logits are stored as bdlm_lm_head would
  * store them (other rows untouched).  H % 8 == 0, V % 8 == 0, 1 <= L <= 64,
- * B*L <= 256 * (SM count); temperature > 0; 0 <= threshold <= 1 for the threshold rule,
- * k >= 1 for the others.  Scratch (the scored-row list, gathered rows, partials) comes from the
- * library workspace.
+ * B*L <= 256 * (SM count); temperature > 0; rule arguments as bdlm_confidence_commit_rule.
+ * Scratch (the scored-row list, gathered rows, partials) comes from the library workspace.
  */
 int bdlm_lm_head_commit(const bdlm_bf16* hidden, const bdlm_bf16* w, const uint8_t* mask,
                         const uint8_t* denoising, int B, int L, int H, int V, int rule, int k,
                         float threshold, float temperature, int32_t* tok_out, float* conf_out,
-                        uint8_t* commit_out, bdlm_bf16* logits, bdlm_stream stream);
+                        float* entropy_out, uint8_t* commit_out, bdlm_bf16* logits,
+                        bdlm_stream stream);
 
 /*
  * Mask update between denoising steps: mask[i] = 0 wherever commit[i] != 0.

@@ -55,7 +55,8 @@ def _load():
                                                      ctypes.c_double, P, I, P, P, P, P, P]
             lib.oracle_confidence_commit.restype = I
             lib.oracle_confidence_commit_rule.argtypes = [I, I, I, P, P, I, I, ctypes.c_double,
-                                                          ctypes.c_double, P, I, P, P, P, P, P]
+                                                          ctypes.c_double, P, I, P, P, P, P, P,
+                                                          P, P]
             lib.oracle_confidence_commit_rule.restype = I
             lib.oracle_apply_commit.argtypes = [I, P, P]
             lib.oracle_apply_commit.restype = None
@@ -141,19 +142,23 @@ def lm_head(hidden, w, rows, cols=None) -> np.ndarray:
 
 
 class CommitResult:
-    def __init__(self, tok, conf, conf32, commit, near):
+    def __init__(self, tok, conf, conf32, commit, near, ent, ent32):
         self.tok, self.conf, self.conf32, self.commit, self.near = tok, conf, conf32, commit, near
+        self.ent, self.ent32 = ent, ent32
 
 
 # Commit rules (JetEngine notes, "Remasking Strategies"): threshold = low_confidence_dynamic,
-# top-k = low_confidence_static, sequential / anti-sequential = left-to-right / right-to-left.
+# top-k = low_confidence_static, sequential / anti-sequential = left-to-right / right-to-left,
+# entropy-bounded = lowest entropies first within an entropy budget (eb_threshold).
 RULE_THRESHOLD, RULE_TOPK, RULE_SEQUENTIAL, RULE_ANTI_SEQUENTIAL = 0, 1, 2, 3
+RULE_ENTROPY_BOUNDED = 4
 
 
 def confidence_commit(logits, mask, threshold, temperature, blocks=None, rule=RULE_THRESHOLD,
                       k=1) -> CommitResult:
-    """Per-position argmax token and confidence, and the per-block commit decision by `rule`
-    (k positions per block for the top-k and sequential rules)."""
+    """Per-position argmax token, confidence and entropy (nats), and the per-block commit
+    decision by `rule` (k positions per block for the top-k and sequential rules; `threshold`
+    is the entropy budget of the entropy-bounded rule)."""
     lib = _load()
     mask = np.ascontiguousarray(mask, dtype=np.uint8)
     B, L = mask.shape
@@ -164,14 +169,17 @@ def confidence_commit(logits, mask, threshold, temperature, blocks=None, rule=RU
     conf32 = np.full((B, L), -np.inf, dtype=np.float32)
     commit = np.zeros((B, L), dtype=np.uint8)
     near = np.zeros((B, L), dtype=np.uint8)
+    ent = np.full((B, L), np.inf, dtype=np.float64)
+    ent32 = np.full((B, L), np.inf, dtype=np.float32)
     bl = None if blocks is None else np.ascontiguousarray(blocks, dtype=np.int32)
     rc = lib.oracle_confidence_commit_rule(B, L, V, _ptr(logits), _ptr(mask), int(rule), int(k),
                                            float(threshold), float(temperature), _ptr(bl),
                                            0 if bl is None else len(bl), _ptr(tok), _ptr(conf),
-                                           _ptr(conf32), _ptr(commit), _ptr(near))
+                                           _ptr(conf32), _ptr(commit), _ptr(near), _ptr(ent),
+                                           _ptr(ent32))
     if rc != 0:
         raise ValueError("oracle_confidence_commit: bad arguments")
-    return CommitResult(tok, conf, conf32, commit, near)
+    return CommitResult(tok, conf, conf32, commit, near, ent, ent32)
 
 
 def apply_commit(mask, commit) -> np.ndarray:

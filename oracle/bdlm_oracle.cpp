@@ -192,18 +192,39 @@ int oracle_lm_head(int n_rows, int H, int V, const uint16_t* hidden, const uint1
 //     first among equal confidences), or every masked position if there are fewer than k.
 //   2 sequential: the k leftmost masked positions (left-to-right unmasking).
 //   3 anti-sequential: the k rightmost masked positions.
-// Confidences are compared after rounding to float32, the precision the GPU reports them in.
-// near: bit 0 = |conf - threshold| <= 1e-5 * threshold (rule 0; a decision that may
-// legitimately differ), bit 1 = a confidence tie within 1e-5 relative decided the position:
-// the fallback's top two (rule 0) or the last chosen and first unchosen (rule 1).
-// blocks (n_blocks; NULL = all B) selects the blocks computed.
+//   4 entropy-bounded (entropy_bounded, budget eb_threshold = `threshold`, notes "Key Config
+//     Parameters"): the masked positions in increasing order of entropy (lowest i first among
+//     equal entropies), as long as the running sum of their entropies stays <= the budget;
+//     at least one.  Reading: the budget bounds the total entropy of the positions committed
+//     in one step, lowest entropy first (the notes name the rule and its parameter only).
+// Per masked position also the entropy of its softmax at temperature T, in nats:
+//     H = -sum_v p_v ln p_v,   p_v = exp((l_v - m) / T) / sum_u exp((l_u - m) / T)
+// (+inf for unmasked positions).
+// Confidences and entropies are compared after rounding to float32, the precision the GPU
+// reports them in; the entropy rule's running sum is a float32 sum in the rule's order.
+// near: bit 0 = a decision at the threshold or budget that may legitimately differ:
+// |conf - threshold| <= 1e-5 * threshold (rule 0), or a running entropy sum within the
+// entropy tolerance (1e-4 + 1e-5 H per term) of the budget (rule 4); bit 1 = a near-tie
+// decided the position: confidences within 1e-5 relative for the fallback's top two (rule 0)
+// or the last chosen and first unchosen (rule 1), entropies within the entropy tolerance of
+// each other at neighbouring places of the order (rule 4).
+// blocks (n_blocks; NULL = all B) selects the blocks computed.  ent / ent32 may be NULL.
 int oracle_confidence_commit_rule(int B, int L, int V, const uint16_t* logits,
                                   const uint8_t* mask, int rule, int k, double threshold,
                                   double temperature, const int32_t* blocks, int n_blocks,
                                   int32_t* tok, double* conf, float* conf32, uint8_t* commit,
-                                  uint8_t* near) {
+                                  uint8_t* near, double* ent, float* ent32) {
     if (L <= 0 || V <= 0 || !(temperature > 0.0)) return -1;
-    if (rule < 0 || rule > 3 || (rule > 0 && k < 1)) return -1;
+    if (rule < 0 || rule > 4 || ((rule == 1 || rule == 2 || rule == 3) && k < 1)) return -1;
+    if (rule == 4 && !(threshold >= 0.0 && std::isfinite(threshold))) return -1;
+    std::vector<double> ent_buf;
+    std::vector<float> ent32_buf;
+    if (rule == 4 && (ent == nullptr || ent32 == nullptr)) {
+        ent_buf.resize(static_cast<size_t>(B) * L);
+        ent32_buf.resize(static_cast<size_t>(B) * L);
+        ent = ent_buf.data();
+        ent32 = ent32_buf.data();
+    }
     const int count = blocks ? n_blocks : B;
     const float thr32 = static_cast<float>(threshold);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -218,6 +239,10 @@ int oracle_confidence_commit_rule(int B, int L, int V, const uint16_t* logits,
                 tok[r] = -1;
                 conf[r] = -std::numeric_limits<double>::infinity();
                 conf32[r] = -std::numeric_limits<float>::infinity();
+                if (ent) {
+                    ent[r] = std::numeric_limits<double>::infinity();
+                    ent32[r] = std::numeric_limits<float>::infinity();
+                }
                 continue;
             }
             const uint16_t* row = logits + r * static_cast<size_t>(V);
@@ -232,6 +257,16 @@ int oracle_confidence_commit_rule(int B, int L, int V, const uint16_t* logits,
             tok[r] = best;
             conf[r] = 1.0 / z;
             conf32[r] = static_cast<float>(conf[r]);
+            if (ent) {
+                // H = -sum_v p_v ln p_v over the probabilities, term by term
+                double h = 0.0;
+                for (int v = 0; v < V; ++v) {
+                    const double p = std::exp((bf16_to_f64(row[v]) - m) / temperature) / z;
+                    if (p > 0.0) h -= p * std::log(p);
+                }
+                ent[r] = h;
+                ent32[r] = static_cast<float>(h);
+            }
             if (rule == 0 && std::fabs(conf[r] - threshold) <= 1e-5 * threshold) near[r] |= 1;
         }
         std::vector<int> masked;
@@ -277,6 +312,32 @@ int oracle_confidence_commit_rule(int B, int L, int V, const uint16_t* logits,
                     near[r0 + last] |= 2;
                 }
             }
+        } else if (rule == 4) {
+            // increasing entropy (float32), lowest position first among equals
+            std::vector<int> order(masked);
+            std::stable_sort(order.begin(), order.end(),
+                             [&](int x, int y) { return ent32[r0 + x] < ent32[r0 + y]; });
+            const float budget32 = static_cast<float>(threshold);
+            float run = 0.f;
+            double tol = 0.0;
+            for (size_t c = 0; c < order.size(); ++c) {
+                const int i = order[c];
+                const float next = run + ent32[r0 + i];
+                tol += 1e-4 + 1e-5 * ent[r0 + i];
+                if (std::fabs(static_cast<double>(next) - threshold) <= tol)
+                    for (int j : masked) near[r0 + j] |= 1;
+                if (c > 0 && !(next <= budget32)) break;
+                run = next;
+                commit[r0 + i] = 1;
+            }
+            for (size_t c = 0; c + 1 < order.size(); ++c) {
+                const int i = order[c], j = order[c + 1];
+                const double hi = ent[r0 + i], hj = ent[r0 + j];
+                if (std::fabs(hi - hj) <= 1e-4 + 1e-5 * std::max(hi, hj)) {
+                    near[r0 + i] |= 2;
+                    near[r0 + j] |= 2;
+                }
+            }
         } else {
             const int n = std::min<int>(k, static_cast<int>(masked.size()));
             for (int c = 0; c < n; ++c) {
@@ -294,7 +355,8 @@ int oracle_confidence_commit(int B, int L, int V, const uint16_t* logits, const 
                              int n_blocks, int32_t* tok, double* conf, float* conf32,
                              uint8_t* commit, uint8_t* near) {
     return oracle_confidence_commit_rule(B, L, V, logits, mask, 0, 1, threshold, temperature,
-                                         blocks, n_blocks, tok, conf, conf32, commit, near);
+                                         blocks, n_blocks, tok, conf, conf32, commit, near,
+                                         nullptr, nullptr);
 }
 
 // Mask update between steps: mask &= ~commit (JetEngine notes, "Important Patterns":

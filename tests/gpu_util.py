@@ -39,3 +39,15 @@ def compare_commit(ref, tok, conf, commit, mask, rtol_conf=1e-5):
     bad = differ & ~near_blk
     assert not bad.any(), f"commit differs in blocks {np.nonzero(bad)[0][:10]}"
     return int((differ & near_blk).sum()), int(near_blk.sum())
+
+
+def compare_entropy(ref, ent, mask):
+    """Entropies of masked positions within 1e-4 + 1e-5 H of the oracle's (float32
+    accumulation over the vocabulary); +inf at unmasked positions.  Returns the largest
+    absolute error."""
+    m = mask.astype(bool)
+    err = np.abs(ent[m].astype(np.float64) - ref.ent[m])
+    tol = 1e-4 + 1e-5 * np.abs(ref.ent[m])
+    assert np.all(err <= tol), f"entropy error {err.max()} (tol {tol[np.argmax(err)]})"
+    assert np.all(np.isposinf(ent[~m]))
+    return float(err.max(initial=0.0))

@@ -57,23 +57,36 @@ def test_host_side_validation_rejects_bad_arguments(so):
         lambda: so.bdlm_lm_head(P + 2, P, P, 4, 8, 16, 64, P, None),  # misaligned hidden
         lambda: so.bdlm_apply_commit(P, P, -1, None),
         # fused LM head + commit: hidden, w, mask, den, B, L, H, V, rule, k, tau, T, tok, conf,
-        # commit, logits, stream
-        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 65, 16, 64, 0, 1, 0.5, 1.0, P, P, P,
-                                       None, None),                            # L > 64
-        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 12, 64, 0, 1, 0.5, 1.0, P, P, P,
-                                       None, None),                            # H % 8 != 0
-        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 60, 0, 1, 0.5, 1.0, P, P, P,
-                                       None, None),                            # V % 8 != 0
-        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 4, 1, 0.5, 1.0, P, P, P,
-                                       None, None),                            # unknown rule
-        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 1, 0, 0.5, 1.0, P, P, P,
-                                       None, None),                            # k = 0
-        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 0, 1, 0.5, -1.0, P, P, P,
-                                       None, None),                            # T < 0
-        lambda: so.bdlm_lm_head_commit(P, P, None, None, 2, 4, 16, 64, 0, 1, 0.5, 1.0, P, P, P,
-                                       None, None),                            # null mask
-        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 0, 1, 0.5, 1.0, P, P, P,
-                                       P + 8, None),                           # misaligned logits
+        # entropy, commit, logits, stream
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 65, 16, 64, 0, 1, 0.5, 1.0, P, P, None,
+                                       P, None, None),                         # L > 64
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 12, 64, 0, 1, 0.5, 1.0, P, P, None,
+                                       P, None, None),                         # H % 8 != 0
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 60, 0, 1, 0.5, 1.0, P, P, None,
+                                       P, None, None),                         # V % 8 != 0
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 5, 1, 0.5, 1.0, P, P, None,
+                                       P, None, None),                         # unknown rule
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 1, 0, 0.5, 1.0, P, P, None,
+                                       P, None, None),                         # k = 0
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 0, 1, 0.5, -1.0, P, P, None,
+                                       P, None, None),                         # T < 0
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 4, 1, -0.5, 1.0, P, P, None,
+                                       P, None, None),                         # budget < 0
+        lambda: so.bdlm_lm_head_commit(P, P, None, None, 2, 4, 16, 64, 0, 1, 0.5, 1.0, P, P,
+                                       None, P, None, None),                   # null mask
+        lambda: so.bdlm_lm_head_commit(P, P, P, None, 2, 4, 16, 64, 0, 1, 0.5, 1.0, P, P, None,
+                                       P, P + 8, None),                        # misaligned logits
+        # commit with a rule: logits, mask, B, L, V, rule, k, tau, T, tok, conf, entropy, commit
+        lambda: so.bdlm_confidence_commit_rule(P, P, 1, 4, 10, 5, 1, 0.5, 1.0, P, P, None, P,
+                                               None),                          # unknown rule
+        lambda: so.bdlm_confidence_commit_rule(P, P, 1, 4, 10, 4, 1, -1.0, 1.0, P, P, None, P,
+                                               None),                          # budget < 0
+        lambda: so.bdlm_confidence_commit_rule(P, P, 1, 4, 10, 4, 1, float("inf"), 1.0, P, P,
+                                               None, P, None),                 # budget inf
+        lambda: so.bdlm_confidence_commit_rule(P, P, 1, 4, 10, 0, 1, 1.5, 1.0, P, P, None, P,
+                                               None),                          # tau > 1
+        lambda: so.bdlm_confidence_commit_rule(P, P, 1, 4, 10, 1, 0, 0.5, 1.0, P, P, None, P,
+                                               None),                          # k = 0
     ]
     for f in bad:
         assert f() == bd.BDLM_ERR_INVALID
@@ -89,5 +102,7 @@ def test_host_side_validation_rejects_bad_arguments(so):
     assert so.bdlm_confidence_commit(P, P, 0, 4, 10, 0.5, 1.0, P, P, P, None) == 0
     assert so.bdlm_lm_head(P, P, P, 0, 8, 16, 64, P, None) == 0
     assert so.bdlm_apply_commit(P, P, 0, None) == 0
-    assert so.bdlm_lm_head_commit(P, P, P, None, 0, 4, 16, 64, 0, 1, 0.5, 1.0, P, P, P, None,
-                                  None) == 0
+    assert so.bdlm_lm_head_commit(P, P, P, None, 0, 4, 16, 64, 0, 1, 0.5, 1.0, P, P, None, P,
+                                  None, None) == 0
+    assert so.bdlm_confidence_commit_rule(P, P, 0, 4, 10, 4, 1, 2.0, 1.0, P, P, None, P,
+                                          None) == 0

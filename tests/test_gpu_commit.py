@@ -4,12 +4,14 @@ import pytest
 
 import oracle
 import workloads as W
-from gpu_util import bf16_tensor, compare_commit, dev, host
+from gpu_util import bf16_tensor, compare_commit, compare_entropy, dev, host
 
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(lib, logits_bits, mask, threshold, temperature, rule=None, k=1):
+def run_gpu(lib, logits_bits, mask, threshold, temperature, rule=None, k=1, entropy=False):
+    """tok, conf, commit (and the entropies when `entropy`) of one call; rule None uses the
+    threshold entry point without entropies."""
     import torch
     B, L = mask.shape
     V = logits_bits.size // (B * L)
@@ -18,12 +20,15 @@ def run_gpu(lib, logits_bits, mask, threshold, temperature, rule=None, k=1):
     tok = torch.empty((B, L), dtype=torch.int32, device="cuda")
     conf = torch.empty((B, L), dtype=torch.float32, device="cuda")
     com = torch.full((B, L), 7, dtype=torch.uint8, device="cuda")
-    if rule is None:
+    ent = torch.full((B, L), -5.0, dtype=torch.float32, device="cuda") if entropy else None
+    if rule is None and not entropy:
         lib.bdlm_confidence_commit(lg, mk, B, L, V, threshold, temperature, tok, conf, com)
     else:
-        lib.bdlm_confidence_commit_rule(lg, mk, B, L, V, rule, k, threshold, temperature, tok,
-                                        conf, com)
+        lib.bdlm_confidence_commit_rule(lg, mk, B, L, V, 0 if rule is None else rule, k,
+                                        threshold, temperature, tok, conf, com, entropy_out=ent)
     torch.cuda.synchronize()
+    if entropy:
+        return host(tok), host(conf), host(com), host(ent)
     return host(tok), host(conf), host(com)
 
 
@@ -165,6 +170,79 @@ def test_rule_arguments_rejected(lib):
     tok = torch.empty((1, 4), dtype=torch.int32, device="cuda")
     conf = torch.empty((1, 4), dtype=torch.float32, device="cuda")
     com = torch.empty((1, 4), dtype=torch.uint8, device="cuda")
-    for rule, k in ((9, 1), (lib.BDLM_COMMIT_TOPK, 0), (-1, 1)):
+    for rule, k, thr in ((9, 1, 0.5), (lib.BDLM_COMMIT_TOPK, 0, 0.5), (-1, 1, 0.5),
+                         (lib.BDLM_COMMIT_ENTROPY_BOUNDED, 1, -0.1)):
         with pytest.raises(lib.BdlmError):
-            lib.bdlm_confidence_commit_rule(lg, mk, 1, 4, 16, rule, k, 0.5, 1.0, tok, conf, com)
+            lib.bdlm_confidence_commit_rule(lg, mk, 1, 4, 16, rule, k, thr, 1.0, tok, conf, com)
+
+
+@pytest.mark.parametrize("config", [1, 2, 4])
+def test_entropy_configs_full_size(lib, config):
+    """Entropies of every masked position at full size (the supplementary peaks, so rows range
+    from flat to nearly one-hot) within 1e-4 + 1e-5 H of the oracle; the threshold rule's
+    tokens, confidences and commits unchanged by asking for them."""
+    c = W.CONFIGS[config]
+    rng = np.random.default_rng(W.seed_for(config, 5))
+    ci = W.commit_inputs(config, rng, c["B"], c["L"], c["V"], supplementary=True)
+    ref = oracle.confidence_commit(ci.logits, ci.mask, ci.threshold, ci.temperature)
+    tok, conf, com, ent = run_gpu(lib, ci.logits, ci.mask, ci.threshold, ci.temperature,
+                                  entropy=True)
+    compare_commit(ref, tok, conf, com, ci.mask)
+    err = compare_entropy(ref, ent, ci.mask)
+    plain = run_gpu(lib, ci.logits, ci.mask, ci.threshold, ci.temperature)
+    for x, y in zip(plain, (tok, conf, com)):
+        assert np.array_equal(x, y)
+    print(f"config {config}: entropy max abs err {err:.2e}, "
+          f"range {ref.ent[ci.mask == 1].min():.3f} .. {ref.ent[ci.mask == 1].max():.3f}")
+
+
+@pytest.mark.parametrize("B,L,V", [(3, 4, 4), (2, 1, 151939), (5, 7, 1001), (2, 64, 3000),
+                                   (1, 3, 1), (4, 16, 151936 + 5)])
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_entropy_odd_shapes(lib, B, L, V, T):
+    rng = np.random.default_rng(B * 7000 + L * 10 + V)
+    frac = rng.uniform(0.0, 1.0, size=B)
+    frac[0] = 1.0
+    mask = W.make_mask_fixed_fraction(rng, B, L, frac)
+    logits = W.poison_unmasked_rows(W.make_logits(rng, B * L, V, peak_height=(0.0, 14.0)), mask)
+    ref = oracle.confidence_commit(logits, mask, 0.4, T)
+    tok, conf, com, ent = run_gpu(lib, logits, mask, 0.4, T, entropy=True)
+    compare_commit(ref, tok, conf, com, mask)
+    compare_entropy(ref, ent, mask)
+
+
+@pytest.mark.parametrize("budget", [0.0, 1.0, 5.0, 60.0])
+def test_entropy_bounded_rule(lib, budget):
+    """entropy_bounded against the oracle on config-4-like blocks (L = 64, masked fraction
+    U[0.1, 0.9], peaks U[0, 16] so the entropies spread), with a block that has no masked
+    position; blocks whose decision the oracle flags as near the budget or a near-tie are
+    counted, not failed."""
+    rng = np.random.default_rng(300 + int(budget * 10))
+    B, L, V = 8, 64, 20000
+    mask = np.zeros((B, L), np.uint8)
+    for b in range(B):
+        mask[b] = W.make_mask_fixed_fraction(rng, 1, L, rng.uniform(0.1, 0.9))[0]
+    mask[3] = 0
+    logits = W.poison_unmasked_rows(W.make_logits(rng, B * L, V, peak_height=(0, 16)), mask)
+    ref = oracle.confidence_commit(logits, mask, budget, 1.0, rule=oracle.RULE_ENTROPY_BOUNDED)
+    tok, conf, com, ent = run_gpu(lib, logits, mask, budget, 1.0,
+                                  rule=lib.BDLM_COMMIT_ENTROPY_BOUNDED, entropy=True)
+    near_diff, near_blocks = compare_commit(ref, tok, conf, com, mask)
+    compare_entropy(ref, ent, mask)
+    has = mask.sum(1) > 0
+    assert np.all(com.sum(1)[has] >= 1) and np.all(com.sum(1)[~has] == 0)
+    assert lib.bdlm_device_error() == 0
+    print(f"budget {budget}: commits per block {com.sum(1).tolist()}, near blocks "
+          f"{near_blocks}, differing {near_diff}")
+
+
+def test_entropy_bounded_full_size_config4(lib):
+    c = W.CONFIGS[4]
+    rng = np.random.default_rng(W.seed_for(4, 6))
+    ci = W.commit_inputs(4, rng, c["B"], c["L"], c["V"], supplementary=True)
+    ref = oracle.confidence_commit(ci.logits, ci.mask, 4.0, 1.0,
+                                   rule=oracle.RULE_ENTROPY_BOUNDED)
+    tok, conf, com, ent = run_gpu(lib, ci.logits, ci.mask, 4.0, 1.0,
+                                  rule=lib.BDLM_COMMIT_ENTROPY_BOUNDED, entropy=True)
+    compare_commit(ref, tok, conf, com, ci.mask)
+    compare_entropy(ref, ent, ci.mask)

@@ -7,13 +7,15 @@ blocks with a position within 1e-5 of the threshold; confidences within 1e-5 rel
 scored rows are the masked rows of DENOISING sequences; every other position must read
 tok = -1, conf = -inf, commit = 0, and logits rows that are not scored stay untouched.  The
 fused results also match the unfused calls (bdlm_lm_head, then
-bdlm_confidence_commit_rule over the scored rows) exactly for tokens and commits."""
+bdlm_confidence_commit_rule over the scored rows) exactly for tokens and commits.  The entropy
+of every scored position is within 1e-4 + 1e-5 H of the oracle's over the same logits (+inf
+elsewhere), and the entropy-bounded rule decides like the oracle."""
 import numpy as np
 import pytest
 
 import oracle
 import workloads as W
-from gpu_util import bf16_tensor, compare_commit, dev, host
+from gpu_util import bf16_tensor, compare_commit, compare_entropy, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -34,16 +36,17 @@ def run_fused(lib, hidden, w, mask, den, B, L, H, V, rule, k, thr, T, want_logit
     tok = torch.full((B, L), -9, dtype=torch.int32, device="cuda")
     conf = torch.full((B, L), 9.0, dtype=torch.float32, device="cuda")
     com = torch.full((B, L), 9, dtype=torch.uint8, device="cuda")
+    ent = torch.full((B, L), -5.0, dtype=torch.float32, device="cuda")
     logits = None
     if want_logits:
         logits = torch.full((B * L, V), float("nan"), dtype=torch.bfloat16, device="cuda")
     lib.bdlm_lm_head_commit(bf16_tensor(hidden), bf16_tensor(w), dev(mask),
                             None if den is None else dev(den), B, L, H, V, rule, k, thr, T, tok,
-                            conf, com, logits)
+                            conf, com, logits, entropy_out=ent)
     torch.cuda.synchronize()
     assert lib.bdlm_device_error() == 0
     lg = None if logits is None else logits.view(torch.int16).cpu().numpy().view(np.uint16)
-    return host(tok), host(conf), host(com), lg
+    return host(tok), host(conf), host(com), lg, host(ent)
 
 
 def scored_mask(mask, den):
@@ -55,7 +58,7 @@ def scored_mask(mask, den):
 
 def check_against_oracle(lib, case, B, L, H, V, rule, k, thr, T, col_sample=None):
     rng, hidden, w, mask, den = case
-    tok, conf, com, lg = run_fused(lib, hidden, w, mask, den, B, L, H, V, rule, k, thr, T)
+    tok, conf, com, lg, ent = run_fused(lib, hidden, w, mask, den, B, L, H, V, rule, k, thr, T)
     sm = scored_mask(mask, den)
     rows = np.nonzero(sm.reshape(-1))[0].astype(np.int32)
     others = np.setdiff1d(np.arange(B * L), rows)
@@ -72,6 +75,7 @@ def check_against_oracle(lib, case, B, L, H, V, rule, k, thr, T, col_sample=None
         assert excess.max() <= 0, f"logits: max excess {excess.max()}"
     ref_c = oracle.confidence_commit(lg, sm, thr, T, rule=rule, k=k)
     near, _ = compare_commit(ref_c, tok, conf, com, sm)
+    compare_entropy(ref_c, ent, sm)
     return tok, conf, com, near
 
 
@@ -85,6 +89,8 @@ CASES = [
     (6, 40, 32, 320, 1288, 0.3, 0.75, 0.2, 0, 1, 0.9, 1.0),
     (7, 65, 2, 2560, 640, 1.0, None, 0.05, 0, 1, 0.2, 1.0),    # 130 rows: a ragged sub-tile
     (8, 1, 4, 128, 64, 0.5, None, 0.5, 0, 1, 0.9, 1.0),        # V smaller than one share
+    (9, 64, 16, 256, 2048, 0.8, 0.75, 0.3, 4, 1, 2.0, 1.0),    # entropy budget 2 nats
+    (10, 150, 4, 512, 4104, 0.7, None, 0.25, 4, 1, 0.5, 0.8),  # entropy rule on CTA pairs
 ]
 
 
@@ -101,9 +107,9 @@ def test_fused_equals_unfused_and_logits_are_optional(lib):
     B, L, H, V = 96, 4, 512, 4104
     case = make_case(11, B, L, H, V, 0.6, 0.75, 0.2)
     _, hidden, w, mask, den = case
-    tok, conf, com, lg = run_fused(lib, hidden, w, mask, den, B, L, H, V, 0, 1, 0.4, 1.0)
-    tok2, conf2, com2, _ = run_fused(lib, hidden, w, mask, den, B, L, H, V, 0, 1, 0.4, 1.0,
-                                     want_logits=False)
+    tok, conf, com, lg, _ = run_fused(lib, hidden, w, mask, den, B, L, H, V, 0, 1, 0.4, 1.0)
+    tok2, conf2, com2, _, _ = run_fused(lib, hidden, w, mask, den, B, L, H, V, 0, 1, 0.4, 1.0,
+                                        want_logits=False)
     assert np.array_equal(tok, tok2) and np.array_equal(com, com2)
     assert np.array_equal(conf, conf2)
     sm = scored_mask(mask, den)
@@ -129,11 +135,12 @@ def test_nothing_scored(lib):
     case = make_case(12, B, L, H, V, 0.5, None, 0.2)
     _, hidden, w, mask, _ = case
     den = np.zeros(B, np.uint8)              # every sequence SAVING
-    tok, conf, com, lg = run_fused(lib, hidden, w, mask, den, B, L, H, V, 0, 1, 0.5, 1.0)
+    tok, conf, com, lg, ent = run_fused(lib, hidden, w, mask, den, B, L, H, V, 0, 1, 0.5, 1.0)
     assert np.all(tok == -1) and np.all(np.isneginf(conf)) and np.all(com == 0)
+    assert np.all(np.isposinf(ent))
     assert np.all(lg == 0x7FC0)
-    tok, conf, com, _ = run_fused(lib, hidden, w, np.zeros_like(mask), None, B, L, H, V, 0, 1,
-                                  0.5, 1.0)
+    tok, conf, com, _, _ = run_fused(lib, hidden, w, np.zeros_like(mask), None, B, L, H, V, 0, 1,
+                                     0.5, 1.0)
     assert np.all(tok == -1) and np.all(com == 0)
 
 

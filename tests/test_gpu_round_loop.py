@@ -150,7 +150,7 @@ def check_against_oracle_chain(c, got, rule, k, thr):
 
 
 @pytest.mark.parametrize("rule,k,thr", [(0, 1, 0.6), (1, 1, 0.5), (1, 2, 0.5), (2, 2, 0.5),
-                                        (3, 1, 0.5)])
+                                        (3, 1, 0.5), (4, 1, 1.5)])
 def test_loop_matches_oracle_chain(lib, rule, k, thr):
     c = Case(seed=40 + rule + 10 * k)
     got = run_loop(lib, c, rule, k, thr)

@@ -23,7 +23,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "commit_worked_exampl
 
 
 def _closed(expr: str) -> float:
-    return float(eval(expr, {"__builtins__": {}}, {"E": math.exp}))
+    return float(eval(expr, {"__builtins__": {}}, {"E": math.exp, "LN": math.log}))
 
 
 def _parse_golden():
@@ -46,6 +46,14 @@ def _parse_golden():
             cases.append(dict(name=parts[0].split()[1], mask=[int(c) for c in parts[1]],
                               replace=parts[2], rule=parts[3], k=int(parts[4]), tau=0.5, T=1.0,
                               commit=[int(c) for c in parts[5]]))
+        elif parts[0].startswith("erow"):
+            r = int(parts[0].split()[1])
+            rows[r].update(h1=float(parts[1]), h05=float(parts[2]), hclosed1=parts[3],
+                           hclosed05=parts[4])
+        elif parts[0].startswith("ecase"):
+            cases.append(dict(name=parts[0].split()[1], mask=[int(c) for c in parts[1]],
+                              replace=parts[2], rule="entropy_bounded", budget=float(parts[3]),
+                              T=float(parts[4]), commit=[int(c) for c in parts[5]]))
     return rows, cases
 
 
@@ -104,6 +112,95 @@ def test_commit_rules_worked_example(case):
     assert list(res.commit[0]) == c["commit"]
     if case == "I":
         assert res.near[0, 1] & 2 and res.near[0, 2] & 2  # the tie at the cut is flagged
+
+
+def test_golden_entropy_closed_forms():
+    """The printed entropies match their closed forms, and the oracle's entropies match both
+    (all four rows masked, T = 1 and T = 0.5)."""
+    rows, _ = _parse_golden()
+    logits = np.array([rows[r]["logits"] for r in range(4)], dtype=np.float32)
+    bits = f32_to_bf16_bits(logits)
+    mask = np.ones((1, 4), np.uint8)
+    for T, key, ckey in ((1.0, "h1", "hclosed1"), (0.5, "h05", "hclosed05")):
+        res = oracle.confidence_commit(bits, mask, 0.5, T)
+        for r in range(4):
+            closed = _closed(rows[r][ckey])
+            assert abs(closed - rows[r][key]) < 5e-7
+            assert abs(res.ent[0, r] - closed) <= 1e-12
+
+
+@pytest.mark.parametrize("case", ["N", "O", "P", "Q", "R", "S", "T", "U", "W"])
+def test_entropy_bounded_worked_example(case):
+    rows, cases = _parse_golden()
+    c = [x for x in cases if x["name"] == case][0]
+    logits = np.array([rows[r]["logits"] for r in range(4)], dtype=np.float32)
+    if c["replace"] != "-":
+        rr, vals = c["replace"].split("=")
+        logits[int(rr)] = [float(x) for x in vals.split(",")]
+    bits = f32_to_bf16_bits(logits)
+    mask = np.array([c["mask"]], dtype=np.uint8)
+    res = oracle.confidence_commit(bits, mask, c["budget"], c["T"],
+                                   rule=oracle.RULE_ENTROPY_BOUNDED)
+    assert list(res.commit[0]) == c["commit"]
+    assert np.all(np.isinf(res.ent[0][mask[0] == 0]))
+    if case == "T":
+        assert res.near[0, 0] & 2 and res.near[0, 2] & 2   # the entropy tie is flagged
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5, 1.7])
+def test_entropy_against_scipy(T):
+    """The oracle's entropy of random bf16 rows equals scipy's entropy of scipy's softmax."""
+    from scipy.special import softmax
+    from scipy.stats import entropy
+    rng = np.random.default_rng(47)
+    B, L, V = 3, 4, 3001
+    bits = make_logits(rng, B * L, V, peak_height=(0.0, 16.0))
+    mask = np.ones((B, L), np.uint8)
+    res = oracle.confidence_commit(bits, mask, 0.5, T)
+    x = bf16_bits_to_f32(bits).astype(np.float64).reshape(B, L, V)
+    want = entropy(softmax(x / T, axis=-1), axis=-1)
+    assert np.allclose(res.ent, want, rtol=1e-10, atol=1e-12)
+    assert np.array_equal(res.ent32, res.ent.astype(np.float32))
+
+
+def test_entropy_special_cases():
+    """Uniform rows give ln V; one dominant logit gives (almost) 0; two equal dominant logits
+    give ln 2; the entropy never exceeds ln V."""
+    V = 1000
+    x = np.zeros((3, V), np.float32)
+    x[1, 7] = 120.0
+    x[2, 3] = x[2, 900] = 120.0
+    bits = f32_to_bf16_bits(x)
+    res = oracle.confidence_commit(bits, np.ones((1, 3), np.uint8), 0.5, 1.0)
+    assert abs(res.ent[0, 0] - math.log(V)) <= 1e-12
+    assert res.ent[0, 1] < 1e-40
+    assert abs(res.ent[0, 2] - math.log(2)) <= 1e-12
+
+
+def test_entropy_bounded_against_numpy():
+    """The entropy rule against a stable argsort of float32 entropies and a float32 running sum
+    taken in that order; at least one commit in every block with a masked position."""
+    rng = np.random.default_rng(53)
+    B, L, V = 24, 16, 400
+    bits = make_logits(rng, B * L, V, peak_height=(0.0, 14.0))
+    mask = make_mask_fixed_fraction(rng, B, L, 0.7)
+    mask[5] = 0
+    for budget in (0.0, 0.5, 3.0, 20.0):
+        res = oracle.confidence_commit(bits, mask, budget, 1.0, rule=oracle.RULE_ENTROPY_BOUNDED)
+        for b in range(B):
+            pos = np.nonzero(mask[b])[0]
+            if len(pos) == 0:
+                assert res.commit[b].sum() == 0
+                continue
+            order = pos[np.argsort(res.ent32[b, pos], kind="stable")]
+            want, run = [order[0]], np.float32(res.ent32[b, order[0]])
+            for i in order[1:]:
+                nxt = np.float32(run + res.ent32[b, i])
+                if not nxt <= np.float32(budget):
+                    break
+                want.append(i)
+                run = nxt
+            assert set(np.nonzero(res.commit[b])[0].tolist()) == set(int(i) for i in want)
 
 
 @pytest.mark.parametrize("k", [1, 2, 3, 9])
