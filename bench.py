@@ -412,9 +412,9 @@ def time_round_graph(rnd: Round, stream, steps: int, warmup: int, flush, barrier
 def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
     """The round through the C-ABI from pinned host buffers.  The paged K/V cache and W are
     resident device state (the cache holds every sequence's prefix); every step copies its own
-    inputs host->device (q, the block's new K/V, the hidden rows, the mask), writes the block
-    K/V into the cache, runs attention, the LM head fused with confidence/commit and the mask
-    update, and copies tok/conf/commit back.  As in a serving loop, the inputs are
+    inputs host->device (q, the block's new K/V, the hidden rows, the mask), runs the attention
+    with the block's K/V-cache write fused in, the LM head fused with confidence/commit and the
+    mask update, and copies tok/conf/commit back.  As in a serving loop, the inputs are
     double-buffered on the device and step k+1's host->device copies run on a copy stream while
     step k computes (events order each buffer's copy after the step that last read it)."""
     import torch
@@ -461,8 +461,8 @@ def e2e_round(lib, a, ci, lm, device, steps, warmup, seed):
         stream.wait_event(copied[i])
         with torch.cuda.stream(stream):
             bf = torch.bfloat16
-            lib.bdlm_write_block_kv(desc, d["kn"].view(bf), d["vn"].view(bf), kp, vp, pt, pl, s)
-            lib.bdlm_block_attention(desc, d["q"].view(bf), kp, vp, pt, pl, L, out, s)
+            lib.bdlm_block_attention_kv(desc, d["q"].view(bf), d["kn"].view(bf), d["vn"].view(bf),
+                                        kp, vp, pt, pl, L, out, s)
             lib.bdlm_lm_head_commit(d["hid"].view(bf), w, d["mk"], None, B, L, lm.H, ci.V,
                                     lib.BDLM_COMMIT_THRESHOLD, 1, ci.threshold, ci.temperature,
                                     outs_d["tok"], outs_d["conf"], outs_d["com"], None, s)
@@ -942,6 +942,47 @@ def bench_config4(bd, device, flush, peaks, reps):
             "parity": {"attention": ap, "commit": commit_parity(ref, tok, conf, com, ci.mask)}}
 
 
+def bench_fused_kv(bd, device, flush, peaks, reps, seed):
+    """Config 2's attention with the block's K/V-cache write: the separate write kernel followed
+    by the attention, against the attention that writes the block's K/V itself (CUDA events,
+    L2 flushed before each call); and the attention alone, with the block already in the
+    cache."""
+    import torch
+    c = W.CONFIGS[2]
+    rng = np.random.default_rng(seed)
+    a = W.make_attention(rng, c["B"], c["L"], c["Hq"], c["Hkv"], c["D"], prefix_range=c["prefix"],
+                         poison=False)
+    kn = _bf16(W._normal_bf16(rng, (a.B, a.L, a.Hkv, a.D), 0.5), device)
+    vn = _bf16(W._normal_bf16(rng, (a.B, a.L, a.Hkv, a.D), 0.5), device)
+    kp, vp = _bf16(a.k_ref, device), _bf16(a.v_ref, device)
+    q = _bf16(a.q, device)
+    pt = torch.from_numpy(a.page_table_ref).to(device)
+    pl = torch.from_numpy(a.prefix_lens).to(device)
+    out = torch.empty((a.B, a.L, a.Hq, a.D), dtype=torch.bfloat16, device=device)
+    desc = bd.attn_desc(a.B, a.L, a.Hq, a.Hkv, a.D, a.page_table_ref.shape[1], a.k_ref.shape[0])
+    stream = torch.cuda.Stream(device=device)
+
+    def attn(s):
+        bd.bdlm_block_attention(desc, q, kp, vp, pt, pl, a.L, out, s)
+
+    def unfused(s):
+        bd.bdlm_write_block_kv(desc, kn, vn, kp, vp, pt, pl, s)
+        bd.bdlm_block_attention(desc, q, kp, vp, pt, pl, a.L, out, s)
+
+    def fused(s):
+        bd.bdlm_block_attention_kv(desc, q, kn, vn, kp, vp, pt, pl, a.L, out, s)
+    t_a = time_call(attn, stream, flush, reps)
+    t_u = time_call(unfused, stream, flush, reps)
+    t_f = time_call(fused, stream, flush, reps)
+    assert bd.bdlm_device_error() == 0
+    nbytes, flops = attention_bytes_flops(a, a.L)
+    nbytes += 2 * a.B * a.L * a.Hkv * a.D * 2 * 2   # the block's K/V read in and written out
+    return {"workload": "config 2 attention with the block's new K/V written into the cache",
+            "attention_us": t_a * 1e3, "write_then_attention_us": t_u * 1e3,
+            "fused_us": t_f * 1e3, "fused": roofline_entry(t_f, nbytes, flops, peaks, "hbm"),
+            "gpu_launches": {"write_then_attention": 3, "fused": 2}}
+
+
 def headline_parity(bd, a, ci, lm, device):
     """Parity of the headline round on the timed inputs: one fused round (attention, LM head +
     confidence/commit, the scored rows' bf16 logits stored), attention of sampled sequences
@@ -1138,6 +1179,8 @@ def run_ours(args, rank, world, local):
         torch.cuda.empty_cache()
         line["parity"] = headline_parity(bd, a, ci, lm, device)
         torch.cuda.empty_cache()
+        line["fused_kv_write"] = bench_fused_kv(bd, device, flush, peaks, 20, W.seed_for(2, 5))
+        torch.cuda.empty_cache()
         line["configs"] = {"1": bench_config1(bd, device, flush, peaks, 20),
                            "3": bench_config3(bd, device, flush, peaks, 10),
                            "4": bench_config4(bd, device, flush, peaks, 10)}
@@ -1156,9 +1199,9 @@ def run_ours(args, rank, world, local):
                        "ms_per_step": e2e_max,
                        "note": "per rank and step: q, the block's new K/V, hidden rows and "
                                "mask copied in from pinned host memory (double-buffered on a "
-                               "copy stream, overlapping the previous step's compute), the "
-                               "block K/V written "
-                               "into the resident cache, attention, fused LM head + commit, "
+                               "copy stream, overlapping the previous step's compute), "
+                               "attention with the block K/V written into the resident cache "
+                               "in the same kernel, fused LM head + commit, "
                                "mask update, tok/conf/commit copied back; the paged cache "
                                "(every prefix) and W are resident"}
         if rank == 0:

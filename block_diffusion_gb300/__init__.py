@@ -33,7 +33,7 @@ BDLM_COMMIT_SEQUENTIAL = 2
 BDLM_COMMIT_ANTI_SEQUENTIAL = 3
 BDLM_COMMIT_ENTROPY_BOUNDED = 4
 
-EXPORTS = ("bdlm_block_attention", "bdlm_prefill_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
+EXPORTS = ("bdlm_block_attention", "bdlm_block_attention_kv", "bdlm_prefill_attention", "bdlm_lm_head", "bdlm_lm_head_device_count",
            "bdlm_lm_head_commit", "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
            "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_round_loop_create",
            "bdlm_round_loop_launch", "bdlm_round_loop_destroy", "bdlm_status_string",
@@ -81,6 +81,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.bdlm_block_attention.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, I, P, P]
     lib.bdlm_block_attention.restype = I
+    lib.bdlm_block_attention_kv.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, I, P,
+                                            P]
+    lib.bdlm_block_attention_kv.restype = I
     lib.bdlm_lm_head.argtypes = [P, P, P, I, I, I, I, P, P]
     lib.bdlm_lm_head.restype = I
     lib.bdlm_confidence_commit.argtypes = [P, P, I, I, I, F, F, P, P, P, P]
@@ -154,6 +157,15 @@ def bdlm_block_attention(desc: AttnDesc, q, k_pages, v_pages, page_table, prefix
                                   _ptr(page_table), _ptr(prefix_lens), int(L), _ptr(out),
                                   _stream(stream))
     _check("bdlm_block_attention", rc)
+
+
+def bdlm_block_attention_kv(desc: AttnDesc, q, k_new, v_new, k_pages, v_pages, page_table,
+                            prefix_lens, L: int, out, stream=None) -> None:
+    lib = load_library()
+    rc = lib.bdlm_block_attention_kv(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                     _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                     _ptr(prefix_lens), int(L), _ptr(out), _stream(stream))
+    _check("bdlm_block_attention_kv", rc)
 
 
 def bdlm_prefill_attention(desc: AttnDesc, prompt_len: int, q, k_new, v_new, k_pages, v_pages,

@@ -143,7 +143,8 @@ LmCommitLayout lm_commit_layout(const bdlm::LmConfPlan& plan, int rows) {
 int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
                    const bdlm_bf16* k_pages, const bdlm_bf16* v_pages, const int32_t* page_table,
                    const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream,
-                   int table_div, int mask_block = 0);
+                   int table_div, int mask_block = 0,
+                   const bdlm::BlockKvWrite* kv_write = nullptr);
 
 }  // namespace
 
@@ -266,6 +267,36 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
   return attention_impl(st, d, q, k_pages, v_pages, page_table, prefix_lens, out, stream, 1);
 }
 
+int bdlm_block_attention_kv(const bdlm_attn_desc* desc, const bdlm_bf16* q,
+                            const bdlm_bf16* k_new, const bdlm_bf16* v_new, bdlm_bf16* k_pages,
+                            bdlm_bf16* v_pages, const int32_t* page_table,
+                            const int32_t* prefix_lens, int L, bdlm_bf16* out,
+                            bdlm_stream stream) {
+  if (!desc) return BDLM_ERR_INVALID;
+  const bdlm_attn_desc d = *desc;
+  if (d.B < 0 || L != d.L || d.L < 1 || d.L > 64 || d.Hq < 1 || d.Hkv < 1 ||
+      d.Hq % d.Hkv != 0 || d.Hq / d.Hkv > 16 || d.D != 128 || d.page_size != 16 ||
+      d.max_pages_per_seq < 1 || d.num_pages < 1 || !isfinite(d.sm_scale))
+    return BDLM_ERR_INVALID;
+  if (d.B == 0) return BDLM_OK;
+  if (!q || !k_new || !v_new || !k_pages || !v_pages || !page_table || !prefix_lens || !out)
+    return BDLM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) ||
+      !aligned16(v_pages) || !aligned16(out))
+    return BDLM_ERR_INVALID;
+  if (static_cast<long long>(d.B) * d.L * d.Hq > 0x7FFFFFFFll ||
+      static_cast<long long>(d.B) * d.max_pages_per_seq > 0x7FFFFFFFll ||
+      static_cast<long long>(d.max_pages_per_seq) * d.page_size > 0x7FFFFFFFll)
+    return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st);
+  if (rc) return rc;
+  const bdlm::BlockKvWrite kw{k_new, v_new, k_pages, v_pages};
+  return attention_impl(st, d, q, k_pages, v_pages, page_table, prefix_lens, out, stream, 1, 0,
+                        &kw);
+}
+
 int bdlm_prefill_attention(const bdlm_attn_desc* desc, int prompt_len, const bdlm_bf16* q,
                            const bdlm_bf16* k_new, const bdlm_bf16* v_new, bdlm_bf16* k_pages,
                            bdlm_bf16* v_pages, const int32_t* page_table,
@@ -329,7 +360,7 @@ namespace {
 int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
                    const bdlm_bf16* k_pages, const bdlm_bf16* v_pages, const int32_t* page_table,
                    const int32_t* prefix_lens, bdlm_bf16* out, bdlm_stream stream,
-                   int table_div, int mask_block) {
+                   int table_div, int mask_block, const bdlm::BlockKvWrite* kv_write) {
   int rc = get_encoder();
   if (rc) return rc;
   const AttnPlan plan = bdlm::plan_attention(d.B, d.L, d.Hq, d.Hkv, d.max_pages_per_seq,
@@ -363,7 +394,7 @@ int attention_impl(DeviceState* st, const bdlm_attn_desc& d, const bdlm_bf16* q,
                                          scale, plan, static_cast<float*>(st->data),
                                          st->attn_cnt, st->err, st->num_sms,
                                          static_cast<cudaStream_t>(stream), table_div,
-                                         mask_block);
+                                         mask_block, kv_write);
   return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
 }
 
@@ -630,10 +661,8 @@ int capture_round_loop(bdlm_round_loop* lp) {
   c.n_vec[3] = static_cast<long long>(R) * d.H * 2 / 16;
   int r2 = BDLM_OK;
   if (bdlm::launch_select_step(c, lp->step, d.steps, lp->cap) != cudaSuccess) r2 = BDLM_ERR_CUDA;
-  if (!r2) r2 = bdlm_write_block_kv(&a, lp->k_w, lp->v_w, d.k_pages, d.v_pages, d.page_table,
-                                    d.prefix_lens, s);
-  if (!r2) r2 = bdlm_block_attention(&a, lp->q_w, d.k_pages, d.v_pages, d.page_table,
-                                     d.prefix_lens, a.L, lp->attn_out, s);
+  if (!r2) r2 = bdlm_block_attention_kv(&a, lp->q_w, lp->k_w, lp->v_w, d.k_pages, d.v_pages,
+                                        d.page_table, d.prefix_lens, a.L, lp->attn_out, s);
   if (!r2) r2 = bdlm_lm_head_commit(lp->h_w, d.w, d.mask, d.denoising, a.B, a.L, d.H, d.V, d.rule,
                                     d.k, d.threshold, d.temperature, lp->tok, lp->conf, nullptr,
                                     lp->com, nullptr, s);

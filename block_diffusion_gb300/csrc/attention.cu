@@ -75,6 +75,12 @@ constexpr int kItemRing = 4;
 struct AttnParams {
   const int32_t* page_table;
   const int32_t* prefix_lens;
+  // the block's new K/V [B, L, Hkv, D] and the pools to write them into (null: the block's K/V
+  // are already in the cache)
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
   uint16_t* out;
   float* part;
   int* err;
@@ -100,6 +106,7 @@ struct Item {
   int q0;  // key position of the sequence's first query (its prefix length)
   int n_tiles, n_chunks;
   int end;
+  int wr;  // the producer writes the block's new K/V into the cache before reading it
 };
 
 __device__ __forceinline__ void record_error(int* err, int bits) { atomicOr(err, bits); }
@@ -133,8 +140,9 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   it.n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
   it.n_chunks = (it.n_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
   it.end = 0;
-  if (it.split == 0 && it.rg == 0 && it.kvh == 0 &&
-      (prefix < 0 || static_cast<long long>(prefix) + p.L > max_tok))
+  const bool len_ok = prefix >= 0 && static_cast<long long>(prefix) + p.L <= max_tok;
+  it.wr = p.k_new != nullptr && len_ok;
+  if (it.split == 0 && it.rg == 0 && it.kvh == 0 && !len_ok)
     record_error(p.err, BDLM_DEVERR_LENGTH);
   return true;
 }
@@ -352,6 +360,39 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, BDLM_DEVERR_PAGE);
       __syncwarp();
+      if (it.wr && max(it.t_begin, it.q0) < it.t_end) {
+        // With the block's K/V-cache write fused in: the new K and V rows of the block tokens
+        // this item reads go to their cache slots now, a batch of 16-byte chunks per lane at a
+        // time (loads first, then stores), and a proxy fence orders the stores before the
+        // item's page boxes read them.  The item is taken one ahead, while the ring is full,
+        // so this work is off the copy stream.  Every item that reads a token writes it (row
+        // groups store the same bytes), so no item depends on another CTA.
+        const int w0 = max(it.t_begin, it.q0), n = (it.t_end - w0) * 32;
+        constexpr int kBatch = 4;
+        for (int c0 = 0; c0 < n; c0 += 32 * kBatch) {
+          uint4 v[kBatch];
+          uint4* dst[kBatch];
+#pragma unroll
+          for (int x = 0; x < kBatch; ++x) {
+            const int c = c0 + x * 32 + lane;
+            dst[x] = nullptr;
+            if (c >= n) continue;
+            const int t = w0 + c / 32, kv = (c / 16) & 1, q = c % 16;
+            const int id = pid[(t - it.t_begin) / kPage];
+            if (id < 0) continue;   // a bad page id (flagged above): its rows are skipped
+            const size_t row = (static_cast<size_t>(it.b) * p.L + (t - it.q0)) * p.Hkv + it.kvh;
+            v[x] = __ldg(reinterpret_cast<const uint4*>((kv ? p.v_new : p.k_new) + row * 128) + q);
+            dst[x] = reinterpret_cast<uint4*>(
+                         (kv ? p.v_pool : p.k_pool) +
+                         ((static_cast<size_t>(id) * kPage + t % kPage) * p.Hkv + it.kvh) * 128) + q;
+          }
+#pragma unroll
+          for (int x = 0; x < kBatch; ++x)
+            if (dst[x] != nullptr) *dst[x] = v[x];
+        }
+        fence_proxy_async_global();
+        __syncwarp();
+      }
       if (lane == 0) publish(it);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       return true;
@@ -389,10 +430,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           gi = nullptr;
           if (!ok) break;
         }
+        const int tok0 = it.t_begin + j * kTile;
         if (lane == 0) ok = mbar_wait(&bar_empty[st], ph ^ 1, &abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        const int tok0 = it.t_begin + j * kTile;
         const int npg = min(kTile / kPage, (it.t_end - tok0 + kPage - 1) / kPage);
         // lane q < 16 copies half q / 8 of page q % 8 of the tile: one box per lane, so the
         // stage's 16 copies issue in parallel (a thread's copies issue one after another)
@@ -1624,9 +1665,15 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
                              const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
-                             cudaStream_t stream, int table_div, int mask_block) {
+                             cudaStream_t stream, int table_div, int mask_block,
+                             const BlockKvWrite* kv_write) {
   AttnParams prm;
   prm.mask_block = mask_block > 0 ? mask_block : 0;
+  prm.k_new = kv_write ? kv_write->k_new : nullptr;
+  prm.v_new = kv_write ? kv_write->v_new : nullptr;
+  prm.k_pool = kv_write ? kv_write->k_pages : nullptr;
+  prm.v_pool = kv_write ? kv_write->v_pages : nullptr;
+  if (kv_write && mask_block > 0) return cudaErrorInvalidValue;   // prefill writes separately
   prm.page_table = page_table;
   prm.table_div = table_div < 1 ? 1 : table_div;
   prm.prefix_lens = prefix_lens;

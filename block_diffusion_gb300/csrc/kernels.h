@@ -94,15 +94,25 @@ struct AttnPlan {
 
 AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_size,
                         int num_sms);
+// The block's new K/V [B, L, Hkv, D] and the pools they go to: the attention writes them into
+// the cache itself, before it reads them.
+struct BlockKvWrite {
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_pages;
+  uint16_t* v_pages;
+};
 // Sequence b uses page-table row b / table_div.  mask_block > 0 makes the queries of a
 // sequence block-causal: query i sees the prefix and the sequence's keys up to the end of its
-// own block of mask_block queries (chunked prefill); else every query sees all L.
+// own block of mask_block queries (chunked prefill); else every query sees all L.  kv_write
+// (may be null; not with mask_block) fuses the block's K/V-cache write into the attention.
 cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const int32_t* page_table,
                              const int32_t* prefix_lens, uint16_t* out, int B, int L, int Hq,
                              int Hkv, int max_pages, int num_pages, float sm_scale,
                              const AttnPlan& plan, float* part, int* cnt, int* err, int num_sms,
-                             cudaStream_t stream, int table_div = 1, int mask_block = 0);
+                             cudaStream_t stream, int table_div = 1, int mask_block = 0,
+                             const BlockKvWrite* kv_write = nullptr);
 
 // ------------------------------------------------------------------ LM head
 struct LmHeadPlan {

@@ -102,6 +102,27 @@ int bdlm_block_attention(const bdlm_attn_desc* desc, const bdlm_bf16* q,
                          bdlm_bf16* out, bdlm_stream stream);
 
 /*
+ * Block attention with the block's K/V-cache write fused in: the block's new K/V are written
+ * into the paged cache and attended to by the same kernel, with no separate write launch.
+ * Source: JetEngine notes, "Optimization History" (opt24: the KV-cache write of the block
+ * combined with the paged attention in one kernel) and "Current Profile (H200, bs=128, opt24)".
+ *
+ * Results as bdlm_write_block_kv followed by bdlm_block_attention: k_new, v_new [B, L, Hkv, D]
+ * bf16 (16-byte aligned) go to the slots prefix_lens[b] .. prefix_lens[b]+L-1 of sequence b,
+ * and out is the block attention over the updated cache.  Inside the kernel, every work item
+ * that reads one of the block's tokens first stores that token's new K (or V) row into its page
+ * slot and then loads its tile; items that share tokens (query-row groups) store identical
+ * bytes.  A page id outside [0, num_pages) or a prefix length that does not fit the page table
+ * skips the writes it concerns and sets a device error bit, as the unfused calls do.  Other
+ * arguments, layouts and limits as bdlm_block_attention; k_pages and v_pages are written.
+ */
+int bdlm_block_attention_kv(const bdlm_attn_desc* desc, const bdlm_bf16* q,
+                            const bdlm_bf16* k_new, const bdlm_bf16* v_new, bdlm_bf16* k_pages,
+                            bdlm_bf16* v_pages, const int32_t* page_table,
+                            const int32_t* prefix_lens, int L, bdlm_bf16* out,
+                            bdlm_stream stream);
+
+/*
  * Block prefill: the prompt's K/V written into the cache and block-causal attention over the
  * prompt, so that the rounds that follow find the prompt in the paged cache.
  * Source: JetEngine notes, "Kernels" (block prefill attention and the KV-cache store) and
@@ -320,8 +341,8 @@ int bdlm_apply_commit(uint8_t* mask, const uint8_t* commit, int n, bdlm_stream s
  * One round (step s, counted on the device):
  *   the step's inputs: slice s of q_steps [S, B, L, Hq, D], k_new_steps / v_new_steps
  *   [S, B, L, Hkv, D] and hidden_steps [S, B*L, H] (the model's outputs for that step, which
- *   this library does not compute) -> bdlm_write_block_kv (the block's K/V into the cache)
- *   -> bdlm_block_attention -> bdlm_lm_head_commit (mask, denoising, rule, k, threshold,
+ *   this library does not compute) -> bdlm_block_attention_kv (the block's K/V written into the
+ *   cache and attended in one kernel) -> bdlm_lm_head_commit (mask, denoising, rule, k, threshold,
  *   temperature; no logits stored) -> tok/conf/commit stored into slice s of tok_steps,
  *   conf_steps, commit_steps [S, B, L] -> bdlm_apply_commit on mask.
  * After the last round *steps_done holds the number of rounds run, and slices at or past it
