@@ -553,10 +553,11 @@ lm_conf_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
           wv[g >> 1][(g & 1) * 8 + k] = *reinterpret_cast<const uint32_t*>(&h);
         }
       }
-      // this warp's columns are in registers: the accumulator may take the tile after next
+      // this warp's columns are in registers: the accumulator may take the tile after next (a
+      // tensor-memory hand-off, ordered by the tcgen05 fences: CTA-scope release suffices)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(buf ? empty1 : empty0);
+      if (lane == 0) mbar_arrive_remote_cta(buf ? empty1 : empty0);
       if (arow < 0) continue;
       if (vbase + kConfShareCols > vend) {
         // a narrow tile or the end of V: columns past the tile take no part

@@ -178,3 +178,22 @@ def test_prefill_chunk_across_a_split_boundary(lib):
     excess = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
     assert excess.max() <= 0, f"max excess {excess.max()}"
     assert lib.bdlm_device_error() == 0
+
+
+@pytest.mark.parametrize("B,L,Hq,Hkv,prefix", [
+    (3, 40, 32, 8, (0, 700)),      # 160 rows: sub-group 1 holds 32 of them
+    (2, 16, 32, 2, (100, 900)),    # 16 query heads per KV head
+    (3, 12, 16, 1, (0, 600)),      # 192 rows, one KV head
+    (3, 33, 16, 2, (0, 500)),      # 264 rows: row groups of 256 and 8
+    (2, 64, 32, 8, (2040, 4200)),  # KV splits, ragged last tiles
+    (40, 64, 32, 8, (0, 1500)),    # enough items for whole sequences, longest first
+    (3, 50, 24, 8, (0, 700)),      # 3 query heads per KV head: 150 rows
+])
+def test_256_row_groups(lib, B, L, Hq, Hkv, prefix):
+    """129-256 query rows per KV head (two 128-row sub-groups sharing each K/V stage): ragged
+    row counts, row groups of 256 and fewer, splits with ragged last tiles, whole sequences,
+    and an odd number of query heads per KV head."""
+    rng = np.random.default_rng(B * 7 + L * 131 + Hq)
+    a = W.make_attention(rng, B, L, Hq, Hkv, 128, prefix_range=prefix)
+    check(lib, a)
+
