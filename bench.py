@@ -107,20 +107,29 @@ def load_peaks():
             "source": "fallback"}
 
 
-def profile_traffic(name: str, src: str):
+def source_digest(srcs) -> str:
+    """sha256 over the concatenated bytes of a kernel's source files (under csrc/, in order)."""
+    h = hashlib.sha256()
+    for s in srcs:
+        h.update(open(os.path.join(ROOT, "block_diffusion_gb300", "csrc", s), "rb").read())
+    return h.hexdigest()
+
+
+def profile_traffic(name: str, srcs):
     """DRAM bytes per launch from the committed ncu summary of kernel `name`, or None when
-    the kernel source changed since the capture (the summary records its sha256)."""
+    the kernel's sources changed since the capture (the summary records their sha256)."""
     path = os.path.join(ROOT, "profiles", f"{name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    digest = source_digest(srcs)
     rec = {}
     for line in text.splitlines():
         line = line.strip().lstrip("-* ")
         if ":" in line and line.startswith(("source_sha256", "traffic_bytes_per_launch")):
             k, v = line.split(":", 1)
-            rec[k.strip()] = v.strip().strip("`")
+            v = v.strip()
+            rec[k.strip()] = v.split("`")[1] if v.startswith("`") else v
     if rec.get("source_sha256") != digest:
         return None
     try:
@@ -1029,10 +1038,14 @@ def headline_parity(bd, a, ci, lm, device):
     return out
 
 
-KERNEL_SOURCES = {"attention": ("attention_config2", "attention.cu"),
-                  "lm_head_commit": ("lm_conf_config2_256rows", "lm_conf.cu"),
-                  "lm_head": ("lm_head_config2_256rows", "lm_head.cu"),
-                  "commit": ("commit_config2", "commit.cu")}
+# kernel -> (ncu summary under profiles/, the source files its device code is compiled from)
+KERNEL_SOURCES = {
+    "attention": ("attention_config2",
+                  ("attention.cu", "attention_common.cuh", "kernels.h", "ptx.cuh")),
+    "lm_head_commit": ("lm_conf_config2_256rows",
+                       ("lm_conf.cu", "lm_common.cuh", "confidence.cuh", "kernels.h", "ptx.cuh")),
+    "lm_head": ("lm_head_config2_256rows", ("lm_head.cu", "lm_common.cuh", "kernels.h", "ptx.cuh")),
+    "commit": ("commit_config2", ("commit.cu", "confidence.cuh", "kernels.h", "ptx.cuh"))}
 
 
 def kernel_roofline(name, alg, ms, peaks):
@@ -1042,8 +1055,7 @@ def kernel_roofline(name, alg, ms, peaks):
     achieved = nbytes / (ms / 1e3) / 1e9
     r = {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-         "traffic": profile_traffic(prof, os.path.join(ROOT, "block_diffusion_gb300", "csrc",
-                                                       src)),
+         "traffic": profile_traffic(prof, src),
          "algorithmic_bytes": nbytes, "ms": ms,
          "peak_source": f"{peaks['source']} (copy bandwidth)"}
     if flops:
