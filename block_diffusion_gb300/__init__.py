@@ -37,7 +37,7 @@ EXPORTS = ("bdlm_block_attention", "bdlm_block_attention_kv", "bdlm_prefill_atte
            "bdlm_lm_head_commit", "bdlm_active_rows", "bdlm_write_block_kv", "bdlm_confidence_commit",
            "bdlm_confidence_commit_rule", "bdlm_apply_commit", "bdlm_round_loop_create",
            "bdlm_round_loop_launch", "bdlm_round_loop_destroy", "bdlm_status_string",
-           "bdlm_device_error", "bdlm_release")
+           "bdlm_device_error", "bdlm_selftest_wait_timeout", "bdlm_release")
 
 
 class AttnDesc(ctypes.Structure):
@@ -114,6 +114,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bdlm_status_string.restype = ctypes.c_char_p
     lib.bdlm_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.bdlm_device_error.restype = I
+    lib.bdlm_selftest_wait_timeout.argtypes = [I, P]
+    lib.bdlm_selftest_wait_timeout.restype = I
     lib.bdlm_release.argtypes = []
     lib.bdlm_release.restype = I
     _lib = lib
@@ -284,6 +286,11 @@ def bdlm_device_error() -> int:
     v = ctypes.c_int(0)
     _check("bdlm_device_error", lib.bdlm_device_error(ctypes.byref(v)))
     return int(v.value)
+
+
+def bdlm_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    _check("bdlm_selftest_wait_timeout",
+           load_library().bdlm_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def bdlm_release() -> None:

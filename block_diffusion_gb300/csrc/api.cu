@@ -185,6 +185,18 @@ int bdlm_device_error(int* bits_out) {
   return BDLM_OK;
 }
 
+int bdlm_selftest_wait_timeout(int limit_us, bdlm_stream stream) {
+  if (limit_us < 1 || limit_us > 2000000) return BDLM_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  const int rc = current_device(&st);
+  if (rc) return rc;
+  const cudaError_t e = bdlm::launch_wait_timeout(
+      st->err, static_cast<unsigned long long>(limit_us) * 1000ull,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BDLM_OK : BDLM_ERR_CUDA;
+}
+
 int bdlm_release(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* st = nullptr;

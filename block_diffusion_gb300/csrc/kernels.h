@@ -188,6 +188,8 @@ cudaError_t launch_record_step(const int* step, int n_steps, int R, const int32_
                                const float* conf, const uint8_t* commit, int32_t* tok_s,
                                float* conf_s, uint8_t* commit_s, const uint4* out, uint4* out_s,
                                long long out_vec, cudaStream_t stream);
+// One CTA whose bounded wait runs out after limit_ns, recorded as BDLM_DEVERR_TIMEOUT in *err.
+cudaError_t launch_wait_timeout(int* err, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_loop_condition(cudaGraphConditionalHandle handle, const uint8_t* mask, int R,
                                   int* step, int n_steps, int* steps_done, cudaStream_t stream);
 cudaError_t launch_active_rows(const uint8_t* mask, const uint8_t* denoising, int B, int L,

@@ -62,10 +62,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete.  Gives up after kWaitLimitNs, or as soon
-// as another thread of the CTA has given up (*abort != 0); returns false then, after
-// setting *abort.  Callers stop issuing work once a wait has failed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Waits for phase `parity` of `bar` to complete.  Gives up after limit_ns (kWaitLimitNs unless
+// given), or as soon as another thread of the CTA has given up (*abort != 0); returns false
+// then, after setting *abort.  Callers stop issuing work once a wait has failed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -73,7 +74,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }

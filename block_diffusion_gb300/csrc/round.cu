@@ -160,6 +160,25 @@ cudaError_t launch_select_step(const StepCopy& c, const int* step, int n_steps,
   return launch_pdl(select_step_kernel, dim3(grid), dim3(256), 0, stream, c, step, n_steps);
 }
 
+namespace {
+// One thread waits, through the kernels' bounded wait, on an mbarrier that nothing arrives on,
+// and records the timeout in the device error word as a kernel's failed wait does.
+__global__ void wait_timeout_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  abort_flag = 0;
+  if (!mbar_wait(&bar, 0, &abort_flag, limit_ns)) atomicOr(err, BDLM_DEVERR_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout(int* err, unsigned long long limit_ns, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_record_step(const int* step, int n_steps, int R, const int32_t* tok,
                                const float* conf, const uint8_t* commit, int32_t* tok_s,
                                float* conf_s, uint8_t* commit_s, const uint4* out, uint4* out_s,

@@ -400,6 +400,17 @@ const char* bdlm_status_string(int status);
  */
 int bdlm_device_error(int* bits_out);
 
+/*
+ * Self-test of the failure path every kernel shares: launches one CTA whose thread waits,
+ * through the same bounded wait the kernels use, on an mbarrier that nothing ever arrives on.
+ * The wait gives up after limit_us microseconds (1 .. 2,000,000) and the kernel records
+ * BDLM_DEVERR_TIMEOUT in the device error word, as a kernel whose wait runs out does; it
+ * faults nothing, so the context stays usable and bdlm_device_error() then reports the bit.
+ * Asynchronous on `stream`.  Returns BDLM_OK, BDLM_ERR_INVALID for a limit out of range, or
+ * an error of the device setup.
+ */
+int bdlm_selftest_wait_timeout(int limit_us, bdlm_stream stream);
+
 /* Frees the workspace of the current device.  The device must be idle. */
 int bdlm_release(void);
 

@@ -106,3 +106,8 @@ def test_host_side_validation_rejects_bad_arguments(so):
                                   None, None) == 0
     assert so.bdlm_confidence_commit_rule(P, P, 0, 4, 10, 4, 1, 2.0, 1.0, P, P, None, P,
                                           None) == 0
+
+
+def test_selftest_wait_limit_is_validated(so):
+    assert so.bdlm_selftest_wait_timeout(0, None) == -1
+    assert so.bdlm_selftest_wait_timeout(2000001, None) == -1
