@@ -1251,32 +1251,63 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 }
 
 
-// Sequences by decreasing KV length (ties: lower index first), for the whole-sequence mode:
-// the persistent attention CTAs take the longest items first, so the last items handed out
-// are the shortest and the CTAs finish close together without cutting sequences into
-// splits.  One CTA; B <= blockDim.x.
+// Sequences by decreasing KV length, for the whole-sequence mode: the persistent attention CTAs
+// take the longest items first, so the last items handed out are the shortest and the CTAs
+// finish close together without cutting sequences into splits.  A counting sort: in this mode a
+// sequence fits the page-id staging buffer, so its KV length is at most kMaxItemPages * kPage
+// tokens.  One CTA (B <= blockDim.x = kMaxOrderSeqs): every sequence counts its length, a scan
+// of the counts from the longest length down gives each length's first slot, and each sequence
+// takes a slot in its length's range (equal lengths in no particular order).
+constexpr int kOrderBuckets = kMaxItemPages * kPage + 1;   // KV lengths 0 .. 2048
+constexpr int kOrderPerThread = (kOrderBuckets + kMaxOrderSeqs - 1) / kMaxOrderSeqs;
+
 __global__ void __launch_bounds__(kMaxOrderSeqs)
 attn_order_kernel(const int32_t* __restrict__ prefix_lens, int B, int L, long long max_tok,
                   int* __restrict__ order) {
-  __shared__ long long s_len[kMaxOrderSeqs];
+  __shared__ int s_cnt[kOrderBuckets];
+  __shared__ int s_warp[kMaxOrderSeqs / 32];
   griddep_wait();
   griddep_launch_dependents();
-  const int b = threadIdx.x;
-  long long len = 0;
-  if (b < B) {
-    const int prefix = prefix_lens[b];
-    len = static_cast<long long>(prefix < 0 ? 0 : prefix) + L;
-    if (len > max_tok) len = max_tok;
-    s_len[b] = len;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int i = t; i < kOrderBuckets; i += kMaxOrderSeqs) s_cnt[i] = 0;
+  __syncthreads();
+  int len = 0, pos = 0;
+  if (t < B) {
+    const int prefix = prefix_lens[t];
+    long long l = static_cast<long long>(prefix < 0 ? 0 : prefix) + L;
+    if (l > max_tok) l = max_tok;
+    if (l > kOrderBuckets - 1) l = kOrderBuckets - 1;   // not reached: max_tok <= 2048 here
+    len = static_cast<int>(l);
+    pos = atomicAdd(&s_cnt[len], 1);
   }
   __syncthreads();
-  if (b >= B) return;
-  int rank = 0;
-  for (int j = 0; j < B; ++j) {
-    const long long lj = s_len[j];
-    rank += (lj > len) || (lj == len && j < b);
+  // thread t owns the kOrderPerThread lengths just below kOrderBuckets - 1 - t * kOrderPerThread
+  int cnt[kOrderPerThread], sum = 0;
+#pragma unroll
+  for (int k = 0; k < kOrderPerThread; ++k) {
+    const int bucket = kOrderBuckets - 1 - (t * kOrderPerThread + k);
+    cnt[k] = bucket >= 0 ? s_cnt[bucket] : 0;
+    sum += cnt[k];
   }
-  order[rank] = b;
+  int incl = sum;   // inclusive scan over the threads (longest lengths first)
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  int start = before + incl - sum;   // sequences longer than this thread's lengths
+#pragma unroll
+  for (int k = 0; k < kOrderPerThread; ++k) {
+    const int bucket = kOrderBuckets - 1 - (t * kOrderPerThread + k);
+    if (bucket >= 0) s_cnt[bucket] = start;
+    start += cnt[k];
+  }
+  __syncthreads();
+  if (t < B) order[s_cnt[len] + pos] = t;
 }
 
 // Merges the splits of every (sequence, KV head, row group) whose KV range was cut into more
