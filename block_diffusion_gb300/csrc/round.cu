@@ -53,39 +53,60 @@ active_rows_kernel(const uint8_t* __restrict__ mask, const uint8_t* __restrict__
 }
 
 // k_new, v_new [B, L, Hkv, D=128] -> the cache slots prefix_len .. prefix_len + L - 1 of each
-// sequence.  One warp per (b, i, kvh) row of 128 bf16 (256 B, 8 B per lane).  Page ids and
+// sequence.  A token's Hkv * D values are contiguous both in k_new / v_new and in its page slot
+// ([page, slot, Hkv, D]), so one warp per token row (b, i) copies two contiguous runs of
+// Hkv * 256 bytes in 16-byte vectors, all of a pass's loads before its stores.  Page ids and
 // lengths are checked; a bad one skips the row and sets the device error word.
-__global__ void write_block_kv_kernel(const uint16_t* __restrict__ k_new,
-                                      const uint16_t* __restrict__ v_new,
-                                      uint16_t* __restrict__ k_pages, uint16_t* __restrict__ v_pages,
-                                      const int32_t* __restrict__ page_table,
-                                      const int32_t* __restrict__ prefix_lens, int B, int L,
-                                      int Hkv, int max_pages, int num_pages, int* err) {
+constexpr int kKvWarps = 8;      // token rows per CTA
+constexpr int kKvVecLane = 4;    // 16-byte vectors per lane and tensor in one pass
+__global__ void __launch_bounds__(kKvWarps * 32)
+write_block_kv_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                      uint16_t* __restrict__ k_pages, uint16_t* __restrict__ v_pages,
+                      const int32_t* __restrict__ page_table,
+                      const int32_t* __restrict__ prefix_lens, int B, int L, int Hkv,
+                      int max_pages, int num_pages, int* err) {
   griddep_wait();
   griddep_launch_dependents();
-  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int t = blockIdx.x * kKvWarps + (threadIdx.x >> 5);  // token row b * L + i
   const int lane = threadIdx.x & 31;
-  const long long rows = static_cast<long long>(B) * L * Hkv;
-  if (row >= rows) return;
-  const int kvh = static_cast<int>(row % Hkv);
-  const long long bi = row / Hkv;
-  const int i = static_cast<int>(bi % L);
-  const int b = static_cast<int>(bi / L);
+  if (t >= B * L) return;
+  const int b = t / L, i = t - b * L;
   const int prefix = prefix_lens[b];
-  const long long tok = static_cast<long long>(prefix) + i;
   if (prefix < 0 || static_cast<long long>(prefix) + L > static_cast<long long>(max_pages) * 16) {
-    if (lane == 0 && i == 0 && kvh == 0) atomicOr(err, BDLM_DEVERR_LENGTH);
+    if (lane == 0 && i == 0) atomicOr(err, BDLM_DEVERR_LENGTH);
     return;
   }
+  const int tok = prefix + i;
   const int page = page_table[static_cast<size_t>(b) * max_pages + tok / 16];
   if (page < 0 || page >= num_pages) {
-    if (lane == 0 && kvh == 0) atomicOr(err, BDLM_DEVERR_PAGE);
+    if (lane == 0) atomicOr(err, BDLM_DEVERR_PAGE);
     return;
   }
-  const size_t src = static_cast<size_t>(row) * 128;
-  const size_t dst = ((static_cast<size_t>(page) * 16 + tok % 16) * Hkv + kvh) * 128;
-  reinterpret_cast<uint2*>(k_pages + dst)[lane] = reinterpret_cast<const uint2*>(k_new + src)[lane];
-  reinterpret_cast<uint2*>(v_pages + dst)[lane] = reinterpret_cast<const uint2*>(v_new + src)[lane];
+  const int nvec = Hkv * 16;  // 16-byte vectors in a token row
+  const uint4* ks = reinterpret_cast<const uint4*>(k_new) + static_cast<size_t>(t) * nvec;
+  const uint4* vs = reinterpret_cast<const uint4*>(v_new) + static_cast<size_t>(t) * nvec;
+  const size_t slot = static_cast<size_t>(page) * 16 + tok % 16;
+  uint4* kd = reinterpret_cast<uint4*>(k_pages) + slot * nvec;
+  uint4* vd = reinterpret_cast<uint4*>(v_pages) + slot * nvec;
+  for (int v0 = 0; v0 < nvec; v0 += 32 * kKvVecLane) {
+    uint4 kr[kKvVecLane], vr[kKvVecLane];
+#pragma unroll
+    for (int q = 0; q < kKvVecLane; ++q) {
+      const int v = v0 + q * 32 + lane;
+      if (v < nvec) {
+        kr[q] = ks[v];
+        vr[q] = vs[v];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kKvVecLane; ++q) {
+      const int v = v0 + q * 32 + lane;
+      if (v < nvec) {
+        kd[v] = kr[q];
+        vd[v] = vr[q];
+      }
+    }
+  }
 }
 
 // Copies step *step's slice of up to four per-step inputs into their working buffers.
@@ -209,9 +230,9 @@ cudaError_t launch_write_block_kv(const uint16_t* k_new, const uint16_t* v_new, 
                                   uint16_t* v_pages, const int32_t* page_table,
                                   const int32_t* prefix_lens, int B, int L, int Hkv,
                                   int max_pages, int num_pages, int* err, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(B) * L * Hkv;
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
-  return launch_pdl(write_block_kv_kernel, dim3(grid), dim3(256), 0, stream, k_new, v_new,
+  const long long rows = static_cast<long long>(B) * L;  // token rows (callers keep it < 2^31)
+  const unsigned grid = static_cast<unsigned>((rows + kKvWarps - 1) / kKvWarps);
+  return launch_pdl(write_block_kv_kernel, dim3(grid), dim3(kKvWarps * 32), 0, stream, k_new, v_new,
                     k_pages, v_pages, page_table, prefix_lens, B, L, Hkv, max_pages, num_pages,
                     err);
 }

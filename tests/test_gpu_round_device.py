@@ -74,7 +74,7 @@ def test_lm_head_device_count_zero(lib):
     assert torch.all(torch.isnan(logits))
 
 
-@pytest.mark.parametrize("B,L,Hkv", [(5, 4, 8), (3, 16, 2), (2, 64, 1)])
+@pytest.mark.parametrize("B,L,Hkv", [(5, 4, 8), (3, 16, 2), (2, 64, 1), (4, 7, 3), (3, 64, 16)])
 def test_write_block_kv(lib, B, L, Hkv):
     import torch
     rng = np.random.default_rng(B * 100 + L)
