@@ -69,7 +69,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ uint64_t bar_oready, bar_ofull[2], bar_done;  // bar_ofull: PV of chunk u, by parity
   __shared__ uint64_t bar_ifull[kItemRing], bar_iempty[kItemRing];
   __shared__ Item s_item[kItemRing];
-  __shared__ int s_pid[3][kMaxItemPages];
+  __shared__ int s_pid[3][ROWS ? kMaxItemPagesRows : kMaxItemPages];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   constexpr int kCols = ROWS ? 1 : N;   // per-column state of the transposed softmax
@@ -1358,7 +1358,8 @@ attn_merge_kernel(const AttnParams p, int N) {
   const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
   long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
   if (kvl > max_tok) kvl = max_tok;
-  const int ns = static_cast<int>((kvl + p.split_tokens - 1) / p.split_tokens);
+  const int per = split_len(static_cast<int>(kvl), p);
+  const int ns = static_cast<int>((kvl + per - 1) / per);
   if (ns <= 1) return;
   float4 acc[kMergeRows];
 #pragma unroll
@@ -1531,6 +1532,12 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
   const int chunks_per_split = pl.n_mma == 16 ? 1 : pl.n_mma == 32 ? 3 : 16;
   pl.split_tokens = pl.chunk_tiles * kTile * chunks_per_split;
   if (pl.split_tokens > kMaxSplitTokens) pl.split_tokens = kMaxSplitTokens;
+  if (pl.n_mma >= 128) {
+    // rows on M: every item reloads its Q and writes a partial, so splits are long and cut
+    // evenly (no short remainder split pays those costs for a tile or two)
+    pl.even = true;
+    pl.split_tokens = pl.n_mma == 256 ? kSplitTokensTwo : kSplitTokensRows;
+  }
   const long long max_tok = static_cast<long long>(max_pages) * kPage;
   const size_t groups = static_cast<size_t>(B) * Hkv * pl.row_groups;
   const long long ctas = static_cast<long long>(num_sms) * ctas_per_sm;
@@ -1583,6 +1590,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   prm.row_groups = plan.row_groups;
   prm.rows_per_group = plan.G * plan.lsub;
   prm.split_tokens = plan.split_tokens;
+  prm.even_splits = plan.even ? 1 : 0;
   prm.max_splits = plan.max_splits;
   prm.chunk_tiles = plan.chunk_tiles;
   prm.scale_log2 = sm_scale * 1.4426950408889634f;

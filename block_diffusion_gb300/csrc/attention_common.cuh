@@ -31,9 +31,18 @@ __host__ __device__ constexpr int attn_threads(bool rows, bool two) {
 constexpr int kMaxSplitTokens = 2048;
 // Page ids staged per item: a split of up to kMaxSplitTokens, or a whole sequence of up to
 // kMaxItemPages pages when sequences are processed whole (two CTAs per SM at N = 16 leave
-// no room for more).
+// no room for more).  The rows-on-M kernels (one CTA per SM) stage up to kMaxItemPagesRows
+// pages, for splits of up to kMaxSplitTokensRows.
 constexpr int kMaxItemPages = kMaxSplitTokens / kPage;
 static_assert(kMaxItemPages >= kMaxSplitTokens / kPage, "a split must fit the page-id buffer");
+constexpr int kMaxSplitTokensRows = 8192;
+constexpr int kMaxItemPagesRows = kMaxSplitTokensRows / kPage;
+// Longest KV split of the rows-on-M kernels: one 128-row sub-group, two sub-groups.
+constexpr int kSplitTokensRows = 3072;
+constexpr int kSplitTokensTwo = 4096;
+static_assert(kSplitTokensRows <= kMaxSplitTokensRows && kSplitTokensTwo <= kMaxSplitTokensRows &&
+                  kSplitTokensRows % kTile == 0 && kSplitTokensTwo % kTile == 0,
+              "a split is whole tiles and fits the page-id buffer");
 // Whole sequences, longest first, replace KV splits when there are at least this many
 // (sequence, KV head, row group) items per CTA and up to kMaxOrderSeqs sequences.
 constexpr int kWholeItemsPerCta = 2;
@@ -62,6 +71,7 @@ struct AttnParams {
   int B, L, Hq, Hkv, G, max_pages, num_pages;
   int table_div;     // sequence b uses page-table row b / table_div (prompt blocks share a row)
   int lsub, row_groups, rows_per_group, split_tokens, max_splits, chunk_tiles;
+  int even_splits;   // cut each sequence into equal splits of at most split_tokens
   int total_items;
   int mask_block;    // > 0: query i of a sequence sees keys < prefix + (i / mask_block + 1) * mask_block
   float scale_log2;  // sm_scale * log2(e)
@@ -92,6 +102,16 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   mbar_wait(bar, parity, &dummy);
 }
 
+// KV tokens per split of a sequence of kv_len tokens: split_tokens, or with even splits the
+// sequence cut into as many splits as split_tokens needs, of equal length rounded up to whole
+// tiles (at most split_tokens, so a split still fits the page-id buffer; the last one takes
+// what is left), so that no split is a short remainder.
+__device__ __forceinline__ int split_len(int kv_len, const AttnParams& p) {
+  if (!p.even_splits || kv_len <= 0) return p.split_tokens;
+  const int ns = (kv_len + p.split_tokens - 1) / p.split_tokens;
+  return ((kv_len + ns - 1) / ns + kTile - 1) / kTile * kTile;
+}
+
 // Item index -> work item; items are enumerated split-major so that the short last splits
 // of long sequences come at the end of the schedule.  Returns false for an empty split.
 __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& it) {
@@ -107,11 +127,12 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
   if (kvl > max_tok) kvl = max_tok;
   const int kv_len = static_cast<int>(kvl);
-  it.t_begin = it.split * p.split_tokens;
+  const int per = split_len(kv_len, p);
+  it.t_begin = it.split * per;
   if (it.t_begin >= kv_len) return false;
   it.q0 = kv_len - p.L;
-  it.t_end = min(kv_len, it.t_begin + p.split_tokens);
-  it.n_splits = (kv_len + p.split_tokens - 1) / p.split_tokens;
+  it.t_end = min(kv_len, it.t_begin + per);
+  it.n_splits = (kv_len + per - 1) / per;
   it.n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
   it.n_chunks = (it.n_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
   it.end = 0;

@@ -88,6 +88,7 @@ struct AttnPlan {
   int chunk_tiles = 1;   // 128-token tiles per S chunk held in tensor memory
   int tmem_cols = 0;     // tensor-memory columns allocated per CTA
   bool whole = false;    // whole sequences, longest first, instead of KV splits
+  bool even = false;     // each sequence cut into equal splits of at most split_tokens
   size_t smem_bytes = 0;
   size_t part_bytes = 0, cnt_bytes = 0;
 };

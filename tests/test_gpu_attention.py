@@ -68,7 +68,7 @@ def test_multiple_splits_and_chunks(lib, L, prefix):
 
 
 @pytest.mark.parametrize("L,Hq,B,prefix", [(4, 32, 96, (100, 1900)), (8, 32, 160, (0, 1200)),
-                                          (4, 16, 200, (3000, 4100))])
+                                          (4, 16, 200, (3000, 4100)), (4, 32, 96, (2044, 2044))])
 def test_whole_sequences_longest_first(lib, L, Hq, B, prefix):
     """Enough (sequence, KV head) items for whole sequences, longest first, with no KV
     splits: items of several tensor-memory chunks, sequences of equal length (ties in the
@@ -187,6 +187,7 @@ def test_prefill_chunk_across_a_split_boundary(lib):
     (3, 33, 16, 2, (0, 500)),      # 264 rows: row groups of 256 and 8
     (2, 64, 32, 8, (2040, 4200)),  # KV splits, ragged last tiles
     (40, 64, 32, 8, (0, 1500)),    # enough items for whole sequences, longest first
+    (40, 64, 32, 8, (1984, 1984)),  # whole sequences, every one of the longest length taken
     (3, 50, 24, 8, (0, 700)),      # 3 query heads per KV head: 150 rows
 ])
 def test_256_row_groups(lib, B, L, Hq, Hkv, prefix):
