@@ -1251,19 +1251,21 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 }
 
 
-// Sequences by decreasing KV length, for the whole-sequence mode: the persistent attention CTAs
-// take the longest items first, so the last items handed out are the shortest and the CTAs
-// finish close together without cutting sequences into splits.  A counting sort: in this mode a
-// sequence fits the page-id staging buffer, so its KV length is at most kMaxItemPages * kPage
-// tokens.  One CTA (B <= blockDim.x = kMaxOrderSeqs): every sequence counts its length, a scan
-// of the counts from the longest length down gives each length's first slot, and each sequence
-// takes a slot in its length's range (equal lengths in no particular order).
-constexpr int kOrderBuckets = kMaxItemPages * kPage + 1;   // KV lengths 0 .. 2048
+// Sequences by decreasing item length, so that the persistent attention CTAs take the longest
+// items first and the last items handed out are the shortest: the CTAs then finish close
+// together.  Whole-sequence mode ranks by KV length (a sequence fits the page-id staging buffer
+// there, so at most kMaxItemPages * kPage tokens); with even KV splits, by the length of the
+// sequence's splits in tiles (at most kMaxSplitTokensRows / kTile), and the items then go out
+// sequence by sequence in that order, all splits of one before the next.  A counting sort in
+// one CTA (B <= blockDim.x = kMaxOrderSeqs): every sequence counts its key, a scan of the
+// counts from the largest key down gives each key's first slot, and each sequence takes a slot
+// in its key's range (equal keys in no particular order).
+constexpr int kOrderBuckets = kMaxItemPages * kPage + 1;   // keys 0 .. 2048
 constexpr int kOrderPerThread = (kOrderBuckets + kMaxOrderSeqs - 1) / kMaxOrderSeqs;
+static_assert(kMaxSplitTokensRows / kTile < kOrderBuckets, "split lengths in tiles fit the keys");
 
 __global__ void __launch_bounds__(kMaxOrderSeqs)
-attn_order_kernel(const int32_t* __restrict__ prefix_lens, int B, int L, long long max_tok,
-                  int* __restrict__ order) {
+attn_order_kernel(const AttnParams p, bool whole, int* __restrict__ order) {
   __shared__ int s_cnt[kOrderBuckets];
   __shared__ int s_warp[kMaxOrderSeqs / 32];
   griddep_wait();
@@ -1272,11 +1274,13 @@ attn_order_kernel(const int32_t* __restrict__ prefix_lens, int B, int L, long lo
   for (int i = t; i < kOrderBuckets; i += kMaxOrderSeqs) s_cnt[i] = 0;
   __syncthreads();
   int len = 0, pos = 0;
-  if (t < B) {
-    const int prefix = prefix_lens[t];
-    long long l = static_cast<long long>(prefix < 0 ? 0 : prefix) + L;
+  if (t < p.B) {
+    const int prefix = p.prefix_lens[t];
+    const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
+    long long l = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;
     if (l > max_tok) l = max_tok;
-    if (l > kOrderBuckets - 1) l = kOrderBuckets - 1;   // not reached: max_tok <= 2048 here
+    if (!whole) l = split_len(static_cast<int>(l), p) / kTile;
+    if (l > kOrderBuckets - 1) l = kOrderBuckets - 1;   // not reached (see above)
     len = static_cast<int>(l);
     pos = atomicAdd(&s_cnt[len], 1);
   }
@@ -1307,7 +1311,7 @@ attn_order_kernel(const int32_t* __restrict__ prefix_lens, int B, int L, long lo
     start += cnt[k];
   }
   __syncthreads();
-  if (t < B) order[s_cnt[len] + pos] = t;
+  if (t < p.B) order[s_cnt[len] + pos] = t;
 }
 
 // Merges the splits of every (sequence, KV head, row group) whose KV range was cut into more
@@ -1545,6 +1549,7 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
              static_cast<long long>(groups) >= kWholeItemsPerCta * ctas;
   if (pl.whole) {
     // every item is a whole sequence: no partials, no merge; the workspace holds the order
+    pl.even = false;
     pl.split_tokens = static_cast<int>((max_tok + kTile - 1) / kTile * kTile);
     pl.max_splits = 1;
     pl.part_bytes = static_cast<size_t>(B) * sizeof(int);
@@ -1553,6 +1558,12 @@ AttnPlan plan_attention(int B, int L, int Hq, int Hkv, int max_pages, int page_s
   }
   pl.max_splits = static_cast<int>((max_tok + pl.split_tokens - 1) / pl.split_tokens);
   pl.part_bytes = groups * pl.max_splits * static_cast<size_t>(pl.n_mma) * 130 * sizeof(float);
+  if (pl.even && B <= kMaxOrderSeqs) {
+    // items longest first: the sequence order goes after the partials
+    pl.ranked = true;
+    pl.order_offset = pl.part_bytes;
+    pl.part_bytes += static_cast<size_t>(B) * sizeof(int);
+  }
   pl.cnt_bytes = 2 * sizeof(int);  // the scheduler's next-item and finished-CTA counters
   return pl;
 }
@@ -1597,14 +1608,21 @@ cudaError_t launch_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   const long long items = static_cast<long long>(B) * Hkv * plan.max_splits * plan.row_groups;
   if (items > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   prm.total_items = static_cast<int>(items);
+  prm.rank_major = 0;
   cudaError_t e;
   if (plan.whole) {
     int* order = reinterpret_cast<int*>(part);
-    e = launch_pdl(attn_order_kernel, dim3(1), dim3(kMaxOrderSeqs), 0, stream, prefix_lens, B, L,
-                   static_cast<long long>(max_pages) * kPage, order);
+    e = launch_pdl(attn_order_kernel, dim3(1), dim3(kMaxOrderSeqs), 0, stream, prm, true, order);
     if (e != cudaSuccess) return e;
     prm.order = order;
     prm.part = nullptr;
+  } else if (plan.ranked) {
+    // even splits, sequences by decreasing split length: the order follows the partials
+    int* order = reinterpret_cast<int*>(reinterpret_cast<char*>(part) + plan.order_offset);
+    e = launch_pdl(attn_order_kernel, dim3(1), dim3(kMaxOrderSeqs), 0, stream, prm, false, order);
+    if (e != cudaSuccess) return e;
+    prm.order = order;
+    prm.rank_major = 1;
   }
   switch (plan.n_mma) {
     case 16:

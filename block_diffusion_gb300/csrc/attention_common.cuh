@@ -72,6 +72,7 @@ struct AttnParams {
   int table_div;     // sequence b uses page-table row b / table_div (prompt blocks share a row)
   int lsub, row_groups, rows_per_group, split_tokens, max_splits, chunk_tiles;
   int even_splits;   // cut each sequence into equal splits of at most split_tokens
+  int rank_major;    // items sequence by sequence in `order`, all splits of one together
   int total_items;
   int mask_block;    // > 0: query i of a sequence sees keys < prefix + (i / mask_block + 1) * mask_block
   float scale_log2;  // sm_scale * log2(e)
@@ -113,15 +114,22 @@ __device__ __forceinline__ int split_len(int kv_len, const AttnParams& p) {
 }
 
 // Item index -> work item; items are enumerated split-major so that the short last splits
-// of long sequences come at the end of the schedule.  Returns false for an empty split.
+// of long sequences come at the end of the schedule, or (rank_major) sequence by sequence in
+// the order of `order`.  Returns false for an empty split.
 __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& it) {
   it.rg = idx % p.row_groups;
   idx /= p.row_groups;
   it.kvh = idx % p.Hkv;
   idx /= p.Hkv;
-  it.b = idx % p.B;
-  it.split = idx / p.B;
-  if (p.order) it.b = __ldg(p.order + it.b);  // whole sequences, longest first
+  if (p.rank_major) {
+    // even splits, sequences by decreasing split length, all splits of one together
+    it.split = idx % p.max_splits;
+    it.b = __ldg(p.order + idx / p.max_splits);
+  } else {
+    it.b = idx % p.B;
+    it.split = idx / p.B;
+    if (p.order) it.b = __ldg(p.order + it.b);  // whole sequences, longest first
+  }
   const int prefix = p.prefix_lens[it.b];
   const long long max_tok = static_cast<long long>(p.max_pages) * kPage;
   long long kvl = static_cast<long long>(prefix < 0 ? 0 : prefix) + p.L;

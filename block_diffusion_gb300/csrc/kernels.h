@@ -89,6 +89,8 @@ struct AttnPlan {
   int tmem_cols = 0;     // tensor-memory columns allocated per CTA
   bool whole = false;    // whole sequences, longest first, instead of KV splits
   bool even = false;     // each sequence cut into equal splits of at most split_tokens
+  bool ranked = false;   // even splits handed out sequence by sequence, longest splits first
+  size_t order_offset = 0;   // ranked: byte offset of the sequence order in the workspace
   size_t smem_bytes = 0;
   size_t part_bytes = 0, cnt_bytes = 0;
 };
