@@ -77,6 +77,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   __shared__ int s_need[2];   // chunk u (parity): some column's max rose enough to rescale O^T
   __shared__ int s_pflag[2];  // P buffer: its tile starts a chunk whose PV waits for a rescale
   __shared__ float s_red[4][kCols];
+  // rows on M: a 1 KB staging buffer per softmax warp for the epilogue's global stores
+  __shared__ __align__(16) uint8_t
+      s_stage[ROWS ? attn_softmax_threads(ROWS, TWO) / 32 : 1][ROWS ? 1024 : 16];
   // the two halves of a row exchange maxima and sums, by exchange parity and sub-group; their
   // mbarriers are per (sub-group, lane quadrant)
   __shared__ float s_hmax[ROWS ? 2 : 1][TWO ? 2 : 1][2][ROWS ? N : 1];
@@ -809,30 +812,36 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                                         static_cast<size_t>(it.kvh) * p.G + r_item % p.G) * 128 + col0
                              : p.out;
         const float inv = 1.f / l_row;
+        uint8_t* stage = s_stage[warp - 2];
+        if (it.n_splits == 1) {
+          // this half of the row as bf16: 128 bytes per lane
+          uint32_t w[32];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t o[16];
-          tmem_ld16(tOx + g * 16, o);
-          tmem_wait_ld();
-          tmem_regs_ready(o);
-          if (!live) continue;
-          if (it.n_splits == 1) {
-            uint32_t w[8];
+          for (int g = 0; g < 4; ++g) {
+            uint32_t o[16];
+            tmem_ld16(tOx + g * 16, o);
+            tmem_wait_ld();
+            tmem_regs_ready(o);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[2 * k]) * inv,
                                                               __uint_as_float(o[2 * k + 1]) * inv);
-              w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+              w[8 * g + k] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + g * 16);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else {
-            float4* d4 = reinterpret_cast<float4*>(mine + r_item * 128 + col0 + g * 16);
+          }
+          store_rows_128b(w, live ? dst : nullptr, stage, lane);
+        } else {
+          // fp32 partial: 32 columns (128 bytes) per lane at a time
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                  __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+          for (int g2 = 0; g2 < 2; ++g2) {
+            uint32_t o[32];
+            tmem_ld16(tOx + g2 * 32, *reinterpret_cast<uint32_t(*)[16]>(o));
+            tmem_ld16(tOx + g2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+            tmem_wait_ld();
+            tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(o));
+            tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(o + 16));
+            store_rows_128b(o, live ? mine + r_item * 128 + col0 + g2 * 32 : nullptr, stage,
+                            lane);
           }
         }
         if (live && it.n_splits > 1 && half == 0) {
@@ -991,30 +1000,37 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                               static_cast<size_t>(it.kvh) * p.G + r_item % p.G) * 128 + col0
                    : p.out;
           const float inv = 1.f / l_row;
+          uint8_t* stage = s_stage[warp - 2];
+          const uint32_t tOr = tO + lane_off + x * N + col0;
+          if (it.n_splits == 1) {
+            // this half of the row as bf16: 128 bytes per lane
+            uint32_t w[32];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t o[16];
-            tmem_ld16(tO + lane_off + x * N + col0 + g * 16, o);
-            tmem_wait_ld();
-            tmem_regs_ready(o);
-            if (!live) continue;
-            if (it.n_splits == 1) {
-              uint32_t w[8];
+            for (int g = 0; g < 4; ++g) {
+              uint32_t o[16];
+              tmem_ld16(tOr + g * 16, o);
+              tmem_wait_ld();
+              tmem_regs_ready(o);
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(
                     __uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
-                w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+                w[8 * g + k] = *reinterpret_cast<const uint32_t*>(&h2);
               }
-              uint4* d4 = reinterpret_cast<uint4*>(dst + g * 16);
-              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            } else {
-              float4* d4 = reinterpret_cast<float4*>(mine + r_item * 128 + col0 + g * 16);
+            }
+            store_rows_128b(w, live ? dst : nullptr, stage, lane);
+          } else {
+            // fp32 partial: 32 columns (128 bytes) per lane at a time
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                d4[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                    __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+            for (int g2 = 0; g2 < 2; ++g2) {
+              uint32_t o[32];
+              tmem_ld16(tOr + g2 * 32, *reinterpret_cast<uint32_t(*)[16]>(o));
+              tmem_ld16(tOr + g2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+              tmem_wait_ld();
+              tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(o));
+              tmem_regs_ready(*reinterpret_cast<uint32_t(*)[16]>(o + 16));
+              store_rows_128b(o, live ? mine + r_item * 128 + col0 + g2 * 32 : nullptr, stage,
+                              lane);
             }
           }
           if (live && it.n_splits > 1 && half == 0) {

@@ -151,6 +151,35 @@ __device__ __forceinline__ bool decode_item(int idx, const AttnParams& p, Item& 
   return true;
 }
 
+// Writes 128 bytes per lane to global memory (lane l: w, the 32 words of its row piece; dst,
+// where they go, or null for nothing) through a 1 KB shared-memory staging buffer, 8 rows at a
+// time, so that each global store instruction writes four whole 128-byte row pieces instead of
+// 16 bytes of each of 32 rows.  Chunk c of staged row r sits at 16 * (c ^ r) within the row, so
+// neither the writes of 8 rows nor the reads fall on one bank.  Whole warp.
+__device__ __forceinline__ void store_rows_128b(const uint32_t (&w)[32], void* dst,
+                                                uint8_t* stage, int lane) {
+  const unsigned long long dptr = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int p8 = 0; p8 < 4; ++p8) {
+    if ((lane >> 3) == p8) {
+      const int r = lane & 7;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ r) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = (lane >> 3) + 4 * h, c = lane & 7;
+      const unsigned long long d = __shfl_sync(0xffffffffu, dptr, p8 * 8 + r);
+      const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 128 + ((c ^ r) << 4));
+      if (d) reinterpret_cast<uint4*>(d)[c] = v;
+    }
+    __syncwarp();
+  }
+}
+
 // Rows on M, two sub-groups: 32 scores of a half-row (keys base .. base + 31 of its 64).
 // FULL: all of them are keys the row sees; otherwise keys at or past nvalid read as -inf.
 template <bool FULL>
