@@ -67,6 +67,20 @@ def test_multiple_splits_and_chunks(lib, L, prefix):
     check(lib, a)
 
 
+@pytest.mark.parametrize("L,kv", [
+    (64, [64, 4096, 4097, 8192, 8193, 12417, 200]),    # two sub-groups: splits of <= 4096 tokens
+    (32, [3072, 3073, 6144, 6145, 9217, 32, 1000]),     # one sub-group: splits of <= 3072 tokens
+])
+def test_even_splits_longest_first(lib, L, kv):
+    """Query rows on M with KV lengths at and just past multiples of the longest split: every
+    sequence is cut into equal splits of whole tiles, the last one taking what is left, and the
+    items go out sequence by sequence, longest splits first."""
+    rng = np.random.default_rng(L * 3 + len(kv))
+    lens = np.asarray(kv, dtype=np.int64) - L
+    a = W.make_attention(rng, len(kv), L, 32, 8, 128, prefix_lens=lens)
+    check(lib, a)
+
+
 @pytest.mark.parametrize("L,Hq,B,prefix", [(4, 32, 96, (100, 1900)), (8, 32, 160, (0, 1200)),
                                           (4, 16, 200, (3000, 4100)), (4, 32, 96, (2044, 2044))])
 def test_whole_sequences_longest_first(lib, L, Hq, B, prefix):
