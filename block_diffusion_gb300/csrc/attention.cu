@@ -181,7 +181,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // Publishes `it` to the item ring (lane 0).
     auto publish = [&](const Item& it) {
       const int rs = seq % kItemRing;
-      if (ok) ok = mbar_wait(&bar_iempty[rs], ((seq / kItemRing) & 1) ^ 1, &abort_flag);
+      if (ok) ok = mbar_wait<ROWS>(&bar_iempty[rs], ((seq / kItemRing) & 1) ^ 1, &abort_flag);
       s_item[rs] = it;
       mbar_arrive(&bar_ifull[rs]);
     };
@@ -267,7 +267,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int q_loads = 0;
     auto load_q = [&](const Item& it, int s) {
       const int b = s % kQBufs;
-      if (ok) ok = mbar_wait(&bar_qempty[b], ((s / kQBufs) & 1) ^ 1, &abort_flag);
+      if (ok) ok = mbar_wait<ROWS>(&bar_qempty[b], ((s / kQBufs) & 1) ^ 1, &abort_flag);
       if (!ok) return;
       mbar_arrive_expect_tx(&bar_qfull[b], 2u * 128u * static_cast<uint32_t>(p.G * p.lsub));
       for (int h = 0; h < 2; ++h)
@@ -292,7 +292,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           if (!ok) break;
         }
         const int tok0 = it.t_begin + j * kTile;
-        if (lane == 0) ok = mbar_wait(&bar_empty[st], ph ^ 1, &abort_flag);
+        if (lane == 0) ok = mbar_wait<ROWS>(&bar_empty[st], ph ^ 1, &abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const int npg = min(kTile / kPage, (it.t_end - tok0 + kPage - 1) / kPage);
@@ -391,7 +391,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     }
     if constexpr (ROWS) {
       // tell the second issuer that no stage follows (once the next stage is free)
-      if (lane == 0 && ok && mbar_wait(&bar_empty[st], ph ^ 1, &abort_flag)) {
+      if (lane == 0 && ok && mbar_wait<ROWS>(&bar_empty[st], ph ^ 1, &abort_flag)) {
         s_sinfo[st].end = 1;
         mbar_arrive(&bar_sready[st]);
       }
@@ -418,7 +418,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint64_t kv_policy = l2_policy_evict_first();
     int st = 0;
     uint32_t ph = 0;
-    while (mbar_wait_warp(&bar_sready[st], ph, &abort_flag)) {
+    while (mbar_wait_warp<ROWS>(&bar_sready[st], ph, &abort_flag)) {
       const StageInfo& si = s_sinfo[st];
       if (si.end) break;
       if (lane < kTile / kPage) {
@@ -454,9 +454,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       // sub-groups into sub-group x's buffer x (one tile per chunk)
       auto do_s = [&](const Item& it, int c, int u, int seq) {
         if constexpr (!TWO)
-          if (!(ok = ok && mbar_wait(&bar_sfree[u & 1], ((u >> 1) & 1) ^ 1, &abort_flag))) return;
+          if (!(ok = ok && mbar_wait<ROWS>(&bar_sfree[u & 1], ((u >> 1) & 1) ^ 1,
+                                           &abort_flag)))
+            return;
         const int qb = seq % kQBufs;
-        if (c == 0 && !(ok = mbar_wait(&bar_qfull[qb], (seq / kQBufs) & 1, &abort_flag))) return;
+        if (c == 0 && !(ok = mbar_wait<ROWS>(&bar_qfull[qb], (seq / kQBufs) & 1,
+                                             &abort_flag)))
+          return;
         tc_fence_after();
         if (kQTmem && c == 0) {
           // the item's Q into tensor memory, 16 head dims (8 columns) per copy, behind the last
@@ -471,7 +475,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
-          if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
+          if (!(ok = mbar_wait<ROWS>(&bar_full[st], ph, &abort_flag))) return;
           tc_fence_after();
           const uint32_t ka = kv_addr + st * kStageBytes;
           for (int x = 0; x < kSub; ++x) {
@@ -510,7 +514,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         for (int j = j0; j < j1; ++j) {
-          if (!(ok = mbar_wait(&bar_full[st], ph, &abort_flag))) return;
+          if (!(ok = mbar_wait<ROWS>(&bar_full[st], ph, &abort_flag))) return;
           const int tok0 = it.t_begin + j * kTile;
           const int valid = min(kTile, it.t_end - tok0);
           const int npg = (valid + kPage - 1) / kPage;
@@ -529,10 +533,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           for (int x = 0; x < kSub; ++x) {
             const int pb = TWO ? x : pcount % kPBufs;
             const uint32_t pph = TWO ? (u & 1) : ((pcount / kPBufs) & 1);
-            if (!(ok = mbar_wait(&bar_pfull[pb], pph, &abort_flag))) return;
+            if (!(ok = mbar_wait<ROWS>(&bar_pfull[pb], pph, &abort_flag))) return;
             if constexpr (!ROWS) {
               if (c > 0 && j == j0 && s_pflag[pb]) {  // the softmax rescales O^T first
-                if (!(ok = mbar_wait(&bar_oready, ocount & 1, &abort_flag))) return;
+                if (!(ok = mbar_wait<ROWS>(&bar_oready, ocount & 1, &abort_flag))) return;
                 ++ocount;
               }
             }
@@ -590,7 +594,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       auto do_pv_s = [&](const Item& it, int c, int u, const Item& nx, int nc, int nseq,
                          bool has_next) {
         const int stv = st;
-        if (!(ok = mbar_wait(&bar_full[stv], ph, &abort_flag))) return;
+        if (!(ok = mbar_wait<ROWS>(&bar_full[stv], ph, &abort_flag))) return;
         if (++st == STAGES) {
           st = 0;
           ph ^= 1;
@@ -621,7 +625,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // at an item boundary S(u + 1) waits for the next item's Q: both PVs first
         const bool inter = has_next && nc > 0;
         for (int x = 0; x < 2; ++x) {
-          if (!(ok = mbar_wait(&bar_pfull[x], u & 1, &abort_flag))) return;
+          if (!(ok = mbar_wait<ROWS>(&bar_pfull[x], u & 1, &abort_flag))) return;
           tc_fence_after();
           for (int q = 0; q < npg; ++q) {
             // A = P in sub-group x's S columns: keys 64h .. 64h+63 as columns 64h .. 64h+31
@@ -635,14 +639,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           }
           if (!inter) continue;
           if (x == 0) {   // K(u + 1) only now: PV_0(u) does not need it
-            if (!(ok = mbar_wait(&bar_full[stk], phk, &abort_flag))) return;
+            if (!(ok = mbar_wait<ROWS>(&bar_full[stk], phk, &abort_flag))) return;
             tc_fence_after();
           }
           issue_s(ka, qb, x);
         }
         if (has_next && !inter) {
-          if (!(ok = mbar_wait(&bar_full[stk], phk, &abort_flag))) return;
-          if (!(ok = mbar_wait(&bar_qfull[qb], (nseq / kQBufs) & 1, &abort_flag))) return;
+          if (!(ok = mbar_wait<ROWS>(&bar_full[stk], phk, &abort_flag))) return;
+          if (!(ok = mbar_wait<ROWS>(&bar_qfull[qb], (nseq / kQBufs) & 1, &abort_flag))) return;
           tc_fence_after();
           issue_s(ka, qb, 0);
           issue_s(ka, qb, 1);
@@ -654,7 +658,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       };
       int seq = 0;
       Item cur, nxt;
-      ok = mbar_wait(&bar_ifull[0], 0, &abort_flag);
+      ok = mbar_wait<ROWS>(&bar_ifull[0], 0, &abort_flag);
       cur = s_item[0];
       if (ok && !cur.end) {
         int c = 0, u = 0;
@@ -669,7 +673,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           } else {
             nseq = seq + 1;
             const int rs = nseq % kItemRing;
-            if (!(ok = mbar_wait(&bar_ifull[rs], (nseq / kItemRing) & 1, &abort_flag))) break;
+            if (!(ok = mbar_wait<ROWS>(&bar_ifull[rs], (nseq / kItemRing) & 1, &abort_flag))) break;
             nxt = s_item[rs];
             has_next = !nxt.end;
           }
@@ -713,7 +717,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int u = 0, pe = 0, pair_ends = 0;
     for (int seq = 0; ok; ++seq) {
       const int rs = seq % kItemRing;
-      if (!(ok = mbar_wait_warp(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      if (!(ok = mbar_wait_warp<ROWS>(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
       const Item it = s_item[rs];
       mbar_arrive(&bar_iempty[rs]);   // the descriptor is in registers: its slot may be reused
       if (it.end) break;
@@ -723,7 +727,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       if constexpr (MASKED) lim = (i_row / p.mask_block + 1) * p.mask_block;
       float m_run = -CUDART_INF_F, l_run = 0.f;       // l_run: this half's sum
       for (int c = 0; c < it.n_chunks && ok; ++c, ++u) {
-        if (!(ok = mbar_wait_warp(&bar_sfull[x], u & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp<ROWS>(&bar_sfull[x], u & 1, &abort_flag))) break;
         tc_fence_after();
         const int key0 = it.t_begin + c * kTile;
         int nvalid = min(kTile, it.t_end - key0);
@@ -744,7 +748,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         s_hmax[pe & 1][x][half][n] = mx;
         mbar_arrive(&bar_pair[pq][pe & 1]);
-        if (!(ok = mbar_wait_warp(&bar_pair[pq][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp<ROWS>(&bar_pair[pq][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
         mx = fmaxf(s_hmax[pe & 1][x][0][n], s_hmax[pe & 1][x][1][n]);
         ++pe;
         // the running max moves only when the tile raises it by more than 2^kLazyRescale
@@ -778,7 +782,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (__any_sync(0xffffffffu, resc)) {
           // bring this warp's half of its rows of O to the new maxima once the previous
           // tile's PV is done
-          if (!(ok = mbar_wait_warp(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp<ROWS>(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1,
+                                          &abort_flag)))
+            break;
           tc_fence_after();
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -797,11 +803,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (c != it.n_chunks - 1) continue;
         // ---- epilogue of the item: this half of the row of O, divided by the row's sum or as
         // a split partial
-        if (!(ok = mbar_wait_warp(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp<ROWS>(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
         s_hsum[pair_ends & 1][x][half][n] = l_run;
         mbar_arrive(&bar_pair_end[pq]);
-        if (!(ok = mbar_wait_warp(&bar_pair_end[pq], pair_ends & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp<ROWS>(&bar_pair_end[pq], pair_ends & 1, &abort_flag))) break;
         const float l_row = s_hsum[pair_ends & 1][x][0][n] + s_hsum[pair_ends & 1][x][1][n];
         ++pair_ends;
         const bool live = r_item < p.rows_per_group && i_row < p.L;
@@ -868,7 +874,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int pcount = 0, u = 0, pe = 0, pair_ends = 0;   // pe, pair_ends: exchanges so far
     for (int seq = 0; ok; ++seq) {
       const int rs = seq % kItemRing;
-      if (!(ok = mbar_wait_warp(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      if (!(ok = mbar_wait_warp<ROWS>(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
       const Item it = s_item[rs];
       mbar_arrive(&bar_iempty[rs]);   // the descriptor is in registers: its slot may be reused
       if (it.end) break;
@@ -889,7 +895,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           const int sb = kSub == 1 ? (u & 1) : x;
           const uint32_t sph = kSub == 1 ? ((u >> 1) & 1) : (u & 1);
           const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(sb * N) + col0;
-          if (!(ok = mbar_wait_warp(&bar_sfull[sb], sph, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp<ROWS>(&bar_sfull[sb], sph, &abort_flag))) break;
           tc_fence_after();
           uint32_t r[64];
 #pragma unroll
@@ -917,7 +923,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     max32<true>(*reinterpret_cast<const uint32_t(*)[32]>(r + 32), 0, 0));
           s_hmax[pe & 1][0][half][n] = hmax;
           mbar_arrive(&bar_pair[q4][pe & 1]);
-          if (!(ok = mbar_wait_warp(&bar_pair[q4][pe & 1], (pe >> 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp<ROWS>(&bar_pair[q4][pe & 1], (pe >> 1) & 1,
+                                          &abort_flag)))
+            break;
           const float mx = fmaxf(s_hmax[pe & 1][0][0][n], s_hmax[pe & 1][0][1][n]);
           ++pe;
           // the running max moves only when the tile raises it by more than 2^kLazyRescale
@@ -954,7 +962,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           if (__any_sync(0xffffffffu, resc)) {
             // bring this warp's half of its rows of O to the new maxima once the previous
             // tile's PV is done
-            if (!(ok = mbar_wait_warp(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+            if (!(ok = mbar_wait_warp<ROWS>(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1,
+                                            &abort_flag)))
+              break;
             tc_fence_after();
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -981,7 +991,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (!ok || c != it.n_chunks - 1) continue;
         // ---- epilogue of the item: this half of each row of O, divided by the row's sum or
         // as a split partial
-        if (!(ok = mbar_wait_warp(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp<ROWS>(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
         const size_t grp = (static_cast<size_t>(it.b) * p.Hkv + it.kvh) * p.row_groups + it.rg;
         float* mine =
@@ -990,7 +1000,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         for (int x = 0; x < kSub; ++x) {
           s_hsum[pair_ends & 1][0][half][n] = l_run[x];
           mbar_arrive(&bar_pair_end[q4]);
-          if (!(ok = mbar_wait_warp(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp<ROWS>(&bar_pair_end[q4], pair_ends & 1, &abort_flag))) break;
           const float l_row = s_hsum[pair_ends & 1][0][0][n] + s_hsum[pair_ends & 1][0][1][n];
           ++pair_ends;
           const int r_item = x * N + n;   // row of the item
@@ -1053,7 +1063,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     int pcount = 0, u = 0;
     for (int seq = 0; ok; ++seq) {
       const int rs = seq % kItemRing;
-      if (!(ok = mbar_wait_warp(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
+      if (!(ok = mbar_wait_warp<ROWS>(&bar_ifull[rs], (seq / kItemRing) & 1, &abort_flag))) break;
       const Item it = s_item[rs];
       if (it.end) break;
 #pragma unroll
@@ -1063,7 +1073,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int j0 = c * p.chunk_tiles;
         const int j1 = min(it.n_tiles, j0 + p.chunk_tiles);
         const uint32_t tS = tmem + lane_off + static_cast<uint32_t>((u & 1) * p.chunk_tiles * N);
-        if (!(ok = mbar_wait_warp(&bar_sfull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp<ROWS>(&bar_sfull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
         // phase A: exact column maxima over the chunk
 #pragma unroll
@@ -1117,7 +1127,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const bool need = s_need[u & 1] != 0;
         if (c > 0 && need) {
           // rescale the running O^T columns (and l) to the new maxima
-          if (!(ok = mbar_wait_warp(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1, &abort_flag))) break;
+          if (!(ok = mbar_wait_warp<ROWS>(&bar_ofull[(u - 1) & 1], ((u - 1) >> 1) & 1,
+                                          &abort_flag)))
+            break;
           tc_fence_after();
 #pragma unroll
           for (int cg = 0; cg < N / 16; ++cg) {
@@ -1167,7 +1179,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
               }
             }
             const int pb = pcount & 1;
-            if (!(ok = mbar_wait_warp(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1, &abort_flag))) break;
+            if (!(ok = mbar_wait_warp<ROWS>(&bar_pempty[pb], ((pcount >> 1) & 1) ^ 1,
+                                            &abort_flag)))
+              break;
             uint8_t* pbuf = sP + pb * (N * 256) + (x >> 6) * (N * 128);
             const uint32_t xc = (x & 63) >> 3;
             const uint32_t xb = (x & 7) * 2;
@@ -1190,7 +1204,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_arrive(&bar_sfree[u & 1]);
         if (c != it.n_chunks - 1) continue;
         // ---- epilogue of the item
-        if (!(ok = mbar_wait_warp(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
+        if (!(ok = mbar_wait_warp<ROWS>(&bar_ofull[u & 1], (u >> 1) & 1, &abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int n = 0; n < N; ++n) {

@@ -50,29 +50,45 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// SUSPEND: a thread whose phase has not completed may be suspended for up to kSuspendHintNs (it
+// resumes as soon as the phase completes) rather than the hardware's default time, so that
+// fewer re-tries take issue slots from the other warps of an issue-bound kernel.
+constexpr uint32_t kSuspendHintNs = 20000;
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if constexpr (SUSPEND) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
 // Waits for phase `parity` of `bar` to complete.  Gives up after limit_ns (kWaitLimitNs unless
 // given), or as soon as another thread of the CTA has given up (*abort != 0); returns false
 // then, after setting *abort.  Callers stop issuing work once a wait has failed.
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<SUSPEND>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait<SUSPEND>(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
@@ -84,8 +100,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // mbar_wait called by all 32 lanes of a warp: the lanes agree on the outcome, so no lane goes
 // on to warp-collective instructions (tcgen05.ld, shuffles, __syncwarp) while another has
 // given up.
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+  return __all_sync(0xffffffffu, mbar_wait<SUSPEND>(bar, parity, abort));
 }
 
 // ------------------------------------------------------------------ proxies / barriers
