@@ -31,6 +31,10 @@
 //    sub-group Q is copied into tensor memory too (tcgen05.cp) and the ring has five stages;
 //    with two sub-groups (TWO, up to 256 rows) both share every K/V stage and sixteen softmax
 //    warps work on both at once.  The block-causal prefill mask (MASKED) applies per row.
+//    These kernels cut a sequence into equal splits (each item reloads Q and writes a large
+//    partial, so no split is a short remainder), hand the items out longest splits first,
+//    stage the epilogue's stores through shared memory (whole 128-byte rows per store
+//    instruction), and wait with a suspend-time hint (fewer re-tries taking issue slots).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
