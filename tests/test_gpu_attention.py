@@ -165,15 +165,23 @@ def test_rows_on_m_rescale_after_a_sharp_key(lib, L):
     check(lib, a)
 
 
-def test_prefill_chunk_across_a_split_boundary(lib):
-    """Block prefill whose cached prefix ends just before a 2048-token KV split boundary: in
-    the chunk that straddles it, the queries of the first blocks see no key of the second
-    split (their partial is empty: max -inf, sum 0) and the merge must ignore it."""
+@pytest.mark.parametrize("Hq,lens", [
+    # 256 query rows per KV head (two sub-groups): KV 126977 is cut into 32 even splits of 4096
+    # tokens, the last of which holds only the chunk's last token
+    (32, [126913]),
+    # 128 rows (one sub-group): KV 70657 / 70684, 24 splits of 3072, the last holding 1 / 28
+    # tokens of the chunk
+    (16, [70593, 70620]),
+])
+def test_prefill_chunk_across_a_split_boundary(lib, Hq, lens):
+    """Block prefill whose chunk straddles a KV split boundary: the queries of the chunk's first
+    blocks see no key of the last split (their partial is empty: max -inf, sum 0) and the
+    merge must ignore it."""
     import torch
     from gpu_util import host
-    rng = np.random.default_rng(2048)
-    B, L, Hq, Hkv, n = 2, 4, 32, 8, 64
-    lens = np.array([2040, 2028])
+    rng = np.random.default_rng(2048 + Hq)
+    B, L, Hkv, n = len(lens), 4, 8, 64
+    lens = np.array(lens)
     a = W.make_attention(rng, B, n, Hq, Hkv, 128, prefix_lens=lens, poison=False)
     q = W._normal_bf16(rng, (B, n, Hq, 128), 0.5)
     kn = W._normal_bf16(rng, (B, n, Hkv, 128), 0.5)
